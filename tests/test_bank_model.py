@@ -1,0 +1,101 @@
+"""Pins for the oracle's shared-memory bank model (CPU only).
+
+Against the examples the pages print (tests/golden/bank_examples.txt), the
+gcd law stated on the bank page ("四种访问，四种结果": a full-warp scalar read
+with stride s touches 32/gcd(s,32) banks with conflict degree gcd(s,32)),
+the +1-padding and XOR-swizzle layouts of "多一列" / "Padding 之外的选择",
+and the footprint example of "放进矩阵转置里看".
+"""
+import math
+import os
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _golden():
+    out = []
+    with open(os.path.join(HERE, "golden", "bank_examples.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, rhs = line.split("=")
+            tag, kind, *args = lhs.split()
+            out.append((tag, kind, " ".join(args), [int(x) for x in rhs.split()]))
+    return out
+
+
+def _eval_index(expr, lane):
+    return eval(expr, {"__builtins__": {}}, {"lane": lane})
+
+
+def test_golden_bank_examples(oracle_lib):
+    cases = _golden()
+    assert len(cases) >= 25
+    for tag, kind, arg, expect in cases:
+        if kind == "bank":
+            assert oracle_lib.bank_of(int(arg)) == expect[0], (tag, arg)
+        else:
+            addrs = [4 * _eval_index(arg, l) for l in range(32)]
+            r = oracle_lib.shared_request(addrs, 4)
+            banks = {oracle_lib.bank_of(a) for a in addrs}
+            assert (r["degree"], len(banks)) == tuple(expect), (tag, arg, r)
+
+
+@pytest.mark.parametrize("stride", range(1, 65))
+def test_gcd_law(oracle_lib, stride):
+    for base in (0, 5):
+        addrs = [4 * (base + l * stride) for l in range(32)]
+        r = oracle_lib.shared_request(addrs, 4)
+        g = math.gcd(stride, 32)
+        assert r["degree"] == g
+        assert len({oracle_lib.bank_of(a) for a in addrs}) == 32 // g
+
+
+def test_padded_tile_rows_and_columns(oracle_lib):
+    # tile[32][33]: bank = (row + col) % 32, row and column reads conflict-free
+    for c in range(32):
+        col = [4 * (r * 33 + c) for r in range(32)]
+        assert oracle_lib.shared_request(col, 4)["degree"] == 1
+        assert [oracle_lib.bank_of(a) for a in col] == [(r + c) % 32 for r in range(32)]
+    for r in range(32):
+        row = [4 * (r * 33 + c) for c in range(32)]
+        assert oracle_lib.shared_request(row, 4)["degree"] == 1
+    # tile[32][32]: column reads are 32-way
+    assert oracle_lib.shared_request([4 * (r * 32 + 3) for r in range(32)], 4)["degree"] == 32
+    # footprint: 32*32*4 = 4096 B vs 32*33*4 = 4224 B (+128 B)
+    assert 32 * 32 * 4 == 4096 and 32 * 33 * 4 == 4224
+
+
+def test_xor_swizzle_is_conflict_free_both_ways(oracle_lib):
+    phys = lambda r, c: 4 * (r * 32 + (c ^ r))
+    for r in range(32):
+        assert sorted((c ^ r) for c in range(32)) == list(range(32))
+        assert oracle_lib.shared_request([phys(r, c) for c in range(32)], 4)["degree"] == 1
+    for c in range(32):
+        assert oracle_lib.shared_request([phys(r, c) for r in range(32)], 4)["degree"] == 1
+
+
+def test_wide_accesses(oracle_lib):
+    # 32 lanes reading consecutive float4: 128 distinct words -> 4 passes, all needed
+    r = oracle_lib.shared_request([16 * l for l in range(32)], 16)
+    assert (r["wavefronts"], r["ideal"], r["distinct"]) == (4, 4, 128)
+    # every lane reading the same float4: broadcast, 1 pass
+    r = oracle_lib.shared_request([48] * 32, 16)
+    assert (r["wavefronts"], r["ideal"]) == (1, 1)
+    # 8 distinct float4 covering 128 contiguous bytes, each read by 4 lanes: 1 pass
+    r = oracle_lib.shared_request([16 * (l % 8) for l in range(32)], 16)
+    assert (r["wavefronts"], r["ideal"]) == (1, 1)
+    # float4 reads 512 B apart (stride 128 floats): same 4 banks, 32 distinct chunks
+    r = oracle_lib.shared_request([512 * l for l in range(32)], 16)
+    assert r["wavefronts"] == 32 and r["ideal"] == 4
+    # doubles (8 B): consecutive -> 2 passes, no excess
+    r = oracle_lib.shared_request([8 * l for l in range(32)], 8)
+    assert (r["wavefronts"], r["ideal"]) == (2, 2)
+    # inactive lanes do not count
+    r = oracle_lib.shared_request([4 * 32 * l for l in range(32)], 4, active=[1] + [0] * 31)
+    assert r["degree"] == 1
+    with pytest.raises(ValueError):
+        oracle_lib.shared_request([2], 4)
