@@ -1,0 +1,346 @@
+#!/usr/bin/env python
+"""Benchmark of the tiled FP32 matrix multiply C = A.B on GB300.
+
+One step = one sgemm_f32 call over the workload (the whole path: argument
+checks, one kernel launch with the copy pipeline, FMA main loop and epilogue).
+Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference]
+
+Timing: inputs resident in HBM; before every timed step the L2 is flushed by
+writing a 256 MiB buffer (outside the step's events); each step is bracketed
+by CUDA events on the launching stream.  ms_per_step is the mean over the K
+steps, max over ranks.  N > 1 runs independent replicas (one full product per
+GPU, no collective on the data path): value = total FLOP / max time.
+
+--impl reference times the FP64 CPU oracle (the only baseline this path has)
+on the host cores, each step a bounded row-block sample of the same product.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP32 GEMM TFLOP/s at M=N=K=4096 and % of GB300 FP32 CUDA-core peak"
+FMA_PER_CLK_PER_SM = 128  # FP32 CUDA-core lanes per SM (4 partitions x 32)
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def _measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {}
+
+
+def _workload(name):
+    from dense_fp32_tiled_gb300 import synth
+    return synth.WORKLOADS[name or synth.HEADLINE]
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+    Q = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.uuid and parts[0] != self.uuid:
+                    continue
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        # samples taken while the GPU was busy: power well above idle
+        busy = [s for s, p in zip(sm, pw)] if pw else sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(rows)}
+
+
+def _traffic_from_profile(stamp: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel as built now (same source stamp); else None."""
+    p = os.path.join(ROOT, "profiles", "sgemm_f32_tiled_4096.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if line.startswith("<!-- bench:"):
+                for kv in line.strip()[len("<!-- bench:"):-3].split():
+                    k, _, v = kv.partition("=")
+                    vals[k] = v
+    if vals.get("source_stamp") == stamp and "dram_bytes_per_launch" in vals:
+        return int(vals["dram_bytes_per_launch"])
+    return None
+
+
+def cpu_baseline(w, seconds: float):
+    """Time the FP64 oracle as it stands on a row-block sample of the product."""
+    import numpy as np
+    import oracle
+    from dense_fp32_tiled_gb300 import synth
+    oracle.build()
+    A = synth.matrix(w.M, w.K, w.seed, w.ids[0], w.kind, w.sigma)
+    B = synth.matrix(w.K, w.N, w.seed, w.ids[1], w.kind, w.sigma)
+    probe = max(1, min(w.M, 8))
+    t0 = time.perf_counter()
+    oracle.gemm(A[:probe], B, with_abs=False)
+    t_probe = time.perf_counter() - t0
+    rows = int(max(1, min(w.M, probe * seconds / max(t_probe, 1e-6))))
+    t0 = time.perf_counter()
+    oracle.gemm(A[:rows], B, with_abs=False)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} product (all N, all K), FP64 "
+                      f"i-k-j loops, {dt:.1f} s"}, rows
+
+
+def run_reference(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from dense_fp32_tiled_gb300 import synth
+    w = _workload(a.workload)
+    oracle.build()
+    A = synth.matrix(w.M, w.K, w.seed, w.ids[0], w.kind, w.sigma)
+    B = synth.matrix(w.K, w.N, w.seed, w.ids[1], w.kind, w.sigma)
+    total_budget = 150.0
+    per_step = total_budget / max(1, a.steps + a.warmup)
+    probe = max(1, min(w.M, 4))
+    t0 = time.perf_counter()
+    oracle.gemm(A[:probe], B, with_abs=False)
+    t_probe = time.perf_counter() - t0
+    rows = int(max(1, min(w.M, probe * per_step / max(t_probe, 1e-6))))
+    for _ in range(a.warmup):
+        oracle.gemm(A[:rows], B, with_abs=False)
+    times = []
+    for _ in range(a.steps):
+        t0 = time.perf_counter()
+        oracle.gemm(A[:rows], B, with_abs=False)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    flops = 2.0 * rows * w.N * w.K
+    value = flops / (ms / 1e3) / 1e12
+    sample = f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} product per step (all N, all K)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, a.gpus, "host cores, no L2 flush"),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def _config(w, n, l2):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "lda": w.lda, "ldb": w.ldb, "ldc": w.ldc,
+            "inputs": f"{w.kind}{'' if w.kind != 'normal' else f'(0,{w.sigma})'} seed {w.seed}",
+            "l2": l2, "parallelism": "replicas" if n > 1 else "single GPU"}
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+        return
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from dense_fp32_tiled_gb300 import build as lib_build
+    if rank == 0:
+        lib_build.build()
+    if world > 1:
+        dist.barrier()
+    import dense_fp32_tiled_gb300 as sg
+    from dense_fp32_tiled_gb300 import synth
+    sg.load_library()
+
+    w = _workload(a.workload)
+    dev = torch.device("cuda", local)
+    A_h, B_h = w.inputs(ld_buffers=True)
+    A = torch.from_numpy(A_h).to(dev)
+    B = torch.from_numpy(B_h).to(dev)
+    c_elems = (w.M - 1) * w.ldc + w.N
+    C = torch.empty(c_elems, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+
+    def step():
+        st = sg.sgemm_f32(w.M, w.N, w.K, A.data_ptr(), w.lda, B.data_ptr(), w.ldb, C.data_ptr(), w.ldc, s)
+        if st != 0:
+            raise sg.SgemmError(st)
+
+    for _ in range(a.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    with ClockSampler(uuid) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter()
+        for i in range(a.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        t_wall = time.perf_counter() - t_wall
+    times = [st.elapsed_time(en) for st, en in zip(starts, ends)]
+    ms = statistics.mean(times)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    flops = float(w.flops)
+    value = world * flops / (ms / 1e3) / 1e12
+    clocks = clk.summary()
+
+    # ---- end to end: pinned host inputs -> device -> product -> host result
+    e2e = None
+    if not a.no_e2e:
+        hA = torch.from_numpy(A_h).pin_memory()
+        hB = torch.from_numpy(B_h).pin_memory()
+        hC = torch.empty(c_elems, dtype=torch.float32).pin_memory()
+        e_steps = max(3, a.steps // 2)
+        for _ in range(2):
+            A.copy_(hA, non_blocking=True); B.copy_(hB, non_blocking=True); step()
+            hC.copy_(C, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            A.copy_(hA, non_blocking=True)
+            B.copy_(hB, non_blocking=True)
+            step()
+            hC.copy_(C, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1) / e_steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * flops / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(A_h.nbytes + B_h.nbytes), "d2h_bytes_per_step": int(c_elems * 4),
+               "ms_per_step": e_ms}
+
+    # ---- roofline: FP32 FMA pipe of all SMs
+    peaks = _measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz") or clocks.get("sm_max_mhz") or 2070.0)
+    sms = props.multi_processor_count
+    peak = sms * FMA_PER_CLK_PER_SM * 2 * sm_max * 1e6 / 1e12
+    achieved = flops / (ms / 1e3) / 1e12 if world == 1 else value / world
+    roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": _traffic_from_profile(_stamp()),
+                "peak_basis": f"{sms} SMs x 128 FP32 FMA/clk x 2 FLOP x {sm_max:.0f} MHz (max SM clock)"}
+    if clocks.get("sm_mhz"):
+        roofline["frac_at_sampled_clock"] = achieved / (peak * clocks["sm_mhz"] / sm_max)
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu, _ = cpu_baseline(w, a.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
+                "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": _config(w, world, "flushed before every timed step (256 MiB write, outside the events)"),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": a.steps,
+                "clocks": clocks, "pct_of_fp32_peak": 100.0 * achieved / peak,
+                "ms_min": min(times), "ms_max": max(times), "wall_s_timed_region": t_wall}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _stamp():
+    from dense_fp32_tiled_gb300 import build as lib_build
+    return lib_build._stamp()
+
+
+if __name__ == "__main__":
+    main()

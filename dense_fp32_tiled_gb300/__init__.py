@@ -1,0 +1,11 @@
+"""GB300-native tiled FP32 matrix multiply C = A.B (sm_103a CUDA, C ABI).
+
+``sgemm(A, B)`` multiplies CUDA float32 tensors through the C-ABI library
+``libsgemm_f32.so`` (built by ``dense_fp32_tiled_gb300.build.build()``);
+``sgemm_f32(...)`` is the raw C call on device addresses.
+"""
+from ._binding import (SGEMM_OK, SgemmError, declared_functions, load_library, sgemm, sgemm_f32,
+                       smem_request, smem_shape, status_string)
+
+__all__ = ["SGEMM_OK", "SgemmError", "declared_functions", "load_library", "sgemm", "sgemm_f32",
+           "smem_request", "smem_shape", "status_string"]

@@ -1,0 +1,123 @@
+"""ctypes binding of libsgemm_f32.so: argument marshalling only.
+
+Every arithmetic step runs in the CUDA library.  PyTorch is used only for
+device memory, strides and the current stream.  There is no fallback: if the
+library is missing or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsgemm_f32.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "sgemm_f32.h")
+
+SGEMM_OK = 0
+_lib = None
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, status: int, what: str = "sgemm_f32"):
+        self.status = status
+        super().__init__(f"{what} failed with status {status}: {status_string(status)}")
+
+
+def load_library():
+    """Load libsgemm_f32.so from the package directory (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"CUDA library {LIB_PATH} is not built; run dense_fp32_tiled_gb300.build.build() "
+            "(or __graft_entry__.build()) first")
+    lib = ctypes.CDLL(LIB_PATH)
+    i32, p, i64p = ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64)
+    lib.sgemm_f32.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p]
+    lib.sgemm_f32.restype = i32
+    lib.sgemm_f32_status_string.argtypes = [i32]
+    lib.sgemm_f32_status_string.restype = ctypes.c_char_p
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.sgemm_f32_smem_shape.argtypes = [i32, ip, ip, ip]
+    lib.sgemm_f32_smem_shape.restype = i32
+    lib.sgemm_f32_smem_request.argtypes = [i32, i32, i32, i32, i64p, ip]
+    lib.sgemm_f32_smem_request.restype = i32
+    _lib = lib
+    return lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/sgemm_f32.h declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sgemm_f32\w*)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return load_library().sgemm_f32_status_string(int(status)).decode()
+
+
+def sgemm_f32(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+              stream: int = 0) -> int:
+    """Raw C-ABI call with integer device addresses; returns the status code."""
+    return load_library().sgemm_f32(int(M), int(N), int(K), ctypes.c_void_p(int(A) or None), int(lda),
+                                    ctypes.c_void_p(int(B) or None), int(ldb),
+                                    ctypes.c_void_p(int(C) or None), int(ldc),
+                                    ctypes.c_void_p(int(stream) or None))
+
+
+def smem_shape(kind: int):
+    nw, ns, nst = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    st = load_library().sgemm_f32_smem_shape(kind, ctypes.byref(nw), ctypes.byref(ns), ctypes.byref(nst))
+    if st != SGEMM_OK:
+        raise SgemmError(st, "sgemm_f32_smem_shape")
+    return nw.value, ns.value, nst.value
+
+
+def smem_request(kind: int, warp: int, step: int, stage: int = 0):
+    """(byte offsets of the 32 lanes, width in bytes) of one shared-memory access."""
+    out = (ctypes.c_int64 * 32)()
+    width = ctypes.c_int()
+    st = load_library().sgemm_f32_smem_request(kind, warp, step, stage, out, ctypes.byref(width))
+    if st != SGEMM_OK:
+        raise SgemmError(st, "sgemm_f32_smem_request")
+    return list(out), width.value
+
+
+def _matrix_args(t, rows: int, cols: int, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if t.dim() != 2 or tuple(t.shape) != (rows, cols):
+        raise ValueError(f"{name} must have shape ({rows}, {cols}), got {tuple(t.shape)}")
+    if cols > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major with unit column stride")
+    ld = t.stride(0) if rows > 1 else max(1, cols)
+    return t.data_ptr(), max(ld, cols, 1)
+
+
+def sgemm(A, B, out=None, stream=None):
+    """C = A @ B for CUDA float32 tensors (row-major, any row stride) via sgemm_f32.
+
+    ``out`` (M x N, row-major) is written when given, else allocated.  Runs on
+    ``stream`` (a torch.cuda.Stream) or the current stream; asynchronous.
+    """
+    import torch
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shape mismatch: {tuple(A.shape)} @ {tuple(B.shape)}")
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    a, lda = _matrix_args(A, M, K, "A")
+    b, ldb = _matrix_args(B, K, N, "B")
+    c, ldc = _matrix_args(out, M, N, "out")
+    s = (stream or torch.cuda.current_stream(A.device)).cuda_stream
+    with torch.cuda.device(A.device):
+        st = sgemm_f32(M, N, K, a, lda, b, ldb, c, ldc, s)
+    if st != SGEMM_OK:
+        raise SgemmError(st)
+    return out

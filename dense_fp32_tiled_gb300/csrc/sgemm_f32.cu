@@ -1,0 +1,371 @@
+// sgemm_f32.cu -- tiled FP32 matrix multiply C = A.B for GB300 (sm_103a),
+// and its C ABI (declared in include/sgemm_f32.h).
+//
+// Data path (vectorised-load page, "这一篇放进 GEMM 路径里看"):
+//   global --(cp.async, coalesced, 16/8/4-byte by alignment class)-->
+//   shared (k-major swizzled A tile, row-major B tile, STAGES-deep ring) -->
+//   registers (two 128-bit reads of A and two of B per k) -->
+//   8 x 8 register tile of FP32 FMAs --> guarded, vectorised stores of C.
+//
+// * Tiling: a CTA computes a BM x BN = 128 x 128 tile of C, walking K in
+//   BK = 16 slices (shared-memory page, "register tiling 在干什么": each value
+//   read from shared memory feeds 8 FMAs, (8+8)/64 = 0.25 reads per FMA).
+// * Warp-level reuse: the 32 lanes of a warp form a 4 x 8 grid over a
+//   32 x 64 warp tile; the 8 lanes of a row read the same A group (one word
+//   per bank, broadcast) and the 4 lanes of a column the same B group
+//   ("广播不是 bank conflict").
+// * Transpose on store: A (row-major, k contiguous) is written k-major so a
+//   thread's 4 consecutive rows are one 128-bit read ("shared memory transpose
+//   的基本想法"); a 16-byte copy cannot split a vector across rows, so A moves
+//   in 4-byte copies, spread over banks by the XOR swizzle in smem_layout.cuh.
+// * Edges ("边界处理会破坏漂亮形状"): copies past M, N or K are issued with a
+//   zero source size, which fills shared memory with 0; stores are guarded.
+//   Misaligned leading dimensions ("对齐也要从数据分配开始") select 8- or
+//   4-byte B copies and C stores instead of 16-byte ones.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "sgemm_f32.h"
+#include "smem_layout.cuh"
+
+namespace {
+
+using namespace sg;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// cp.async with an explicit source size: bytes beyond `src_bytes` are
+// written as zero in shared memory and not read from global memory.
+template <int BYTES>
+__device__ __forceinline__ void cp_async(uint32_t dst, const float *src, uint32_t src_bytes) {
+    if constexpr (BYTES == 16) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                     : "memory");
+    } else if constexpr (BYTES == 8) {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                     : "memory");
+    } else {
+        static_assert(BYTES == 4, "copy width");
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                     : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int PENDING>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(PENDING) : "memory");
+}
+
+// One CTA: C tile (tm, tn).  VB = B copy width in floats (4, 2 or 1).
+// vc = C store width in floats (4, 2 or 1), uniform over the grid.
+template <int VB>
+__global__ void __launch_bounds__(NT, 2)
+sgemm_f32_tiled_kernel(const int M, const int N, const int K,
+                       const float *__restrict__ A, const int lda,
+                       const float *__restrict__ B, const int ldb,
+                       float *__restrict__ C, const int ldc,
+                       const int tiles_m, const int tiles_n, const int vc) {
+    extern __shared__ __align__(128) float smem[];
+    const int tid = threadIdx.x;
+    int tm, tn;
+    tile_of(blockIdx.x, tiles_m, tiles_n, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN;
+    const int KT = (K + BK - 1) / BK;
+    const bool k_tail = (K % BK) != 0;
+    const uint32_t sbase = smem_u32(smem);
+
+    // ---- A copy set-up: 8 copies, two rows (q >> 2), four k groups (q & 3)
+    int a_kk, a_m[2];
+    {
+        int k, m;
+        a_copy_coord(tid, 0, k, m);
+        a_kk = k;
+        a_m[0] = m;
+        a_copy_coord(tid, 4, k, m);
+        a_m[1] = m;
+    }
+    const float *a_row[2];
+    uint32_t a_bytes[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int row = m0 + a_m[h];
+        const bool ok = row < M;
+        a_row[h] = A + static_cast<size_t>(ok ? row : 0) * lda;
+        a_bytes[h] = ok ? 4u : 0u;
+    }
+
+    // ---- B copy set-up
+    constexpr int NB = b_copies<VB>();
+    int b_k0, b_n;
+    b_copy_coord<VB>(tid, 0, b_k0, b_n);
+
+    const int b_col = n0 + b_n;
+    const int b_valid = N - b_col;       // valid floats from b_col on
+    const uint32_t b_bytes = b_valid >= VB ? VB * 4u : (b_valid > 0 ? b_valid * 4u : 0u);
+    const float *b_colp = B + (b_valid > 0 ? b_col : 0);
+
+    auto load_tile = [&](int kt, int stage) {
+        const uint32_t st = sbase + stage * (STAGE_FLOATS * 4);
+        const int kb = kt * BK;
+        const bool tail = k_tail && (kt == KT - 1);
+#pragma unroll
+        for (int q = 0; q < A_COPIES; ++q) {
+            int k, m;
+            a_copy_coord(tid, q, k, m);
+            const float *src = a_row[q >> 2] + kb + k;
+            uint32_t bytes = a_bytes[q >> 2];
+            if (tail && kb + k >= K) {
+                src = a_row[q >> 2] + kb;
+                bytes = 0;
+            }
+            cp_async<4>(st + as_word(k, m) * 4, src, bytes);
+        }
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+            int k, n;
+            b_copy_coord<VB>(tid, q, k, n);
+            const int kg = kb + k;
+            const float *src = b_colp + static_cast<size_t>(kg) * ldb;
+            uint32_t bytes = b_bytes;
+            if (tail && kg >= K) {
+                src = B;
+                bytes = 0;
+            }
+            cp_async<VB * 4>(st + bs_word(k, n) * 4, src, bytes);
+        }
+
+    };
+
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+
+    const int ra = frag_row0(tid);
+    const int cb = frag_col0(tid);
+
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < KT) load_tile(s, s);
+        cp_async_commit();
+    }
+
+    for (int kt = 0; kt < KT; ++kt) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();  // tile kt visible to all; stage (kt-1) free again
+        const int nk = kt + STAGES - 1;
+        if (nk < KT) load_tile(nk, nk % STAGES);
+        cp_async_commit();
+
+        const float *st = smem + (kt % STAGES) * STAGE_FLOATS;
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(st + as_word(k, ra));
+            const float4 a1 = *reinterpret_cast<const float4 *>(st + as_word(k, ra + 16));
+            const float4 b0 = *reinterpret_cast<const float4 *>(st + bs_word(k, cb));
+            const float4 b1 = *reinterpret_cast<const float4 *>(st + bs_word(k, cb + 32));
+            const float a[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float b[TN] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+    }
+    cp_async_wait<0>();
+
+    // ---- epilogue: guarded stores, vectorised where the C class allows
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int row = m0 + frag_row(tid, i);
+        if (row >= M) continue;
+        float *crow = C + static_cast<size_t>(row) * ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = n0 + cb + 32 * h;
+            const float *v = &acc[i][4 * h];
+            if (col + 3 < N && vc == 4) {
+                *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
+            } else if (col + 3 < N && vc == 2) {
+                *reinterpret_cast<float2 *>(crow + col) = make_float2(v[0], v[1]);
+                *reinterpret_cast<float2 *>(crow + col + 2) = make_float2(v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (col + e < N) crow[col + e] = v[e];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+int g_device_state[kMaxDevices];  // 0 = not yet set up, 1 = ready, <0 = status
+
+int setup_device(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_device_state[dev] != 0) return g_device_state[dev] > 0 ? SGEMM_OK : g_device_state[dev];
+    int major = 0, minor = 0;
+    int st = SGEMM_OK;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        major != 10 || minor != 3) {
+        st = SGEMM_ERR_DEVICE;
+    } else {
+        const void *kernels[] = {reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<4>),
+                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<2>),
+                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<1>)};
+        for (const void *k : kernels) {
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
+                st = SGEMM_ERR_DEVICE;
+                break;
+            }
+        }
+    }
+    if (st != SGEMM_OK) (void)cudaGetLastError();  // do not leave our failure sticky for the caller
+    g_device_state[dev] = st == SGEMM_OK ? 1 : st;
+    return st;
+}
+
+// Largest v in {4, 2, 1} floats such that the pointer and every row start are
+// 4*v-byte aligned.
+int vector_class(const void *p, long long ld) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    if (a % 16 == 0 && ld % 4 == 0) return 4;
+    if (a % 8 == 0 && ld % 2 == 0) return 2;
+    return 1;
+}
+
+bool ranges_overlap(const void *p, long long p_elems, const void *q, long long q_elems) {
+    if (p_elems <= 0 || q_elems <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + static_cast<uintptr_t>(p_elems) * 4;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(q), b1 = b0 + static_cast<uintptr_t>(q_elems) * 4;
+    return a0 < b1 && b0 < a1;
+}
+
+long long extent(long long rows, long long cols, long long ld) {
+    return (rows == 0 || cols == 0) ? 0 : (rows - 1) * ld + cols;
+}
+
+template <int VB>
+cudaError_t launch(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                   int tiles_m, int tiles_n, int vc, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles_m * tiles_n));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, sgemm_f32_tiled_kernel<VB>, M, N, K, A, lda, B, ldb, C, ldc, tiles_m,
+                              tiles_n, vc);
+}
+
+}  // namespace
+
+extern "C" int sgemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                         cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_LD;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (C == nullptr) return SGEMM_ERR_NULL_PTR;
+    if (K > 0 && (A == nullptr || B == nullptr)) return SGEMM_ERR_NULL_PTR;
+    if (reinterpret_cast<uintptr_t>(C) % 4 != 0) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && (reinterpret_cast<uintptr_t>(A) % 4 != 0 || reinterpret_cast<uintptr_t>(B) % 4 != 0))
+        return SGEMM_ERR_INVALID_ARG;
+    const long long c_ext = extent(M, N, ldc);
+    if (K > 0 && (ranges_overlap(C, c_ext, A, extent(M, K, lda)) || ranges_overlap(C, c_ext, B, extent(K, N, ldb))))
+        return SGEMM_ERR_ALIAS;
+    const long long tiles_m = (static_cast<long long>(M) + BM - 1) / BM;
+    const long long tiles_n = (static_cast<long long>(N) + BN - 1) / BN;
+    if (tiles_m * tiles_n > INT_MAX) return SGEMM_ERR_INVALID_DIM;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_DEVICE;
+    }
+    const int st = setup_device(dev);
+    if (st != SGEMM_OK) return st;
+
+    const int vb = K > 0 ? vector_class(B, ldb) : 4;
+    const int vc = vector_class(C, ldc);
+    cudaError_t err;
+    switch (vb) {
+        case 4: err = launch<4>(M, N, K, A, lda, B, ldb, C, ldc, (int)tiles_m, (int)tiles_n, vc, stream); break;
+        case 2: err = launch<2>(M, N, K, A, lda, B, ldb, C, ldc, (int)tiles_m, (int)tiles_n, vc, stream); break;
+        default: err = launch<1>(M, N, K, A, lda, B, ldb, C, ldc, (int)tiles_m, (int)tiles_n, vc, stream); break;
+    }
+    if (err != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
+}
+
+extern "C" const char *sgemm_f32_status_string(int status) {
+    switch (status) {
+        case SGEMM_OK: return "success";
+        case SGEMM_ERR_INVALID_DIM: return "invalid dimension (negative M, N or K, or too many tiles)";
+        case SGEMM_ERR_INVALID_LD: return "invalid leading dimension (lda < max(1,K), ldb or ldc < max(1,N))";
+        case SGEMM_ERR_NULL_PTR: return "null pointer for a non-empty matrix";
+        case SGEMM_ERR_ALIAS: return "C overlaps A or B";
+        case SGEMM_ERR_LAUNCH: return "kernel launch rejected by the CUDA runtime";
+        case SGEMM_ERR_DEVICE: return "current device is not sm_103 or its set-up failed";
+        case SGEMM_ERR_INVALID_ARG: return "invalid argument (misaligned pointer or out-of-range value)";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n_stages) {
+    int steps;
+    switch (kind) {
+        case 0: steps = A_COPIES; break;
+        case 1: steps = b_copies<4>(); break;
+        case 2:
+        case 3: steps = 2 * BK; break;
+        case 4: steps = b_copies<2>(); break;
+        case 5: steps = b_copies<1>(); break;
+        default: return SGEMM_ERR_INVALID_ARG;
+    }
+    if (n_warps) *n_warps = NT / 32;
+    if (n_steps) *n_steps = steps;
+    if (n_stages) *n_stages = STAGES;
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_f32_smem_request(int kind, int warp, int step, int stage, int64_t byte_offset[32],
+                                      int *width_bytes) {
+    int n_warps, n_steps, n_stages;
+    if (sgemm_f32_smem_shape(kind, &n_warps, &n_steps, &n_stages) != SGEMM_OK) return SGEMM_ERR_INVALID_ARG;
+    if (warp < 0 || warp >= n_warps || step < 0 || step >= n_steps || stage < 0 || stage >= n_stages ||
+        byte_offset == nullptr)
+        return SGEMM_ERR_INVALID_ARG;
+    int width = 16;
+    for (int lane = 0; lane < 32; ++lane) {
+        const int tid = warp * 32 + lane;
+        int word = 0, k = 0, x = 0;
+        switch (kind) {
+            case 0: a_copy_coord(tid, step, k, x); word = as_word(k, x); width = 4; break;
+            case 1: b_copy_coord<4>(tid, step, k, x); word = bs_word(k, x); width = 16; break;
+            case 4: b_copy_coord<2>(tid, step, k, x); word = bs_word(k, x); width = 8; break;
+            case 5: b_copy_coord<1>(tid, step, k, x); word = bs_word(k, x); width = 4; break;
+            case 2: word = as_word(step >> 1, frag_row0(tid) + 16 * (step & 1)); width = 16; break;
+            case 3: word = bs_word(step >> 1, frag_col0(tid) + 32 * (step & 1)); width = 16; break;
+        }
+        byte_offset[lane] = (static_cast<int64_t>(stage) * STAGE_FLOATS + word) * 4;
+    }
+    if (width_bytes) *width_bytes = width;
+    return SGEMM_OK;
+}

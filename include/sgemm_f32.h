@@ -1,0 +1,105 @@
+/*
+ * sgemm_f32.h -- C ABI of the GB300 (sm_103a) tiled FP32 matrix multiply.
+ *
+ * Operation (the textbook product the tiled kernel computes; page
+ * "CUDA 深入浅出（五）: Vectorized Load 和 Shared Memory Layout", section
+ * "这一篇放进 GEMM 路径里看"):
+ *
+ *     C[i*ldc + j] = sum_{k<K} A[i*lda + k] * B[k*ldb + j]
+ *                    for 0 <= i < M, 0 <= j < N,
+ *
+ * with FP32 inputs, FP32 fused multiply-adds and an FP32 result.  lda, ldb
+ * and ldc are row strides in elements (same page, section
+ * "对齐也要从数据分配开始": the leading dimension fixes where each row starts,
+ * and with it which rows allow 16-byte vector access).  C is overwritten;
+ * there is no alpha/beta scaling and no transposed-operand mode.  Rounding:
+ * IEEE round-to-nearest FMA, denormals kept; the summation order over k is
+ * unspecified, so results agree with an exact dot product to FP32 rounding,
+ * not bit for bit with another order.
+ *
+ * All functions are thread-safe.  None allocates device memory.
+ */
+#ifndef SGEMM_F32_H
+#define SGEMM_F32_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_DIM = -1,  /* M, N or K negative, or the tile grid too large */
+    SGEMM_ERR_INVALID_LD = -2,   /* lda < max(1,K), ldb < max(1,N) or ldc < max(1,N) */
+    SGEMM_ERR_NULL_PTR = -3,     /* a pointer is NULL although its matrix is not empty */
+    SGEMM_ERR_ALIAS = -4,        /* C's address range overlaps A's or B's */
+    SGEMM_ERR_LAUNCH = -5,       /* the kernel launch was rejected by the runtime */
+    SGEMM_ERR_DEVICE = -6,       /* current device is not sm_103 or its set-up failed */
+    SGEMM_ERR_INVALID_ARG = -7   /* any other out-of-range argument */
+} sgemm_status;
+
+/*
+ * sgemm_f32 -- enqueue C = A.B on `stream`.
+ *
+ *   M, N, K : sizes; A is M x K, B is K x N, C is M x N.  Each >= 0.
+ *   A, lda  : DEVICE pointer to row-major A, row i at A + i*lda; lda >= max(1,K).
+ *   B, ldb  : DEVICE pointer to row-major B, row k at B + k*ldb; ldb >= max(1,N).
+ *   C, ldc  : DEVICE pointer to row-major C, row i at C + i*ldc; ldc >= max(1,N).
+ *             Elements between N and ldc in each row are not touched.
+ *   stream  : CUDA stream of the current device (0 = legacy default stream).
+ *
+ * Any pointer alignment (a multiple of 4 bytes) is accepted: the library
+ * picks 16-, 8- or 4-byte copy widths from the alignment of each pointer and
+ * its row stride.  The caller owns all memory; A and B are only read, C is
+ * only written.  C must not overlap A or B (checked on address ranges).
+ *
+ * Edge cases: M == 0 or N == 0 returns SGEMM_OK without launching anything.
+ * K == 0 sets C to zero (the empty sum); A and B may then be NULL.
+ *
+ * Errors: the arguments are checked on the host before anything is launched,
+ * and an invalid call returns its error code without touching the GPU.  A
+ * rejected launch returns SGEMM_ERR_LAUNCH.  The call is asynchronous:
+ * faults during execution surface at the caller's next synchronisation.
+ */
+int sgemm_f32(int M, int N, int K,
+              const float *A, int lda,
+              const float *B, int ldb,
+              float *C, int ldc,
+              cudaStream_t stream);
+
+/* Static English description of a status code (never NULL). */
+const char *sgemm_f32_status_string(int status);
+
+/*
+ * sgemm_f32_smem_request -- host-only description of the kernel's
+ * shared-memory accesses, for checking its layout against the bank rule
+ * bank = (byte_address / 4) % 32 (page "Memory Bank 机制与加速计算",
+ * sections "地址怎样落到 bank" and "为什么 double 和 float4 要另算").
+ * Touches no GPU.
+ *
+ *   kind : 0 = A tile copy into shared memory (4-byte copies),
+ *          1 = B tile copy into shared memory (16-byte copies; aligned class),
+ *          2 = A fragment read (16-byte), 3 = B fragment read (16-byte),
+ *          4 = B tile copy, 8-byte class, 5 = B tile copy, 4-byte class.
+ *   warp : warp index in the CTA, 0 <= warp < *n_warps.
+ *   step : which instruction of that warp, 0 <= step < *n_steps (for copies:
+ *          the copy index within one stage; for reads: 2*k + half, k < BK).
+ *   stage: pipeline stage the access targets, 0 <= stage < *n_stages.
+ *   byte_offset[32] (out): shared-memory byte offset each lane touches,
+ *          relative to the start of the dynamic shared-memory block.
+ *   width_bytes (out): bytes each lane moves (4, 8 or 16).
+ *
+ * sgemm_f32_smem_shape reports the valid ranges for a kind.  Both return
+ * SGEMM_OK or SGEMM_ERR_INVALID_ARG.
+ */
+int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n_stages);
+int sgemm_f32_smem_request(int kind, int warp, int step, int stage,
+                           int64_t byte_offset[32], int *width_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_F32_H */

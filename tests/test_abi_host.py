@@ -1,0 +1,79 @@
+"""C-ABI library: loads, exports what include/sgemm_f32.h declares, and
+rejects invalid calls on the host before touching any GPU (CPU only)."""
+import ctypes
+
+import pytest
+
+import dense_fp32_tiled_gb300 as sg
+from dense_fp32_tiled_gb300 import build as sg_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sg_build.build()
+    return sg.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = sg.declared_functions()
+    assert {"sgemm_f32", "sgemm_f32_status_string", "sgemm_f32_smem_shape",
+            "sgemm_f32_smem_request"} <= set(names)
+    raw = ctypes.CDLL(sg_build.LIB)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        s = sg.status_string(code)
+        assert s and s != "unknown status"
+    assert sg.status_string(12345) == "unknown status"
+
+
+# Every call below fails argument checks, which run before any CUDA call.
+FAKE = 0x10000  # never dereferenced: the call returns before any launch
+
+
+@pytest.mark.parametrize("args,code", [
+    ((-1, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4), -1),
+    ((4, -1, 4, FAKE, 4, FAKE, 4, FAKE, 4), -1),
+    ((4, 4, -1, FAKE, 4, FAKE, 4, FAKE, 4), -1),
+    ((4, 4, 8, FAKE, 7, FAKE, 4, FAKE, 4), -2),          # lda < K
+    ((4, 5, 8, FAKE, 8, FAKE, 4, FAKE, 5), -2),          # ldb < N
+    ((4, 5, 8, FAKE, 8, FAKE, 5, FAKE, 4), -2),          # ldc < N
+    ((4, 4, 0, 0, 1, 0, 4, FAKE, 0), -2),                # ldc 0
+    ((4, 4, 4, 0, 4, FAKE, 4, FAKE * 2, 4), -3),         # A null, K > 0
+    ((4, 4, 4, FAKE, 4, 0, 4, FAKE * 2, 4), -3),         # B null, K > 0
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, 0, 4), -3),         # C null
+    ((4, 4, 4, FAKE + 2, 4, FAKE * 2, 4, FAKE * 3, 4), -7),  # A not 4-byte aligned
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3 + 1, 4), -7),  # C not 4-byte aligned
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE + 16, 4), -4),     # C overlaps A
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 2 + 60, 4), -4), # C overlaps B's last element
+])
+def test_invalid_calls_rejected_on_host(lib, args, code):
+    assert sg.sgemm_f32(*args, 0) == code
+
+
+def test_adjacent_buffers_are_not_aliases(lib):
+    # C starts right after B ends: not an overlap, so the call proceeds past the
+    # alias check; with M=0 it then returns OK without launching.
+    assert sg.sgemm_f32(0, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 2 + 64, 4, 0) == 0
+
+
+def test_empty_outputs_are_noops(lib):
+    assert sg.sgemm_f32(0, 5, 5, 0, 5, 0, 5, 0, 5, 0) == 0
+    assert sg.sgemm_f32(5, 0, 5, 0, 5, 0, 1, 0, 1, 0) == 0
+
+
+def test_torch_wrapper_rejects_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    with pytest.raises(TypeError):
+        sg.sgemm(torch.ones(2, 2), torch.ones(2, 2))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from dense_fp32_tiled_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _binding.load_library()
