@@ -61,9 +61,10 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(PENDING) : "memory");
 }
 
-// One CTA: C tile (tm, tn).  VB = B copy width in floats (4, 2 or 1).
-// vc = C store width in floats (4, 2 or 1), uniform over the grid.
-template <int VB>
+// One CTA: C tile (tm, tn).  VA = A load width in floats (4 or 1), VB = B
+// copy width in floats (4, 2 or 1), vc = C store width in floats (4, 2 or 1),
+// all chosen on the host from pointer and leading-dimension alignment.
+template <int VA, int VB>
 __global__ void __launch_bounds__(NT, 2)
 sgemm_f32_tiled_kernel(const int M, const int N, const int K,
                        const float *__restrict__ A, const int lda,
@@ -76,55 +77,60 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
     tile_of(blockIdx.x, tiles_m, tiles_n, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN;
     const int KT = (K + BK - 1) / BK;
-    const bool k_tail = (K % BK) != 0;
     const uint32_t sbase = smem_u32(smem);
 
-    // ---- A copy set-up: 8 copies, two rows (q >> 2), four k groups (q & 3)
-    int a_kk, a_m[2];
-    {
-        int k, m;
-        a_copy_coord(tid, 0, k, m);
-        a_kk = k;
-        a_m[0] = m;
-        a_copy_coord(tid, 4, k, m);
-        a_m[1] = m;
-    }
-    const float *a_row[2];
-    uint32_t a_bytes[2];
+    // ---- A: global -> registers (float4 per row) -> transposed scalar stores
+    int a_k[A_VECS], a_m;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int row = m0 + a_m[h];
-        const bool ok = row < M;
-        a_row[h] = A + static_cast<size_t>(ok ? row : 0) * lda;
-        a_bytes[h] = ok ? 4u : 0u;
-    }
+    for (int f = 0; f < A_VECS; ++f) a_load_coord(tid, f, a_k[f], a_m);
+    const bool a_ok = m0 + a_m < M;
+    const float *a_ptr = A + static_cast<size_t>(a_ok ? m0 + a_m : 0) * lda;
+    float4 a_reg[A_VECS];
 
-    // ---- B copy set-up
+    // Loads A[m][kb + a_k[f] .. +3]; elements past M or K read as 0 (the
+    // predicated edge loads of "边界处理会破坏漂亮形状").  Rows past M read
+    // row 0 (always in bounds) and are zeroed afterwards.
+    auto load_a = [&](int kt) {
+        const int kb = kt * BK;
+#pragma unroll
+        for (int f = 0; f < A_VECS; ++f) {
+            const int k = kb + a_k[f];
+            const float *p = a_ptr + k;
+            float4 v;
+            if (VA == 4 && k + 3 < K) {
+                v = __ldg(reinterpret_cast<const float4 *>(p));
+            } else {
+                v.x = k + 0 < K ? __ldg(p + 0) : 0.0f;
+                v.y = k + 1 < K ? __ldg(p + 1) : 0.0f;
+                v.z = k + 2 < K ? __ldg(p + 2) : 0.0f;
+                v.w = k + 3 < K ? __ldg(p + 3) : 0.0f;
+            }
+            a_reg[f] = a_ok ? v : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+    };
+    auto store_a = [&](int stage) {
+        float *st = smem + stage * STAGE_FLOATS;
+#pragma unroll
+        for (int f = 0; f < A_VECS; ++f) {
+            st[as_word(a_k[f] + 0, a_m)] = a_reg[f].x;
+            st[as_word(a_k[f] + 1, a_m)] = a_reg[f].y;
+            st[as_word(a_k[f] + 2, a_m)] = a_reg[f].z;
+            st[as_word(a_k[f] + 3, a_m)] = a_reg[f].w;
+        }
+    };
+
+    // ---- B: global -> shared by cp.async, row-major tile
     constexpr int NB = b_copies<VB>();
     int b_k0, b_n;
     b_copy_coord<VB>(tid, 0, b_k0, b_n);
-
     const int b_col = n0 + b_n;
-    const int b_valid = N - b_col;       // valid floats from b_col on
+    const int b_valid = N - b_col;  // valid floats from b_col on
     const uint32_t b_bytes = b_valid >= VB ? VB * 4u : (b_valid > 0 ? b_valid * 4u : 0u);
     const float *b_colp = B + (b_valid > 0 ? b_col : 0);
 
-    auto load_tile = [&](int kt, int stage) {
+    auto load_b = [&](int kt, int stage) {
         const uint32_t st = sbase + stage * (STAGE_FLOATS * 4);
         const int kb = kt * BK;
-        const bool tail = k_tail && (kt == KT - 1);
-#pragma unroll
-        for (int q = 0; q < A_COPIES; ++q) {
-            int k, m;
-            a_copy_coord(tid, q, k, m);
-            const float *src = a_row[q >> 2] + kb + k;
-            uint32_t bytes = a_bytes[q >> 2];
-            if (tail && kb + k >= K) {
-                src = a_row[q >> 2] + kb;
-                bytes = 0;
-            }
-            cp_async<4>(st + as_word(k, m) * 4, src, bytes);
-        }
 #pragma unroll
         for (int q = 0; q < NB; ++q) {
             int k, n;
@@ -132,35 +138,49 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
             const int kg = kb + k;
             const float *src = b_colp + static_cast<size_t>(kg) * ldb;
             uint32_t bytes = b_bytes;
-            if (tail && kg >= K) {
+            if (kg >= K) {  // past the last row of B: zero fill, read nothing
                 src = B;
                 bytes = 0;
             }
             cp_async<VB * 4>(st + bs_word(k, n) * 4, src, bytes);
         }
-
     };
 
-    float acc[TM][TN];
+    // ---- accumulators, paired for the packed FP32 FMA (fma.rn.f32x2).  With
+    // rows r = 2i+{0,1} and cols c = 2j+{0,1} of the 8 x 8 register tile,
+    //   dg[i][j] = (acc[2i][2j],   acc[2i+1][2j+1])  += (a_2i, a_2i+1) * (b_2j,   b_2j+1)
+    //   ad[i][j] = (acc[2i][2j+1], acc[2i+1][2j])    += (a_2i, a_2i+1) * (b_2j+1, b_2j)
+    // so both operands are natural register pairs of the 128-bit fragment
+    // reads (plus one swapped copy of each B pair): 32 packed FMAs per k.
+    float2 dg[TM / 2][TN / 2], ad[TM / 2][TN / 2];
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
+    for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN / 2; ++j) {
+            dg[i][j] = make_float2(0.0f, 0.0f);
+            ad[i][j] = make_float2(0.0f, 0.0f);
+        }
 
     const int ra = frag_row0(tid);
     const int cb = frag_col0(tid);
 
+    if (KT > 0) {
+        load_a(0);
+        store_a(0);
+    }
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < KT) load_tile(s, s);
+        if (s < KT) load_b(s, s);
         cp_async_commit();
     }
 
     for (int kt = 0; kt < KT; ++kt) {
+        const bool more = kt + 1 < KT;
+        if (more) load_a(kt + 1);  // in flight during this tile's FMAs
         cp_async_wait<STAGES - 2>();
         __syncthreads();  // tile kt visible to all; stage (kt-1) free again
         const int nk = kt + STAGES - 1;
-        if (nk < KT) load_tile(nk, nk % STAGES);
+        if (nk < KT) load_b(nk, nk % STAGES);
         cp_async_commit();
 
         const float *st = smem + (kt % STAGES) * STAGE_FLOATS;
@@ -170,13 +190,21 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
             const float4 a1 = *reinterpret_cast<const float4 *>(st + as_word(k, ra + 16));
             const float4 b0 = *reinterpret_cast<const float4 *>(st + bs_word(k, cb));
             const float4 b1 = *reinterpret_cast<const float4 *>(st + bs_word(k, cb + 32));
-            const float a[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float b[TN] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float2 ap[TM / 2] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
+                                       make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
+            const float2 bp[TN / 2] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                       make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+            const float2 bq[TN / 2] = {make_float2(b0.y, b0.x), make_float2(b0.w, b0.z),
+                                       make_float2(b1.y, b1.x), make_float2(b1.w, b1.z)};
 #pragma unroll
-            for (int i = 0; i < TM; ++i)
+            for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < TN / 2; ++j) {
+                    dg[i][j] = __ffma2_rn(ap[i], bp[j], dg[i][j]);
+                    ad[i][j] = __ffma2_rn(ap[i], bq[j], ad[i][j]);
+                }
         }
+        if (more) store_a((kt + 1) % STAGES);  // published by the next barrier
     }
     cp_async_wait<0>();
 
@@ -189,7 +217,11 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = n0 + cb + 32 * h;
-            const float *v = &acc[i][4 * h];
+            // row i = 2*ip + r of the tile; cols 4h .. 4h+3 = pairs jp = 2h, 2h+1
+            const int ip = i >> 1, r = i & 1;
+            const float2 d0 = dg[ip][2 * h], x0 = ad[ip][2 * h];
+            const float2 d1 = dg[ip][2 * h + 1], x1 = ad[ip][2 * h + 1];
+            const float v[4] = {r ? x0.y : d0.x, r ? d0.y : x0.x, r ? x1.y : d1.x, r ? d1.y : x1.x};
             if (col + 3 < N && vc == 4) {
                 *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
             } else if (col + 3 < N && vc == 2) {
@@ -223,9 +255,12 @@ int setup_device(int dev) {
         major != 10 || minor != 3) {
         st = SGEMM_ERR_DEVICE;
     } else {
-        const void *kernels[] = {reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<4>),
-                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<2>),
-                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<1>)};
+        const void *kernels[] = {reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<4, 4>),
+                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<4, 2>),
+                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<4, 1>),
+                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<1, 4>),
+                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<1, 2>),
+                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<1, 1>)};
         for (const void *k : kernels) {
             if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
                 cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -260,7 +295,7 @@ long long extent(long long rows, long long cols, long long ld) {
     return (rows == 0 || cols == 0) ? 0 : (rows - 1) * ld + cols;
 }
 
-template <int VB>
+template <int VA, int VB>
 cudaError_t launch(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
                    int tiles_m, int tiles_n, int vc, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -268,7 +303,7 @@ cudaError_t launch(int M, int N, int K, const float *A, int lda, const float *B,
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, sgemm_f32_tiled_kernel<VB>, M, N, K, A, lda, B, ldb, C, ldc, tiles_m,
+    return cudaLaunchKernelEx(&cfg, sgemm_f32_tiled_kernel<VA, VB>, M, N, K, A, lda, B, ldb, C, ldc, tiles_m,
                               tiles_n, vc);
 }
 
@@ -299,14 +334,18 @@ extern "C" int sgemm_f32(int M, int N, int K, const float *A, int lda, const flo
     const int st = setup_device(dev);
     if (st != SGEMM_OK) return st;
 
+    const int va = K > 0 ? (vector_class(A, lda) == 4 ? 4 : 1) : 4;
     const int vb = K > 0 ? vector_class(B, ldb) : 4;
     const int vc = vector_class(C, ldc);
+    const int tm_ = static_cast<int>(tiles_m), tn_ = static_cast<int>(tiles_n);
     cudaError_t err;
-    switch (vb) {
-        case 4: err = launch<4>(M, N, K, A, lda, B, ldb, C, ldc, (int)tiles_m, (int)tiles_n, vc, stream); break;
-        case 2: err = launch<2>(M, N, K, A, lda, B, ldb, C, ldc, (int)tiles_m, (int)tiles_n, vc, stream); break;
-        default: err = launch<1>(M, N, K, A, lda, B, ldb, C, ldc, (int)tiles_m, (int)tiles_n, vc, stream); break;
+#define SGEMM_LAUNCH(VA_, VB_) launch<VA_, VB_>(M, N, K, A, lda, B, ldb, C, ldc, tm_, tn_, vc, stream)
+    if (va == 4) {
+        err = vb == 4 ? SGEMM_LAUNCH(4, 4) : vb == 2 ? SGEMM_LAUNCH(4, 2) : SGEMM_LAUNCH(4, 1);
+    } else {
+        err = vb == 4 ? SGEMM_LAUNCH(1, 4) : vb == 2 ? SGEMM_LAUNCH(1, 2) : SGEMM_LAUNCH(1, 1);
     }
+#undef SGEMM_LAUNCH
     if (err != cudaSuccess) {
         (void)cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
@@ -331,7 +370,7 @@ extern "C" const char *sgemm_f32_status_string(int status) {
 extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n_stages) {
     int steps;
     switch (kind) {
-        case 0: steps = A_COPIES; break;
+        case 0: steps = 4 * A_VECS; break;
         case 1: steps = b_copies<4>(); break;
         case 2:
         case 3: steps = 2 * BK; break;
@@ -357,7 +396,7 @@ extern "C" int sgemm_f32_smem_request(int kind, int warp, int step, int stage, i
         const int tid = warp * 32 + lane;
         int word = 0, k = 0, x = 0;
         switch (kind) {
-            case 0: a_copy_coord(tid, step, k, x); word = as_word(k, x); width = 4; break;
+            case 0: a_load_coord(tid, step >> 2, k, x); word = as_word(k + (step & 3), x); width = 4; break;
             case 1: b_copy_coord<4>(tid, step, k, x); word = bs_word(k, x); width = 16; break;
             case 4: b_copy_coord<2>(tid, step, k, x); word = bs_word(k, x); width = 8; break;
             case 5: b_copy_coord<1>(tid, step, k, x); word = bs_word(k, x); width = 4; break;

@@ -9,16 +9,21 @@
 //
 // Layout (per pipeline stage):
 //   As: BK x BM floats, k-major ("transposed" A tile, as in the
-//       vectorised-load page's "shared memory transpose 的基本想法"), with an
-//       XOR swizzle of the 8-float block index inside each 32-float bank row:
-//       logical (k, m) lives at word k*BM + (m ^ ((k & 3) << 3)).  The
-//       swizzle ("Padding 之外的选择" on the bank page) keeps 4-float groups
-//       contiguous and 16-byte aligned, so fragment reads stay 128-bit, and
-//       spreads the transposing 4-byte copies of 4 consecutive k over 4
-//       different bank groups.  +1 padding would break the 16-byte alignment
-//       of the fragment reads.
+//       vectorised-load page's "shared memory transpose 的基本想法"): logical
+//       (k, m) lives at word k*BM + m.  Each warp's transposing stores write
+//       32 consecutive m of one k (one word per bank), and the fragment reads
+//       take 4 consecutive m (16-byte aligned), so neither padding nor a
+//       swizzle is needed: the thread->element map alone keeps every access
+//       conflict-free (the bank page's "Padding 之外的选择" point that the
+//       layout and the thread mapping are chosen together).
 //   Bs: BK x BN floats, row-major as in global memory (the page's
 //       "原样写" variant); fragment reads along n are contiguous.
+//
+// 128-bit shared loads on sm_103 are served per half-warp; when lanes share
+// addresses (broadcast), each group of 4 consecutive lanes can receive at
+// most 2 distinct 16-byte groups per pass (measured with ncu, see the
+// oracle's bank model).  The lane grid below gives every quad 2 A groups and
+// 2 B groups, so each fragment read costs the minimum 2 passes.
 #pragma once
 
 #if defined(__CUDACC__)
@@ -33,7 +38,7 @@ constexpr int BM = 128;          // CTA tile rows (M)
 constexpr int BN = 128;          // CTA tile cols (N)
 constexpr int BK = 16;           // K depth of one pipeline stage
 constexpr int NT = 256;          // threads per CTA (8 warps)
-constexpr int STAGES = 4;        // global->shared pipeline depth
+constexpr int STAGES = 3;        // shared-memory ring depth
 constexpr int TM = 8;            // per-thread register tile rows
 constexpr int TN = 8;            // per-thread register tile cols
 constexpr int WARPS_M = 4;       // warp grid over the CTA tile
@@ -44,25 +49,29 @@ constexpr int A_STAGE_FLOATS = BK * BM;
 constexpr int B_STAGE_FLOATS = BK * BN;
 constexpr int STAGE_FLOATS = A_STAGE_FLOATS + B_STAGE_FLOATS;
 constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
-constexpr int A_COPIES = BM * BK / NT;  // 4-byte copies per thread per stage
+constexpr int A_VECS = BM * BK / (4 * NT);  // float4 of A a thread stages per k-tile
 
 static_assert(WARPS_M * WARPS_N * 32 == NT, "warp grid");
 static_assert(WM == 4 * TM && WN == 8 * TN, "lane grid 4 x 8");
 static_assert((STAGE_FLOATS * 4) % 128 == 0, "stages start on a bank row");
+static_assert(NT == 256 && BM == 128 && BK == 16, "A staging map covers 128 rows x 16 k");
 
 // ---- shared-memory word offsets inside one stage -----------------------
-SG_HD int as_word(int k, int m) { return k * BM + (m ^ ((k & 3) << 3)); }
+SG_HD int as_word(int k, int m) { return k * BM + m; }
 SG_HD int bs_word(int k, int n) { return A_STAGE_FLOATS + k * BN + n; }
 
 // ---- global->shared copy maps -----------------------------------------
-// A: 4-byte copies (a 16-byte copy cannot transpose).  Warp w owns rows
-// [16w, 16w+16); copy q of lane l moves element (k, m) with
-//   k = 4*(q & 3) + (l & 3),  m = 16w + 8*(q >> 2) + (l >> 2).
-// A warp instruction therefore reads 8 rows x 16 contiguous bytes of A.
-SG_HD void a_copy_coord(int tid, int q, int &k, int &m) {
+// A: staged through registers.  Warp w owns rows [32(w % 4), 32(w % 4) + 32)
+// and k columns [8(w / 4), 8(w / 4) + 8); float4 f (0 or 1) of lane l holds
+// A[m][k..k+3] with
+//   m = 32(w % 4) + l,  k = 8(w / 4) + 4f,
+// so one warp load reads 32 rows x 16 bytes and the pair f = 0, 1 covers
+// whole 32-byte sectors.  The 4 components go to As by 4 scalar stores (the
+// transpose), component c to logical (k + c, m): 32 consecutive words.
+SG_HD void a_load_coord(int tid, int f, int &k, int &m) {
     const int w = tid >> 5, l = tid & 31;
-    k = 4 * (q & 3) + (l & 3);
-    m = 16 * w + 8 * (q >> 2) + (l >> 2);
+    m = 32 * (w & 3) + l;
+    k = 8 * (w >> 2) + 4 * f;
 }
 
 // B: vector copies of VB floats (VB = 4, 2, 1 by alignment class).  Copy q
@@ -79,17 +88,20 @@ template <int VB>
 SG_HD constexpr int b_copies() { return BK * BN / (NT * VB); }
 
 // ---- register-tile maps ------------------------------------------------
-// Warp w covers rows WM*(w / WARPS_N) and cols WN*(w % WARPS_N); lane l is
-// (lr, lc) = (l >> 3, l & 7).  Thread rows: 4*lr + {0..3} and 16 + 4*lr +
-// {0..3}; thread cols: 4*lc + {0..3} and 32 + 4*lc + {0..3}.  Each k step
-// a thread reads two 4-float groups of As row k and two of Bs row k.
+// Warp w covers rows WM*(w / WARPS_N) and cols WN*(w % WARPS_N).  Lane
+// l = 16h + 4q + 2e1 + e0 (h half-warp, q quad, e1 e0 lane bits in the quad)
+// sits at (lr, lc) = (2h + e0, 2q + e1) of a 4 x 8 lane grid: each quad holds
+// 2 rows x 2 columns of the grid.  Thread rows: 4*lr + {0..3} and
+// 16 + 4*lr + {0..3}; thread cols: 4*lc + {0..3} and 32 + 4*lc + {0..3}.
+SG_HD int lane_lr(int l) { return 2 * (l >> 4) + (l & 1); }
+SG_HD int lane_lc(int l) { return 2 * ((l >> 2) & 3) + ((l & 3) >> 1); }
 SG_HD int frag_row0(int tid) {
     const int w = tid >> 5, l = tid & 31;
-    return WM * (w / WARPS_N) + 4 * (l >> 3);
+    return WM * (w / WARPS_N) + 4 * lane_lr(l);
 }
 SG_HD int frag_col0(int tid) {
     const int w = tid >> 5, l = tid & 31;
-    return WN * (w % WARPS_N) + 4 * (l & 7);
+    return WN * (w % WARPS_N) + 4 * lane_lc(l);
 }
 // i, j in [0, 8): row / col of register-tile element (i, j).
 SG_HD int frag_row(int tid, int i) { return frag_row0(tid) + (i & 3) + 16 * (i >> 2); }

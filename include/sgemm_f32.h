@@ -79,13 +79,14 @@ const char *sgemm_f32_status_string(int status);
  * sections "地址怎样落到 bank" and "为什么 double 和 float4 要另算").
  * Touches no GPU.
  *
- *   kind : 0 = A tile copy into shared memory (4-byte copies),
+ *   kind : 0 = A tile store into shared memory (4-byte transposing stores),
  *          1 = B tile copy into shared memory (16-byte copies; aligned class),
  *          2 = A fragment read (16-byte), 3 = B fragment read (16-byte),
  *          4 = B tile copy, 8-byte class, 5 = B tile copy, 4-byte class.
  *   warp : warp index in the CTA, 0 <= warp < *n_warps.
  *   step : which instruction of that warp, 0 <= step < *n_steps (for copies:
- *          the copy index within one stage; for reads: 2*k + half, k < BK).
+ *          the copy or store index within one stage; for reads: 2*k + half,
+ *          k < BK).
  *   stage: pipeline stage the access targets, 0 <= stage < *n_stages.
  *   byte_offset[32] (out): shared-memory byte offset each lane touches,
  *          relative to the start of the dynamic shared-memory block.

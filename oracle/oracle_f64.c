@@ -133,36 +133,12 @@ int oracle_bank_of(uint64_t byte_address) {
     return (int)((byte_address / 4u) % 32u);
 }
 
-/*
- * One warp-wide shared-memory request.  Lane l (active[l] != 0) touches
- * width_bytes / 4 consecutive 32-bit words starting at byte_address[l]
- * (width_bytes is 4, 8 or 16 and each address is a multiple of it).
- *
- * Reading of the pages: one pass over the banks (a wavefront) can serve one
- * 32-bit word per bank and hand that word to every lane that asked for it
- * (broadcast); two different words in the same bank need two passes
- * (conflict).  So the passes the request needs are the largest number of
- * distinct words that fall in any one bank.  A wide request may need several
- * passes without any conflict simply because it moves more than 32 distinct
- * words; the least it can need is ceil(distinct_words / 32).
- *
- * Outputs: *wavefronts (passes needed), *ideal (ceil(distinct words / 32)),
- * *degree (the largest number of distinct words in one bank, as for a
- * scalar access), *distinct (number of distinct words).  Returns 0, or -1 on
- * a bad argument (width not 4/8/16, misaligned address, more than 32 lanes).
- */
-int oracle_shared_request(int n_lanes, const uint64_t *byte_address,
-                          const uint8_t *active, int width_bytes,
-                          int *wavefronts, int *ideal, int *degree,
-                          int *distinct) {
-    if (n_lanes < 0 || n_lanes > 32) return -1;
-    if (width_bytes != 4 && width_bytes != 8 && width_bytes != 16) return -1;
-    const int wpl = width_bytes / 4;
-    uint64_t words[32 * 4];
+/* Distinct 32-bit words touched by the active lanes lo..hi-1; returns count. */
+static int collect_words(int lo, int hi, const uint64_t *byte_address, const uint8_t *active,
+                         int wpl, uint64_t *words) {
     int nw = 0;
-    for (int l = 0; l < n_lanes; ++l) {
+    for (int l = lo; l < hi; ++l) {
         if (active && !active[l]) continue;
-        if (byte_address[l] % (uint64_t)width_bytes) return -1;
         for (int w = 0; w < wpl; ++w) {
             const uint64_t word = byte_address[l] / 4u + (uint64_t)w;
             int seen = 0;
@@ -171,16 +147,148 @@ int oracle_shared_request(int n_lanes, const uint64_t *byte_address,
             if (!seen) words[nw++] = word;
         }
     }
+    return nw;
+}
+
+/* The pages' rule inside one pass: the largest number of distinct words that
+ * fall in one bank (the same word is broadcast).  Also returns the bank mask. */
+static int pass_degree(int nw, const uint64_t *words, uint32_t *bank_mask) {
     int per_bank[32];
     memset(per_bank, 0, sizeof per_bank);
     int worst = 0;
+    uint32_t mask = 0;
     for (int q = 0; q < nw; ++q) {
         const int b = oracle_bank_of(words[q] * 4u);
+        mask |= 1u << b;
         if (++per_bank[b] > worst) worst = per_bank[b];
     }
-    if (wavefronts) *wavefronts = worst;
-    if (ideal) *ideal = (nw + 31) / 32;
-    if (degree) *degree = worst;
+    if (bank_mask) *bank_mask = mask;
+    return worst;
+}
+
+/* Largest number of distinct accesses among the groups of 4 consecutive
+ * active lanes ("quads") in lo..hi-1. */
+static int max_quad_distinct(int lo, int hi, const uint64_t *addr, const uint8_t *act) {
+    int worst = 0;
+    for (int q = lo; q < hi; q += 4) {
+        uint64_t seen[4];
+        int n = 0;
+        for (int l = q; l < q + 4 && l < hi; ++l) {
+            if (!act[l]) continue;
+            int dup = 0;
+            for (int t = 0; t < n; ++t)
+                if (seen[t] == addr[l]) { dup = 1; break; }
+            if (!dup) seen[n++] = addr[l];
+        }
+        if (n > worst) worst = n;
+    }
+    return worst;
+}
+
+/* 1 when no two active lanes in lo..hi-1 access the same address. */
+static int all_distinct(int lo, int hi, const uint64_t *addr, const uint8_t *act) {
+    for (int a = lo; a < hi; ++a) {
+        if (!act[a]) continue;
+        for (int b = a + 1; b < hi; ++b)
+            if (act[b] && addr[b] == addr[a]) return 0;
+    }
+    return 1;
+}
+
+/* Passes for the active lanes lo..hi-1 of one wide request (see below). */
+static int wide_passes(int lo, int hi, const uint64_t *addr, const uint8_t *act, int wpl,
+                       int split_quarters, int *max_degree) {
+    uint64_t words[32 * 4];
+    uint32_t m0, m1;
+    const int nw = collect_words(lo, hi, addr, act, wpl, words);
+    if (!nw) return 0;
+    const int deg = pass_degree(nw, words, &m0);
+    if (!all_distinct(lo, hi, addr, act) || !split_quarters) {
+        if (max_degree && deg > *max_degree) *max_degree = deg;
+        if (!all_distinct(lo, hi, addr, act))
+            return (max_quad_distinct(lo, hi, addr, act) + 1) / 2 * deg;
+        return deg;
+    }
+    const int mid = lo + (hi - lo) / 2;
+    const int n0 = collect_words(lo, mid, addr, act, wpl, words);
+    const int d0 = n0 ? pass_degree(n0, words, &m0) : 0;
+    const int n1 = collect_words(mid, hi, addr, act, wpl, words);
+    const int d1 = n1 ? pass_degree(n1, words, &m1) : 0;
+    const int dq = d0 > d1 ? d0 : d1;
+    if (max_degree && dq > *max_degree) *max_degree = dq;
+    if (!n0 || !n1 || !(m0 & m1)) return dq;
+    return d0 + d1;
+}
+
+/*
+ * One warp-wide shared-memory request.  Lane l (active[l] != 0) touches
+ * width_bytes / 4 consecutive 32-bit words starting at byte_address[l]
+ * (width_bytes is 4, 8 or 16 and each address is a multiple of it).
+ *
+ * Within one pass over the banks (a wavefront) each bank serves one 32-bit
+ * word, which may go to every lane that asked for it (broadcast); two
+ * different words in one bank need two passes (conflict).  This is the bank
+ * page's rule ("四种访问，四种结果"), and for 4-byte accesses the passes are
+ * the largest number of distinct words in one bank (the conflict degree).
+ *
+ * For 8- and 16-byte accesses the same page says to analyse the lanes each
+ * transaction actually serves ("为什么 double 和 float4 要另算").  The lane
+ * grouping used here was fitted to ncu wavefront counts of 26 lane patterns
+ * x 2 widths measured on sm_103 (tests/probes/lds_probe.cu, counts in
+ * tests/golden/lds_wavefronts_sm103.txt), and reproduces all of them:
+ *   8-byte : the whole warp is one group;
+ *   16-byte: each half-warp is a group, and the two halves never share passes.
+ * A group whose lanes all read different addresses needs as many passes as
+ * its conflict degree (for 16 bytes: per 8-lane quarter, the two quarters
+ * sharing passes when their banks are disjoint).  A group in which some
+ * lanes share an address (a broadcast) is served 2 distinct accesses per
+ * quad of 4 consecutive lanes per pass, each pass also limited by the
+ * conflict degree: passes = ceil(most distinct accesses in a quad / 2) x
+ * degree.
+ *
+ * Outputs: *wavefronts (passes needed), *ideal (least passes the same amount
+ * of distinct data could need: one per 32 distinct words, counted per
+ * half-warp for 16-byte accesses), *degree (largest number of distinct words
+ * in one bank within one group), *distinct (distinct words over the warp).
+ * Returns 0, or -1 on a bad argument (width not 4/8/16, misaligned address,
+ * more than 32 lanes).
+ */
+int oracle_shared_request(int n_lanes, const uint64_t *byte_address,
+                          const uint8_t *active, int width_bytes,
+                          int *wavefronts, int *ideal, int *degree,
+                          int *distinct) {
+    if (n_lanes < 0 || n_lanes > 32) return -1;
+    if (width_bytes != 4 && width_bytes != 8 && width_bytes != 16) return -1;
+    const int wpl = width_bytes / 4;
+    uint64_t addr[32];
+    uint8_t act[32];
+    for (int l = 0; l < 32; ++l) {
+        const int on = l < n_lanes && (!active || active[l]);
+        if (on && byte_address[l] % (uint64_t)width_bytes) return -1;
+        addr[l] = on ? byte_address[l] : 0;
+        act[l] = (uint8_t)on;
+    }
+    uint64_t words[32 * 4];
+    const int nw = collect_words(0, 32, addr, act, wpl, words);
+    int deg = 0, wf = 0, id = 0;
+    if (width_bytes == 4) {
+        uint32_t m;
+        deg = nw ? pass_degree(nw, words, &m) : 0;
+        wf = deg;
+        id = (nw + 31) / 32;
+    } else if (width_bytes == 8) {
+        wf = wide_passes(0, 32, addr, act, wpl, 0, &deg);
+        id = (nw + 31) / 32;
+    } else {
+        for (int h = 0; h < 2; ++h) {
+            wf += wide_passes(16 * h, 16 * h + 16, addr, act, wpl, 1, &deg);
+            const int nh = collect_words(16 * h, 16 * h + 16, addr, act, wpl, words);
+            id += (nh + 31) / 32;
+        }
+    }
+    if (wavefronts) *wavefronts = wf;
+    if (ideal) *ideal = id;
+    if (degree) *degree = deg;
     if (distinct) *distinct = nw;
     return 0;
 }

@@ -78,24 +78,46 @@ def test_xor_swizzle_is_conflict_free_both_ways(oracle_lib):
         assert oracle_lib.shared_request([phys(r, c) for r in range(32)], 4)["degree"] == 1
 
 
+def test_measured_wide_load_wavefronts(oracle_lib):
+    """The lane grouping of 8- and 16-byte loads, against ncu counts on sm_103."""
+    n = 0
+    with open(os.path.join(HERE, "golden", "lds_wavefronts_sm103.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, rhs = line.split("=")
+            width, expr = lhs.split(None, 1)
+            width = int(width)
+            addrs = [width * _eval_index(expr.strip(), l) for l in range(32)]
+            r = oracle_lib.shared_request(addrs, width)
+            assert r["wavefronts"] == int(rhs.split()[0]), (width, expr, r)
+            n += 1
+    assert n == 52
+
+
 def test_wide_accesses(oracle_lib):
-    # 32 lanes reading consecutive float4: 128 distinct words -> 4 passes, all needed
+    # 32 lanes reading consecutive float4: 512 distinct bytes -> 4 passes, all needed
     r = oracle_lib.shared_request([16 * l for l in range(32)], 16)
     assert (r["wavefronts"], r["ideal"], r["distinct"]) == (4, 4, 128)
-    # every lane reading the same float4: broadcast, 1 pass
+    # every lane reading the same float4: one pass per half-warp
     r = oracle_lib.shared_request([48] * 32, 16)
-    assert (r["wavefronts"], r["ideal"]) == (1, 1)
-    # 8 distinct float4 covering 128 contiguous bytes, each read by 4 lanes: 1 pass
+    assert (r["wavefronts"], r["ideal"]) == (2, 2)
+    # 8 distinct float4 covering 128 contiguous bytes, each quad of lanes
+    # reading 4 of them: two passes per half
     r = oracle_lib.shared_request([16 * (l % 8) for l in range(32)], 16)
-    assert (r["wavefronts"], r["ideal"]) == (1, 1)
-    # float4 reads 512 B apart (stride 128 floats): same 4 banks, 32 distinct chunks
+    assert (r["wavefronts"], r["ideal"]) == (4, 2)
+    # the same 8 float4 with lanes paired inside each quad: one pass per half
+    r = oracle_lib.shared_request([16 * (l >> 1) for l in range(16)] * 2, 16)
+    assert (r["wavefronts"], r["ideal"]) == (2, 2)
+    # float4 reads 512 B apart: same 4 banks, 8 distinct words per bank per quarter
     r = oracle_lib.shared_request([512 * l for l in range(32)], 16)
-    assert r["wavefronts"] == 32 and r["ideal"] == 4
+    assert r["wavefronts"] == 32 and r["ideal"] == 4 and r["degree"] == 8
     # doubles (8 B): consecutive -> 2 passes, no excess
     r = oracle_lib.shared_request([8 * l for l in range(32)], 8)
     assert (r["wavefronts"], r["ideal"]) == (2, 2)
     # inactive lanes do not count
     r = oracle_lib.shared_request([4 * 32 * l for l in range(32)], 4, active=[1] + [0] * 31)
-    assert r["degree"] == 1
+    assert r["degree"] == 1 and r["wavefronts"] == 1
     with pytest.raises(ValueError):
         oracle_lib.shared_request([2], 4)
