@@ -61,9 +61,17 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(PENDING) : "memory");
 }
 
-// One CTA: C tile (tm, tn).  VA = A load width in floats (4 or 1), VB = B
+// One CTA: C tile (tm, tn).  VA = A copy width in floats (4 or 1), VB = B
 // copy width in floats (4, 2 or 1), vc = C store width in floats (4, 2 or 1),
 // all chosen on the host from pointer and leading-dimension alignment.
+//
+// Pipeline (one __syncthreads per K tile): at iteration kt
+//   1. wait until the copy group of tile kt+1 has landed (own copies), then
+//      barrier: tile kt+1's raw A and B, and the transposed As of tile kt,
+//      are visible to all; every thread has finished tile kt-1;
+//   2. issue the copies of tile kt+STAGES-1 into the stage tile kt-1 used;
+//   3. transpose tile kt+1's raw A into the As buffer tile kt-1 used;
+//   4. 16 k steps of fragment reads and packed FMAs on tile kt.
 template <int VA, int VB>
 __global__ void __launch_bounds__(NT, 2)
 sgemm_f32_tiled_kernel(const int M, const int N, const int K,
@@ -79,47 +87,17 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
     const int KT = (K + BK - 1) / BK;
     const uint32_t sbase = smem_u32(smem);
 
-    // ---- A: global -> registers (float4 per row) -> transposed scalar stores
-    int a_k[A_VECS], a_m;
-#pragma unroll
-    for (int f = 0; f < A_VECS; ++f) a_load_coord(tid, f, a_k[f], a_m);
-    const bool a_ok = m0 + a_m < M;
-    const float *a_ptr = A + static_cast<size_t>(a_ok ? m0 + a_m : 0) * lda;
-    float4 a_reg[A_VECS];
+    // ---- A copies (global -> raw staging tile).  Rows past M and columns
+    // past K are zero-filled by a zero source size ("边界处理会破坏漂亮形状").
+    constexpr int NA = VA == 4 ? A_COPIES16 : A_COPIES4;
+    int a_m0, a_k;
+    if constexpr (VA == 4) a_copy16_coord(tid, 0, a_m0, a_k);
+    else a_copy4_coord(tid, 0, a_m0, a_k);
+    constexpr int A_ROW_STEP = VA == 4 ? 64 : 16;  // rows between a thread's copies
+    const float *a_base = A + static_cast<size_t>(m0 + a_m0 < M ? m0 + a_m0 : 0) * lda + a_k;
+    const size_t a_step = static_cast<size_t>(A_ROW_STEP) * lda;
 
-    // Loads A[m][kb + a_k[f] .. +3]; elements past M or K read as 0 (the
-    // predicated edge loads of "边界处理会破坏漂亮形状").  Rows past M read
-    // row 0 (always in bounds) and are zeroed afterwards.
-    auto load_a = [&](int kt) {
-        const int kb = kt * BK;
-#pragma unroll
-        for (int f = 0; f < A_VECS; ++f) {
-            const int k = kb + a_k[f];
-            const float *p = a_ptr + k;
-            float4 v;
-            if (VA == 4 && k + 3 < K) {
-                v = __ldg(reinterpret_cast<const float4 *>(p));
-            } else {
-                v.x = k + 0 < K ? __ldg(p + 0) : 0.0f;
-                v.y = k + 1 < K ? __ldg(p + 1) : 0.0f;
-                v.z = k + 2 < K ? __ldg(p + 2) : 0.0f;
-                v.w = k + 3 < K ? __ldg(p + 3) : 0.0f;
-            }
-            a_reg[f] = a_ok ? v : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        }
-    };
-    auto store_a = [&](int stage) {
-        float *st = smem + stage * STAGE_FLOATS;
-#pragma unroll
-        for (int f = 0; f < A_VECS; ++f) {
-            st[as_word(a_k[f] + 0, a_m)] = a_reg[f].x;
-            st[as_word(a_k[f] + 1, a_m)] = a_reg[f].y;
-            st[as_word(a_k[f] + 2, a_m)] = a_reg[f].z;
-            st[as_word(a_k[f] + 3, a_m)] = a_reg[f].w;
-        }
-    };
-
-    // ---- B: global -> shared by cp.async, row-major tile
+    // ---- B copies (global -> shared, row-major tile)
     constexpr int NB = b_copies<VB>();
     int b_k0, b_n;
     b_copy_coord<VB>(tid, 0, b_k0, b_n);
@@ -128,21 +106,44 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
     const uint32_t b_bytes = b_valid >= VB ? VB * 4u : (b_valid > 0 ? b_valid * 4u : 0u);
     const float *b_colp = B + (b_valid > 0 ? b_col : 0);
 
-    auto load_b = [&](int kt, int stage) {
-        const uint32_t st = sbase + stage * (STAGE_FLOATS * 4);
+    auto issue_tile = [&](int kt) {
+        const int stage = kt % STAGES;
         const int kb = kt * BK;
+#pragma unroll
+        for (int q = 0; q < NA; ++q) {
+            int m, k;
+            if constexpr (VA == 4) a_copy16_coord(tid, q, m, k);
+            else a_copy4_coord(tid, q, m, k);
+            const int kg = kb + k;
+            const int left = K - kg;  // valid floats from kg on
+            uint32_t bytes = (m0 + m < M && left > 0) ? (left >= VA ? VA * 4u : left * 4u) : 0u;
+            const float *src = bytes ? a_base + q * a_step + kb : A;
+            cp_async<VA * 4>(sbase + ar_word(stage, m, k) * 4, src, bytes);
+        }
 #pragma unroll
         for (int q = 0; q < NB; ++q) {
             int k, n;
             b_copy_coord<VB>(tid, q, k, n);
             const int kg = kb + k;
-            const float *src = b_colp + static_cast<size_t>(kg) * ldb;
-            uint32_t bytes = b_bytes;
-            if (kg >= K) {  // past the last row of B: zero fill, read nothing
-                src = B;
-                bytes = 0;
-            }
-            cp_async<VB * 4>(st + bs_word(k, n) * 4, src, bytes);
+            const bool ok = kg < K && b_bytes != 0;
+            const float *src = ok ? b_colp + static_cast<size_t>(kg) * ldb : B;
+            cp_async<VB * 4>(sbase + bs_word(stage, k, n) * 4, src, ok ? b_bytes : 0u);
+        }
+    };
+
+    // ---- A transpose: raw staging tile -> k-major As buffer
+    auto transpose_tile = [&](int kt) {
+        const int stage = kt % STAGES;
+        const int buf = kt & 1;
+#pragma unroll
+        for (int f = 0; f < A_VECS; ++f) {
+            int k, m;
+            a_xpose_coord(tid, f, k, m);
+            const float4 v = *reinterpret_cast<const float4 *>(smem + ar_word(stage, m, k));
+            smem[as_word(buf, k + 0, m)] = v.x;
+            smem[as_word(buf, k + 1, m)] = v.y;
+            smem[as_word(buf, k + 2, m)] = v.z;
+            smem[as_word(buf, k + 3, m)] = v.w;
         }
     };
 
@@ -164,32 +165,33 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
     const int ra = frag_row0(tid);
     const int cb = frag_col0(tid);
 
-    if (KT > 0) {
-        load_a(0);
-        store_a(0);
-    }
+    // prologue: tiles 0 .. STAGES-2 in flight, tile 0 transposed
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < KT) load_b(s, s);
+        if (s < KT) issue_tile(s);
         cp_async_commit();
+    }
+    if (KT > 0) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        transpose_tile(0);
     }
 
     for (int kt = 0; kt < KT; ++kt) {
-        const bool more = kt + 1 < KT;
-        if (more) load_a(kt + 1);  // in flight during this tile's FMAs
-        cp_async_wait<STAGES - 2>();
-        __syncthreads();  // tile kt visible to all; stage (kt-1) free again
-        const int nk = kt + STAGES - 1;
-        if (nk < KT) load_b(nk, nk % STAGES);
+        cp_async_wait<STAGES - 3>();
+        __syncthreads();
+        if (kt + STAGES - 1 < KT) issue_tile(kt + STAGES - 1);
         cp_async_commit();
+        if (kt + 1 < KT) transpose_tile(kt + 1);
 
-        const float *st = smem + (kt % STAGES) * STAGE_FLOATS;
+        const int stage = kt % STAGES;
+        const int buf = kt & 1;
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(st + as_word(k, ra));
-            const float4 a1 = *reinterpret_cast<const float4 *>(st + as_word(k, ra + 16));
-            const float4 b0 = *reinterpret_cast<const float4 *>(st + bs_word(k, cb));
-            const float4 b1 = *reinterpret_cast<const float4 *>(st + bs_word(k, cb + 32));
+            const float4 a0 = *reinterpret_cast<const float4 *>(smem + as_word(buf, k, ra));
+            const float4 a1 = *reinterpret_cast<const float4 *>(smem + as_word(buf, k, ra + 16));
+            const float4 b0 = *reinterpret_cast<const float4 *>(smem + bs_word(stage, k, cb));
+            const float4 b1 = *reinterpret_cast<const float4 *>(smem + bs_word(stage, k, cb + 32));
             const float2 ap[TM / 2] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
                                        make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
             const float2 bp[TN / 2] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
@@ -204,7 +206,6 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
                     ad[i][j] = __ffma2_rn(ap[i], bq[j], ad[i][j]);
                 }
         }
-        if (more) store_a((kt + 1) % STAGES);  // published by the next barrier
     }
     cp_async_wait<0>();
 
@@ -370,17 +371,20 @@ extern "C" const char *sgemm_f32_status_string(int status) {
 extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n_stages) {
     int steps;
     switch (kind) {
-        case 0: steps = 4 * A_VECS; break;
+        case 0: steps = A_COPIES16; break;
         case 1: steps = b_copies<4>(); break;
         case 2:
         case 3: steps = 2 * BK; break;
         case 4: steps = b_copies<2>(); break;
         case 5: steps = b_copies<1>(); break;
+        case 6: steps = A_COPIES4; break;
+        case 7: steps = A_VECS; break;
+        case 8: steps = 4 * A_VECS; break;
         default: return SGEMM_ERR_INVALID_ARG;
     }
     if (n_warps) *n_warps = NT / 32;
     if (n_steps) *n_steps = steps;
-    if (n_stages) *n_stages = STAGES;
+    if (n_stages) *n_stages = (kind == 2 || kind == 8) ? 2 : STAGES;
     return SGEMM_OK;
 }
 
@@ -396,14 +400,17 @@ extern "C" int sgemm_f32_smem_request(int kind, int warp, int step, int stage, i
         const int tid = warp * 32 + lane;
         int word = 0, k = 0, x = 0;
         switch (kind) {
-            case 0: a_load_coord(tid, step >> 2, k, x); word = as_word(k + (step & 3), x); width = 4; break;
-            case 1: b_copy_coord<4>(tid, step, k, x); word = bs_word(k, x); width = 16; break;
-            case 4: b_copy_coord<2>(tid, step, k, x); word = bs_word(k, x); width = 8; break;
-            case 5: b_copy_coord<1>(tid, step, k, x); word = bs_word(k, x); width = 4; break;
-            case 2: word = as_word(step >> 1, frag_row0(tid) + 16 * (step & 1)); width = 16; break;
-            case 3: word = bs_word(step >> 1, frag_col0(tid) + 32 * (step & 1)); width = 16; break;
+            case 0: a_copy16_coord(tid, step, x, k); word = ar_word(stage, x, k); width = 16; break;
+            case 6: a_copy4_coord(tid, step, x, k); word = ar_word(stage, x, k); width = 4; break;
+            case 1: b_copy_coord<4>(tid, step, k, x); word = bs_word(stage, k, x); width = 16; break;
+            case 4: b_copy_coord<2>(tid, step, k, x); word = bs_word(stage, k, x); width = 8; break;
+            case 5: b_copy_coord<1>(tid, step, k, x); word = bs_word(stage, k, x); width = 4; break;
+            case 7: a_xpose_coord(tid, step, k, x); word = ar_word(stage, x, k); width = 16; break;
+            case 8: a_xpose_coord(tid, step >> 2, k, x); word = as_word(stage, k + (step & 3), x); width = 4; break;
+            case 2: word = as_word(stage, step >> 1, frag_row0(tid) + 16 * (step & 1)); width = 16; break;
+            case 3: word = bs_word(stage, step >> 1, frag_col0(tid) + 32 * (step & 1)); width = 16; break;
         }
-        byte_offset[lane] = (static_cast<int64_t>(stage) * STAGE_FLOATS + word) * 4;
+        byte_offset[lane] = static_cast<int64_t>(word) * 4;
     }
     if (width_bytes) *width_bytes = width;
     return SGEMM_OK;

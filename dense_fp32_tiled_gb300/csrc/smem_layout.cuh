@@ -7,23 +7,23 @@
 // (bank = (byte_address / 4) % 32; bank page, "地址怎样落到 bank") to exactly
 // the addresses the kernel issues.
 //
-// Layout (per pipeline stage):
-//   As: BK x BM floats, k-major ("transposed" A tile, as in the
-//       vectorised-load page's "shared memory transpose 的基本想法"): logical
-//       (k, m) lives at word k*BM + m.  Each warp's transposing stores write
-//       32 consecutive m of one k (one word per bank), and the fragment reads
-//       take 4 consecutive m (16-byte aligned), so neither padding nor a
-//       swizzle is needed: the thread->element map alone keeps every access
-//       conflict-free (the bank page's "Padding 之外的选择" point that the
-//       layout and the thread mapping are chosen together).
-//   Bs: BK x BN floats, row-major as in global memory (the page's
-//       "原样写" variant); fragment reads along n are contiguous.
+// Layout.  A ring of STAGES stages, each holding
+//   Bs : BK x BN floats, the B tile row-major as in global memory (the
+//        vectorised-load page's "原样写" variant); fragment reads along n
+//        are contiguous;
+//   Ar : BM x BK floats, the A tile as it arrives from global memory (row m,
+//        k contiguous), each 64-byte row split in four 16-byte groups stored
+//        at group g ^ ((m >> 1) & 3) (an XOR swizzle, "Padding 之外的选择" on
+//        the bank page: 16-byte copies of 8 rows and 128-bit reads of 32
+//        consecutive rows both spread over all banks);
+// followed by two buffers
+//   As : BK x BM floats, k-major ("transposed" A tile, the vectorised-load
+//        page's "shared memory transpose 的基本想法"): logical (k, m) at word
+//        k*BM + m.  Each thread moves its share of Ar to As one tile ahead of
+//        use (two 128-bit reads, eight 4-byte stores); each warp store writes
+//        32 consecutive m of one k (one word per bank) and the fragment reads
+//        take 4 consecutive m (16-byte aligned), so As needs no padding.
 //
-// 128-bit shared loads on sm_103 are served per half-warp; when lanes share
-// addresses (broadcast), each group of 4 consecutive lanes can receive at
-// most 2 distinct 16-byte groups per pass (measured with ncu, see the
-// oracle's bank model).  The lane grid below gives every quad 2 A groups and
-// 2 B groups, so each fragment read costs the minimum 2 passes.
 #pragma once
 
 #if defined(__CUDACC__)
@@ -38,37 +38,56 @@ constexpr int BM = 128;          // CTA tile rows (M)
 constexpr int BN = 128;          // CTA tile cols (N)
 constexpr int BK = 16;           // K depth of one pipeline stage
 constexpr int NT = 256;          // threads per CTA (8 warps)
-constexpr int STAGES = 3;        // shared-memory ring depth
+constexpr int STAGES = 4;        // copy ring depth (tiles in flight: STAGES - 1)
 constexpr int TM = 8;            // per-thread register tile rows
 constexpr int TN = 8;            // per-thread register tile cols
 constexpr int WARPS_M = 4;       // warp grid over the CTA tile
 constexpr int WARPS_N = 2;
 constexpr int WM = BM / WARPS_M; // 32 rows per warp
 constexpr int WN = BN / WARPS_N; // 64 cols per warp
-constexpr int A_STAGE_FLOATS = BK * BM;
 constexpr int B_STAGE_FLOATS = BK * BN;
-constexpr int STAGE_FLOATS = A_STAGE_FLOATS + B_STAGE_FLOATS;
-constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
-constexpr int A_VECS = BM * BK / (4 * NT);  // float4 of A a thread stages per k-tile
+constexpr int A_RAW_FLOATS = BM * BK;
+constexpr int STAGE_FLOATS = B_STAGE_FLOATS + A_RAW_FLOATS;
+constexpr int AS_FLOATS = BK * BM;
+constexpr int AS_BASE = STAGES * STAGE_FLOATS;  // first As buffer (floats)
+constexpr int SMEM_FLOATS = AS_BASE + 2 * AS_FLOATS;
+constexpr int SMEM_BYTES = SMEM_FLOATS * 4;
+constexpr int A_VECS = BM * BK / (4 * NT);  // float4 of A a thread transposes per tile
 
 static_assert(WARPS_M * WARPS_N * 32 == NT, "warp grid");
 static_assert(WM == 4 * TM && WN == 8 * TN, "lane grid 4 x 8");
-static_assert((STAGE_FLOATS * 4) % 128 == 0, "stages start on a bank row");
-static_assert(NT == 256 && BM == 128 && BK == 16, "A staging map covers 128 rows x 16 k");
+static_assert((STAGE_FLOATS * 4) % 128 == 0 && (AS_FLOATS * 4) % 128 == 0, "regions start on a bank row");
+static_assert(NT == 256 && BM == 128 && BK == 16, "A copy and transpose maps cover 128 rows x 16 k");
 
-// ---- shared-memory word offsets inside one stage -----------------------
-SG_HD int as_word(int k, int m) { return k * BM + m; }
-SG_HD int bs_word(int k, int n) { return A_STAGE_FLOATS + k * BN + n; }
+// ---- shared-memory word offsets (floats from the start of the block) --
+SG_HD int bs_word(int stage, int k, int n) { return stage * STAGE_FLOATS + k * BN + n; }
+SG_HD int ar_word(int stage, int m, int k) {
+    return stage * STAGE_FLOATS + B_STAGE_FLOATS + m * BK + 4 * ((k >> 2) ^ ((m >> 1) & 3)) + (k & 3);
+}
+SG_HD int as_word(int buf, int k, int m) { return AS_BASE + buf * AS_FLOATS + k * BM + m; }
 
 // ---- global->shared copy maps -----------------------------------------
-// A: staged through registers.  Warp w owns rows [32(w % 4), 32(w % 4) + 32)
-// and k columns [8(w / 4), 8(w / 4) + 8); float4 f (0 or 1) of lane l holds
-// A[m][k..k+3] with
+// A (16-byte class): copy q of thread t moves the 4 floats A[m][k..k+3] with
+//   m = 64q + t/4,  k = 4 (t % 4),
+// so a warp copies 8 rows x 64 contiguous bytes.
+SG_HD void a_copy16_coord(int tid, int q, int &m, int &k) {
+    m = 64 * q + (tid >> 2);
+    k = 4 * (tid & 3);
+}
+constexpr int A_COPIES16 = BM * BK / (4 * NT);
+// A (4-byte class, misaligned rows): copy q of thread t moves A[m][k] with
+//   m = 16q + t/16,  k = t % 16.
+SG_HD void a_copy4_coord(int tid, int q, int &m, int &k) {
+    m = 16 * q + (tid >> 4);
+    k = tid & 15;
+}
+constexpr int A_COPIES4 = BM * BK / NT;
+
+// A transpose: float4 f (0 or 1) of lane l in warp w is A[m][k..k+3] with
 //   m = 32(w % 4) + l,  k = 8(w / 4) + 4f,
-// so one warp load reads 32 rows x 16 bytes and the pair f = 0, 1 covers
-// whole 32-byte sectors.  The 4 components go to As by 4 scalar stores (the
-// transpose), component c to logical (k + c, m): 32 consecutive words.
-SG_HD void a_load_coord(int tid, int f, int &k, int &m) {
+// read from Ar (lanes on 32 consecutive rows) and written to As as 4 scalar
+// stores, component c to (k + c, m): 32 consecutive words per store.
+SG_HD void a_xpose_coord(int tid, int f, int &k, int &m) {
     const int w = tid >> 5, l = tid & 31;
     m = 32 * (w & 3) + l;
     k = 8 * (w >> 2) + 4 * f;

@@ -79,15 +79,19 @@ const char *sgemm_f32_status_string(int status);
  * sections "地址怎样落到 bank" and "为什么 double 和 float4 要另算").
  * Touches no GPU.
  *
- *   kind : 0 = A tile store into shared memory (4-byte transposing stores),
- *          1 = B tile copy into shared memory (16-byte copies; aligned class),
- *          2 = A fragment read (16-byte), 3 = B fragment read (16-byte),
- *          4 = B tile copy, 8-byte class, 5 = B tile copy, 4-byte class.
+ *   kind : 0 = A tile copy into the raw staging tile (16-byte copies),
+ *          6 = the same, 4-byte copies (misaligned A rows),
+ *          1 = B tile copy (16-byte copies), 4 = 8-byte, 5 = 4-byte class,
+ *          7 = A transpose read (raw tile -> registers, 16-byte),
+ *          8 = A transpose store (registers -> k-major tile, 4-byte),
+ *          2 = A fragment read (16-byte), 3 = B fragment read (16-byte).
  *   warp : warp index in the CTA, 0 <= warp < *n_warps.
- *   step : which instruction of that warp, 0 <= step < *n_steps (for copies:
- *          the copy or store index within one stage; for reads: 2*k + half,
- *          k < BK).
- *   stage: pipeline stage the access targets, 0 <= stage < *n_stages.
+ *   step : which instruction of that warp, 0 <= step < *n_steps (copies,
+ *          transpose reads and stores: index within one tile; fragment
+ *          reads: 2*k + half, k < BK).
+ *   stage: ring stage (copies, transpose reads, B reads) or k-major buffer
+ *          (A reads, transpose stores) the access targets, 0 <= stage <
+ *          *n_stages.
  *   byte_offset[32] (out): shared-memory byte offset each lane touches,
  *          relative to the start of the dynamic shared-memory block.
  *   width_bytes (out): bytes each lane moves (4, 8 or 16).

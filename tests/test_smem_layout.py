@@ -13,8 +13,9 @@ import pytest
 import dense_fp32_tiled_gb300 as sg
 from dense_fp32_tiled_gb300 import build as sg_build
 
-KINDS = {0: "A copy (4 B)", 1: "B copy (16 B)", 2: "A fragment read", 3: "B fragment read",
-         4: "B copy (8 B)", 5: "B copy (4 B)"}
+KINDS = {0: "A copy (16 B)", 1: "B copy (16 B)", 2: "A fragment read", 3: "B fragment read",
+         4: "B copy (8 B)", 5: "B copy (4 B)", 6: "A copy (4 B)", 7: "A transpose read",
+         8: "A transpose store"}
 
 
 @pytest.fixture(scope="module")
@@ -34,8 +35,11 @@ def test_every_access_conflict_free(lib, oracle_lib, kind):
                 assert r["wavefronts"] == r["ideal"], (KINDS[kind], stage, warp, step, r)
 
 
-@pytest.mark.parametrize("kind,tile_words", [(0, 16 * 128), (1, 16 * 128), (4, 16 * 128), (5, 16 * 128)])
-def test_copies_fill_each_tile_word_once(lib, kind, tile_words):
+TILE = 16 * 128
+
+
+@pytest.mark.parametrize("kind", [0, 1, 4, 5, 6, 8])
+def test_copies_and_stores_fill_each_tile_word_once(lib, kind):
     n_warps, n_steps, _ = sg.smem_shape(kind)
     words = []
     for warp in range(n_warps):
@@ -43,20 +47,45 @@ def test_copies_fill_each_tile_word_once(lib, kind, tile_words):
             offs, width = sg.smem_request(kind, warp, step, 0)
             for o in offs:
                 words += [o // 4 + w for w in range(width // 4)]
-    assert len(words) == tile_words and len(set(words)) == tile_words
+    assert len(words) == TILE and len(set(words)) == TILE
+    lo = min(words)
+    assert max(words) - lo == TILE - 1  # one contiguous tile region
 
 
-def test_fragment_reads_stay_inside_their_tile(lib):
-    # A reads land in the A part of a stage, B reads in the B part
-    a_words = set(range(0, 16 * 128))
-    b_words = set(range(16 * 128, 2 * 16 * 128))
-    for kind, region in ((2, a_words), (3, b_words)):
+def test_transpose_reads_what_the_copies_wrote(lib):
+    # the transpose reads every word of the raw A tile exactly once
+    def region(kind):
         n_warps, n_steps, _ = sg.smem_shape(kind)
+        out = []
         for warp in range(n_warps):
             for step in range(n_steps):
                 offs, width = sg.smem_request(kind, warp, step, 0)
+                out += [o // 4 + w for o in offs for w in range(width // 4)]
+        return out
+    copied = region(0)
+    read = region(7)
+    assert sorted(copied) == sorted(read) and len(set(read)) == TILE
+    assert sorted(region(6)) == sorted(copied)
+
+
+def test_fragment_reads_stay_inside_their_tile(lib):
+    # A reads land in the As buffer the transpose stores fill, B reads in B's region
+    def region(kind):
+        n_warps, n_steps, _ = sg.smem_shape(kind)
+        out = set()
+        for warp in range(n_warps):
+            for step in range(n_steps):
+                offs, width = sg.smem_request(kind, warp, step, 0)
+                out |= {o // 4 + w for o in offs for w in range(width // 4)}
+        return out
+    assert region(2) == region(8)
+    assert region(3) == region(1)
+    for kind in (2, 3):
+        n_warps, n_steps, _ = sg.smem_shape(kind)
+        for warp in range(n_warps):
+            for step in range(n_steps):
+                offs, _ = sg.smem_request(kind, warp, step, 0)
                 assert all(o % 16 == 0 for o in offs)
-                assert all(o // 4 + w in region for o in offs for w in range(4))
 
 
 def test_bad_query_rejected(lib):
