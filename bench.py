@@ -37,8 +37,8 @@ FMA_PER_CLK_PER_SM = 128  # FP32 CUDA-core lanes per SM (4 partitions x 32)
 def _args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
@@ -62,13 +62,14 @@ def _workload(name):
 
 class ClockSampler:
     """nvidia-smi clocks/throttle sampling during the timed region."""
-    Q = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, uuid: str | None):
         self.uuid = uuid
         self.proc = None
+        self.t0 = self.t1 = None  # wall-clock bounds of the timed region
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
 
     def __enter__(self):
@@ -76,7 +77,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                                          "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except OSError:
             self.proc = None
@@ -94,27 +95,39 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
+        rows, inside = [], []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
-                if self.uuid and parts[0] != self.uuid:
+                if self.uuid and parts[1] != self.uuid:
                     continue
                 rows.append(parts)
-        if not rows:
+                try:
+                    t = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    t += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                except (ValueError, IndexError):
+                    t = None
+                if t is not None and self.t0 is not None and self.t0 - 0.15 <= t <= self.t1 + 0.15:
+                    inside.append(parts)
+        use = inside or rows
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[2]) for r in use) if v is not None]
+        mx = [v for v in (num(r[3]) for r in use) if v is not None]
+        pw = [v for v in (num(r[4]) for r in use) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
-        # samples taken while the GPU was busy: power well above idle
-        busy = [s for s, p in zip(sm, pw)] if pw else sm
-        return {"sm_mhz": statistics.median(busy) if busy else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "power_w_max": max(pw) if pw else None, "samples": len(rows)}
+        reasons = sorted({n for r in use for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "power_w_max": max(pw) if pw else None,
+                "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
 def _traffic_from_profile(stamp: str):
@@ -259,6 +272,7 @@ def main():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
+        clk.t0 = time.time()
         t_wall = time.perf_counter()
         for i in range(a.steps):
             flush.zero_()
@@ -269,6 +283,7 @@ def main():
         if world > 1:
             dist.barrier()
         t_wall = time.perf_counter() - t_wall
+        clk.t1 = time.time()
     times = [st.elapsed_time(en) for st, en in zip(starts, ends)]
     ms = statistics.mean(times)
     if world > 1:
@@ -285,7 +300,7 @@ def main():
         hA = torch.from_numpy(A_h).pin_memory()
         hB = torch.from_numpy(B_h).pin_memory()
         hC = torch.empty(c_elems, dtype=torch.float32).pin_memory()
-        e_steps = max(3, a.steps // 2)
+        e_steps = max(3, min(50, a.steps // 2))
         for _ in range(2):
             A.copy_(hA, non_blocking=True); B.copy_(hB, non_blocking=True); step()
             hC.copy_(C, non_blocking=True)
