@@ -37,6 +37,10 @@ def load_library():
     i32, p, i64p = ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64)
     lib.sgemm_f32.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p]
     lib.sgemm_f32.restype = i32
+    lib.sgemm_f32_ws.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p, ctypes.c_size_t, p]
+    lib.sgemm_f32_ws.restype = i32
+    lib.sgemm_f32_workspace_size.argtypes = [i32, i32, i32]
+    lib.sgemm_f32_workspace_size.restype = ctypes.c_size_t
     lib.sgemm_f32_status_string.argtypes = [i32]
     lib.sgemm_f32_status_string.restype = ctypes.c_char_p
     ip = ctypes.POINTER(ctypes.c_int)
@@ -69,6 +73,20 @@ def sgemm_f32(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int
                                     ctypes.c_void_p(int(stream) or None))
 
 
+def sgemm_f32_ws(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                 workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    """Raw C-ABI call of the workspace variant; returns the status code."""
+    return load_library().sgemm_f32_ws(int(M), int(N), int(K), ctypes.c_void_p(int(A) or None), int(lda),
+                                       ctypes.c_void_p(int(B) or None), int(ldb),
+                                       ctypes.c_void_p(int(C) or None), int(ldc),
+                                       ctypes.c_void_p(int(workspace) or None), int(workspace_bytes),
+                                       ctypes.c_void_p(int(stream) or None))
+
+
+def workspace_size(M: int, N: int, K: int) -> int:
+    return int(load_library().sgemm_f32_workspace_size(int(M), int(N), int(K)))
+
+
 def smem_shape(kind: int):
     nw, ns, nst = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     st = load_library().sgemm_f32_smem_shape(kind, ctypes.byref(nw), ctypes.byref(ns), ctypes.byref(nst))
@@ -99,11 +117,28 @@ def _matrix_args(t, rows: int, cols: int, name: str):
     return t.data_ptr(), max(ld, cols, 1)
 
 
-def sgemm(A, B, out=None, stream=None):
-    """C = A @ B for CUDA float32 tensors (row-major, any row stride) via sgemm_f32.
+_workspaces = {}
+
+
+def _workspace(device, nbytes: int):
+    """A per-device scratch buffer for sgemm_f32_ws, grown on demand (torch memory)."""
+    import torch
+    buf = _workspaces.get(device)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 1 << 12), dtype=torch.uint8, device=device)
+        _workspaces[device] = buf
+    return buf
+
+
+def sgemm(A, B, out=None, stream=None, balanced=True):
+    """C = A @ B for CUDA float32 tensors (row-major, any row stride) via the C ABI.
 
     ``out`` (M x N, row-major) is written when given, else allocated.  Runs on
     ``stream`` (a torch.cuda.Stream) or the current stream; asynchronous.
+    With ``balanced`` (default) the call goes through sgemm_f32_ws with a
+    per-device workspace, which enables the stream-K schedule; otherwise
+    through sgemm_f32.  Calls that share the cached workspace must run in
+    stream order (the default when one stream is used).
     """
     import torch
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
@@ -117,7 +152,13 @@ def sgemm(A, B, out=None, stream=None):
     c, ldc = _matrix_args(out, M, N, "out")
     s = (stream or torch.cuda.current_stream(A.device)).cuda_stream
     with torch.cuda.device(A.device):
-        st = sgemm_f32(M, N, K, a, lda, b, ldb, c, ldc, s)
+        if balanced:
+            nbytes = workspace_size(M, N, K)
+            ws = _workspace(A.device, nbytes) if nbytes else None
+            st = sgemm_f32_ws(M, N, K, a, lda, b, ldb, c, ldc, ws.data_ptr() if ws is not None else 0,
+                              ws.numel() if ws is not None else 0, s)
+        else:
+            st = sgemm_f32(M, N, K, a, lda, b, ldb, c, ldc, s)
     if st != SGEMM_OK:
         raise SgemmError(st)
     return out

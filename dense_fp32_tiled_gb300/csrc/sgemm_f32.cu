@@ -61,9 +61,41 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(PENDING) : "memory");
 }
 
-// One CTA: C tile (tm, tn).  VA = A copy width in floats (4 or 1), VB = B
-// copy width in floats (4, 2 or 1), vc = C store width in floats (4, 2 or 1),
-// all chosen on the host from pointer and leading-dimension alignment.
+struct Problem {
+    int M, N, K;
+    const float *__restrict__ A;
+    int lda;
+    const float *__restrict__ B;
+    int ldb;
+    float *__restrict__ C;
+    int ldc;
+    int tiles_m, tiles_n;
+    int vc;  // C store width in floats (4, 2 or 1)
+};
+
+// The 8 x 8 register tile, paired for the packed FP32 FMA (fma.rn.f32x2).
+// With rows r = 2i+{0,1} and cols c = 2j+{0,1} of the tile,
+//   dg[i][j] = (acc[2i][2j],   acc[2i+1][2j+1])  += (a_2i, a_2i+1) * (b_2j,   b_2j+1)
+//   ad[i][j] = (acc[2i][2j+1], acc[2i+1][2j])    += (a_2i, a_2i+1) * (b_2j+1, b_2j)
+// so both operands are natural register pairs of the 128-bit fragment reads
+// (plus one swapped copy of each B pair): 32 packed FMAs per k.
+struct Acc {
+    float2 dg[TM / 2][TN / 2], ad[TM / 2][TN / 2];
+};
+
+__device__ __forceinline__ void acc_zero(Acc &acc) {
+#pragma unroll
+    for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j) {
+            acc.dg[i][j] = make_float2(0.0f, 0.0f);
+            acc.ad[i][j] = make_float2(0.0f, 0.0f);
+        }
+}
+
+// Accumulates the product of the CTA's C tile (m0, n0) over K tiles
+// [kt0, kt1) into acc.  VA = A copy width in floats (4 or 1), VB = B copy
+// width in floats (4, 2 or 1), chosen on the host from alignment.
 //
 // Pipeline (one __syncthreads per K tile): at iteration kt
 //   1. wait until the copy group of tile kt+1 has landed (own copies), then
@@ -72,19 +104,13 @@ __device__ __forceinline__ void cp_async_wait() {
 //   2. issue the copies of tile kt+STAGES-1 into the stage tile kt-1 used;
 //   3. transpose tile kt+1's raw A into the As buffer tile kt-1 used;
 //   4. 16 k steps of fragment reads and packed FMAs on tile kt.
+// On return every copy has landed and every thread is past its last shared
+// read, so the caller may start another range at once.
 template <int VA, int VB>
-__global__ void __launch_bounds__(NT, 2)
-sgemm_f32_tiled_kernel(const int M, const int N, const int K,
-                       const float *__restrict__ A, const int lda,
-                       const float *__restrict__ B, const int ldb,
-                       float *__restrict__ C, const int ldc,
-                       const int tiles_m, const int tiles_n, const int vc) {
-    extern __shared__ __align__(128) float smem[];
+__device__ __forceinline__ void mma_k_range(const Problem &p, const int m0, const int n0, const int kt0,
+                                            const int kt1, float *smem, Acc &acc) {
     const int tid = threadIdx.x;
-    int tm, tn;
-    tile_of(blockIdx.x, tiles_m, tiles_n, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN;
-    const int KT = (K + BK - 1) / BK;
+    const int K = p.K, M = p.M, N = p.N;
     const uint32_t sbase = smem_u32(smem);
 
     // ---- A copies (global -> raw staging tile).  Rows past M and columns
@@ -94,8 +120,8 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
     if constexpr (VA == 4) a_copy16_coord(tid, 0, a_m0, a_k);
     else a_copy4_coord(tid, 0, a_m0, a_k);
     constexpr int A_ROW_STEP = VA == 4 ? 64 : 16;  // rows between a thread's copies
-    const float *a_base = A + static_cast<size_t>(m0 + a_m0 < M ? m0 + a_m0 : 0) * lda + a_k;
-    const size_t a_step = static_cast<size_t>(A_ROW_STEP) * lda;
+    const float *a_base = p.A + static_cast<size_t>(m0 + a_m0 < M ? m0 + a_m0 : 0) * p.lda + a_k;
+    const size_t a_step = static_cast<size_t>(A_ROW_STEP) * p.lda;
 
     // ---- B copies (global -> shared, row-major tile)
     constexpr int NB = b_copies<VB>();
@@ -104,7 +130,7 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
     const int b_col = n0 + b_n;
     const int b_valid = N - b_col;  // valid floats from b_col on
     const uint32_t b_bytes = b_valid >= VB ? VB * 4u : (b_valid > 0 ? b_valid * 4u : 0u);
-    const float *b_colp = B + (b_valid > 0 ? b_col : 0);
+    const float *b_colp = p.B + (b_valid > 0 ? b_col : 0);
 
     auto issue_tile = [&](int kt) {
         const int stage = kt % STAGES;
@@ -117,7 +143,7 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
             const int kg = kb + k;
             const int left = K - kg;  // valid floats from kg on
             uint32_t bytes = (m0 + m < M && left > 0) ? (left >= VA ? VA * 4u : left * 4u) : 0u;
-            const float *src = bytes ? a_base + q * a_step + kb : A;
+            const float *src = bytes ? a_base + q * a_step + kb : p.A;
             cp_async<VA * 4>(sbase + ar_word(stage, m, k) * 4, src, bytes);
         }
 #pragma unroll
@@ -126,7 +152,7 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
             b_copy_coord<VB>(tid, q, k, n);
             const int kg = kb + k;
             const bool ok = kg < K && b_bytes != 0;
-            const float *src = ok ? b_colp + static_cast<size_t>(kg) * ldb : B;
+            const float *src = ok ? b_colp + static_cast<size_t>(kg) * p.ldb : p.B;
             cp_async<VB * 4>(sbase + bs_word(stage, k, n) * 4, src, ok ? b_bytes : 0u);
         }
     };
@@ -147,42 +173,27 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
         }
     };
 
-    // ---- accumulators, paired for the packed FP32 FMA (fma.rn.f32x2).  With
-    // rows r = 2i+{0,1} and cols c = 2j+{0,1} of the 8 x 8 register tile,
-    //   dg[i][j] = (acc[2i][2j],   acc[2i+1][2j+1])  += (a_2i, a_2i+1) * (b_2j,   b_2j+1)
-    //   ad[i][j] = (acc[2i][2j+1], acc[2i+1][2j])    += (a_2i, a_2i+1) * (b_2j+1, b_2j)
-    // so both operands are natural register pairs of the 128-bit fragment
-    // reads (plus one swapped copy of each B pair): 32 packed FMAs per k.
-    float2 dg[TM / 2][TN / 2], ad[TM / 2][TN / 2];
-#pragma unroll
-    for (int i = 0; i < TM / 2; ++i)
-#pragma unroll
-        for (int j = 0; j < TN / 2; ++j) {
-            dg[i][j] = make_float2(0.0f, 0.0f);
-            ad[i][j] = make_float2(0.0f, 0.0f);
-        }
-
     const int ra = frag_row0(tid);
     const int cb = frag_col0(tid);
 
-    // prologue: tiles 0 .. STAGES-2 in flight, tile 0 transposed
+    // prologue: tiles kt0 .. kt0+STAGES-2 in flight, tile kt0 transposed
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < KT) issue_tile(s);
+        if (kt0 + s < kt1) issue_tile(kt0 + s);
         cp_async_commit();
     }
-    if (KT > 0) {
+    if (kt0 < kt1) {
         cp_async_wait<STAGES - 2>();
         __syncthreads();
-        transpose_tile(0);
+        transpose_tile(kt0);
     }
 
-    for (int kt = 0; kt < KT; ++kt) {
+    for (int kt = kt0; kt < kt1; ++kt) {
         cp_async_wait<STAGES - 3>();
         __syncthreads();
-        if (kt + STAGES - 1 < KT) issue_tile(kt + STAGES - 1);
+        if (kt + STAGES - 1 < kt1) issue_tile(kt + STAGES - 1);
         cp_async_commit();
-        if (kt + 1 < KT) transpose_tile(kt + 1);
+        if (kt + 1 < kt1) transpose_tile(kt + 1);
 
         const int stage = kt % STAGES;
         const int buf = kt & 1;
@@ -202,38 +213,153 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
             for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
                 for (int j = 0; j < TN / 2; ++j) {
-                    dg[i][j] = __ffma2_rn(ap[i], bp[j], dg[i][j]);
-                    ad[i][j] = __ffma2_rn(ap[i], bq[j], ad[i][j]);
+                    acc.dg[i][j] = __ffma2_rn(ap[i], bp[j], acc.dg[i][j]);
+                    acc.ad[i][j] = __ffma2_rn(ap[i], bq[j], acc.ad[i][j]);
                 }
         }
     }
     cp_async_wait<0>();
+}
 
-    // ---- epilogue: guarded stores, vectorised where the C class allows
+// Writes the register tile to C tile (m0, n0) with guarded stores,
+// vectorised where C's alignment class allows.  With ADD_PARTIAL, the value
+// already in C (a partial sum left there by another CTA) is read back from
+// L2 and added first: final = this CTA's sum + the other part.
+template <bool ADD_PARTIAL>
+__device__ __forceinline__ void store_tile(const Problem &p, const int m0, const int n0, const Acc &acc) {
+    const int tid = threadIdx.x;
+    const int cb = frag_col0(tid);
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
         const int row = m0 + frag_row(tid, i);
-        if (row >= M) continue;
-        float *crow = C + static_cast<size_t>(row) * ldc;
+        if (row >= p.M) continue;
+        float *crow = p.C + static_cast<size_t>(row) * p.ldc;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = n0 + cb + 32 * h;
             // row i = 2*ip + r of the tile; cols 4h .. 4h+3 = pairs jp = 2h, 2h+1
             const int ip = i >> 1, r = i & 1;
-            const float2 d0 = dg[ip][2 * h], x0 = ad[ip][2 * h];
-            const float2 d1 = dg[ip][2 * h + 1], x1 = ad[ip][2 * h + 1];
-            const float v[4] = {r ? x0.y : d0.x, r ? d0.y : x0.x, r ? x1.y : d1.x, r ? d1.y : x1.x};
-            if (col + 3 < N && vc == 4) {
+            const float2 d0 = acc.dg[ip][2 * h], x0 = acc.ad[ip][2 * h];
+            const float2 d1 = acc.dg[ip][2 * h + 1], x1 = acc.ad[ip][2 * h + 1];
+            float v[4] = {r ? x0.y : d0.x, r ? d0.y : x0.x, r ? x1.y : d1.x, r ? d1.y : x1.x};
+            if (col + 3 < p.N && p.vc == 4) {
+                if (ADD_PARTIAL) {
+                    const float4 o = __ldcg(reinterpret_cast<const float4 *>(crow + col));
+                    v[0] += o.x; v[1] += o.y; v[2] += o.z; v[3] += o.w;
+                }
                 *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
-            } else if (col + 3 < N && vc == 2) {
+            } else if (col + 3 < p.N && p.vc == 2) {
+                if (ADD_PARTIAL) {
+                    const float2 o0 = __ldcg(reinterpret_cast<const float2 *>(crow + col));
+                    const float2 o1 = __ldcg(reinterpret_cast<const float2 *>(crow + col + 2));
+                    v[0] += o0.x; v[1] += o0.y; v[2] += o1.x; v[3] += o1.y;
+                }
                 *reinterpret_cast<float2 *>(crow + col) = make_float2(v[0], v[1]);
                 *reinterpret_cast<float2 *>(crow + col + 2) = make_float2(v[2], v[3]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (col + e < N) crow[col + e] = v[e];
+                    if (col + e < p.N) crow[col + e] = ADD_PARTIAL ? v[e] + __ldcg(crow + col + e) : v[e];
             }
         }
+    }
+}
+
+// Data-parallel schedule: one CTA per C tile, the whole K range.
+template <int VA, int VB>
+__global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p) {
+    extern __shared__ __align__(128) float smem[];
+    int tm, tn;
+    tile_of(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
+    Acc acc;
+    acc_zero(acc);
+    mma_k_range<VA, VB>(p, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, smem, acc);
+    store_tile<false>(p, tm * BM, tn * BN, acc);
+}
+
+// ---- flags between CTAs (stream-K fix-up) ------------------------------
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
+constexpr unsigned kSpinLimit = 1u << 24;  // x ~64 ns sleeps: about a second, then give up
+
+// Stream-K schedule with a data-parallel head.  A persistent, co-resident
+// grid of G CTAs first computes tiles 0 .. dp_tiles-1 one whole tile at a time
+// (tile c, c+G, ...: CTAs running together work on neighbouring tiles, which
+// keeps A and B panels in L2), then splits the (tile, K tile) iterations of
+// the remaining T - dp_tiles tiles into G equal contiguous ranges, so every
+// CTA ends with the same amount of FMA work whatever T mod G is.  A tile cut
+// by a range boundary is shared by exactly two CTAs (more remaining tiles
+// than CTAs makes every range longer than a tile):
+//   * the CTA whose range starts inside the tile (its first segment, k from
+//     the cut to the end) stores its partial sums into the tile of C itself
+//     and raises flags[tile];
+//   * the CTA whose range ends inside the tile (its last segment, k from 0
+//     to the cut) waits for the flag, adds the partial to its own sums and
+//     stores the result, then lowers the flag for the next call.
+// The producer's segment comes first in its range, so no wait can form a
+// cycle.  A wait longer than kSpinLimit polls records error bit 1 in
+// flags[T] and stores without the partial: a wrong result, never a hang.
+template <int VA, int VB>
+__global__ void __launch_bounds__(NT, 2)
+sgemm_f32_streamk_kernel(const Problem p, const int dp_tiles, unsigned *flags) {
+    extern __shared__ __align__(128) float smem[];
+    const int KT = (p.K + BK - 1) / BK;
+    const int T = p.tiles_m * p.tiles_n;
+    const int G = gridDim.x;
+    for (int lin = blockIdx.x; lin < dp_tiles; lin += G) {
+        int tm, tn;
+        tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
+        Acc acc;
+        acc_zero(acc);
+        mma_k_range<VA, VB>(p, tm * BM, tn * BN, 0, KT, smem, acc);
+        store_tile<false>(p, tm * BM, tn * BN, acc);
+        __syncthreads();  // shared memory free for the next tile
+    }
+    const long long total_iters = static_cast<long long>(T - dp_tiles) * KT;
+    const long long base = static_cast<long long>(dp_tiles) * KT;
+    const long long it_end = base + total_iters * (blockIdx.x + 1) / G;
+    long long it = base + total_iters * blockIdx.x / G;
+    while (it < it_end) {
+        const int lin = static_cast<int>(it / KT);
+        const int k0 = static_cast<int>(it % KT);
+        const int k1 = static_cast<int>(k0 + (it_end - it) < KT ? k0 + (it_end - it) : KT);
+        int tm, tn;
+        tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
+        Acc acc;
+        acc_zero(acc);
+        mma_k_range<VA, VB>(p, tm * BM, tn * BN, k0, k1, smem, acc);
+        if (k0 == 0 && k1 == KT) {
+            store_tile<false>(p, tm * BM, tn * BN, acc);
+        } else if (k0 > 0) {
+            store_tile<false>(p, tm * BM, tn * BN, acc);  // partial sums for k >= cut
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                st_release(flags + lin, 1u);
+            }
+        } else {
+            if (threadIdx.x == 0) {
+                unsigned spins = 0;
+                while (ld_acquire(flags + lin) == 0u) {
+                    if (++spins > kSpinLimit) {
+                        atomicOr(flags + T, 1u);
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            __syncthreads();
+            store_tile<true>(p, tm * BM, tn * BN, acc);
+            if (threadIdx.x == 0) flags[lin] = 0u;
+        }
+        it += k1 - k0;
+        __syncthreads();  // shared memory free for the next range
     }
 }
 
@@ -242,38 +368,59 @@ sgemm_f32_tiled_kernel(const int M, const int N, const int K,
 // ---------------------------------------------------------------------------
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-int g_device_state[kMaxDevices];  // 0 = not yet set up, 1 = ready, <0 = status
+constexpr int kVariants = 6;  // (VA, VB) in {4, 1} x {4, 2, 1}
+using DpKernel = void (*)(Problem);
+using SkKernel = void (*)(Problem, int, unsigned *);
+const DpKernel kDp[kVariants] = {sgemm_f32_tiled_kernel<4, 4>, sgemm_f32_tiled_kernel<4, 2>,
+                                 sgemm_f32_tiled_kernel<4, 1>, sgemm_f32_tiled_kernel<1, 4>,
+                                 sgemm_f32_tiled_kernel<1, 2>, sgemm_f32_tiled_kernel<1, 1>};
+const SkKernel kSk[kVariants] = {sgemm_f32_streamk_kernel<4, 4>, sgemm_f32_streamk_kernel<4, 2>,
+                                 sgemm_f32_streamk_kernel<4, 1>, sgemm_f32_streamk_kernel<1, 4>,
+                                 sgemm_f32_streamk_kernel<1, 2>, sgemm_f32_streamk_kernel<1, 1>};
 
-int setup_device(int dev) {
+struct DeviceInfo {
+    int state;                    // 0 = not yet set up, 1 = ready, < 0 = status
+    int sms;                      // multiprocessors
+    int sk_per_sm[kVariants];     // co-resident stream-K CTAs per SM
+};
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+int setup_device(int dev, DeviceInfo *out) {
     if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_device_state[dev] != 0) return g_device_state[dev] > 0 ? SGEMM_OK : g_device_state[dev];
-    int major = 0, minor = 0;
-    int st = SGEMM_OK;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        major != 10 || minor != 3) {
-        st = SGEMM_ERR_DEVICE;
-    } else {
-        const void *kernels[] = {reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<4, 4>),
-                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<4, 2>),
-                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<4, 1>),
-                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<1, 4>),
-                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<1, 2>),
-                                 reinterpret_cast<const void *>(&sgemm_f32_tiled_kernel<1, 1>)};
-        for (const void *k : kernels) {
-            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
-                st = SGEMM_ERR_DEVICE;
-                break;
+    DeviceInfo &d = g_dev[dev];
+    if (d.state == 0) {
+        int major = 0, minor = 0, st = SGEMM_OK;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || major != 10 ||
+            minor != 3) {
+            st = SGEMM_ERR_DEVICE;
+        } else {
+            for (int v = 0; v < kVariants && st == SGEMM_OK; ++v) {
+                const void *fns[2] = {reinterpret_cast<const void *>(kDp[v]), reinterpret_cast<const void *>(kSk[v])};
+                for (const void *f : fns) {
+                    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+                            cudaSuccess ||
+                        cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
+                        st = SGEMM_ERR_DEVICE;
+                        break;
+                    }
+                }
+                if (st == SGEMM_OK &&
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sk_per_sm[v], kSk[v], NT, SMEM_BYTES) !=
+                        cudaSuccess)
+                    st = SGEMM_ERR_DEVICE;
             }
         }
+        if (st != SGEMM_OK) (void)cudaGetLastError();  // do not leave our failure sticky for the caller
+        d.state = st == SGEMM_OK ? 1 : st;
     }
-    if (st != SGEMM_OK) (void)cudaGetLastError();  // do not leave our failure sticky for the caller
-    g_device_state[dev] = st == SGEMM_OK ? 1 : st;
-    return st;
+    if (d.state < 0) return d.state;
+    *out = d;
+    return SGEMM_OK;
 }
 
 // Largest v in {4, 2, 1} floats such that the pointer and every row start are
@@ -285,10 +432,10 @@ int vector_class(const void *p, long long ld) {
     return 1;
 }
 
-bool ranges_overlap(const void *p, long long p_elems, const void *q, long long q_elems) {
-    if (p_elems <= 0 || q_elems <= 0) return false;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + static_cast<uintptr_t>(p_elems) * 4;
-    const uintptr_t b0 = reinterpret_cast<uintptr_t>(q), b1 = b0 + static_cast<uintptr_t>(q_elems) * 4;
+bool ranges_overlap(const void *p, long long p_bytes, const void *q, long long q_bytes) {
+    if (p_bytes <= 0 || q_bytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + static_cast<uintptr_t>(p_bytes);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(q), b1 = b0 + static_cast<uintptr_t>(q_bytes);
     return a0 < b1 && b0 < a1;
 }
 
@@ -296,22 +443,12 @@ long long extent(long long rows, long long cols, long long ld) {
     return (rows == 0 || cols == 0) ? 0 : (rows - 1) * ld + cols;
 }
 
-template <int VA, int VB>
-cudaError_t launch(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
-                   int tiles_m, int tiles_n, int vc, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles_m * tiles_n));
-    cfg.blockDim = dim3(NT);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, sgemm_f32_tiled_kernel<VA, VB>, M, N, K, A, lda, B, ldb, C, ldc, tiles_m,
-                              tiles_n, vc);
+long long tile_count(int M, int N) {
+    return ((static_cast<long long>(M) + BM - 1) / BM) * ((static_cast<long long>(N) + BN - 1) / BN);
 }
 
-}  // namespace
-
-extern "C" int sgemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
-                         cudaStream_t stream) {
+// Host-side argument checks shared by every entry point; touches no GPU.
+int check_args(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const float *C, int ldc) {
     if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
     if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_LD;
     if (M == 0 || N == 0) return SGEMM_OK;
@@ -320,38 +457,112 @@ extern "C" int sgemm_f32(int M, int N, int K, const float *A, int lda, const flo
     if (reinterpret_cast<uintptr_t>(C) % 4 != 0) return SGEMM_ERR_INVALID_ARG;
     if (K > 0 && (reinterpret_cast<uintptr_t>(A) % 4 != 0 || reinterpret_cast<uintptr_t>(B) % 4 != 0))
         return SGEMM_ERR_INVALID_ARG;
-    const long long c_ext = extent(M, N, ldc);
-    if (K > 0 && (ranges_overlap(C, c_ext, A, extent(M, K, lda)) || ranges_overlap(C, c_ext, B, extent(K, N, ldb))))
+    const long long c_bytes = 4 * extent(M, N, ldc);
+    if (K > 0 && (ranges_overlap(C, c_bytes, A, 4 * extent(M, K, lda)) ||
+                  ranges_overlap(C, c_bytes, B, 4 * extent(K, N, ldb))))
         return SGEMM_ERR_ALIAS;
-    const long long tiles_m = (static_cast<long long>(M) + BM - 1) / BM;
-    const long long tiles_n = (static_cast<long long>(N) + BN - 1) / BN;
-    if (tiles_m * tiles_n > INT_MAX) return SGEMM_ERR_INVALID_DIM;
+    if (tile_count(M, N) > INT_MAX) return SGEMM_ERR_INVALID_DIM;
+    return SGEMM_OK;
+}
 
+// Runs one product whose arguments passed check_args (M, N > 0).  Uses the
+// stream-K schedule when `flags` holds at least tiles + 1 words and the tile
+// count does not divide evenly over the co-resident CTAs; else one CTA per tile.
+int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+        unsigned *flags, size_t flag_bytes, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         (void)cudaGetLastError();
         return SGEMM_ERR_DEVICE;
     }
-    const int st = setup_device(dev);
+    DeviceInfo info;
+    const int st = setup_device(dev, &info);
     if (st != SGEMM_OK) return st;
 
     const int va = K > 0 ? (vector_class(A, lda) == 4 ? 4 : 1) : 4;
     const int vb = K > 0 ? vector_class(B, ldb) : 4;
-    const int vc = vector_class(C, ldc);
-    const int tm_ = static_cast<int>(tiles_m), tn_ = static_cast<int>(tiles_n);
-    cudaError_t err;
-#define SGEMM_LAUNCH(VA_, VB_) launch<VA_, VB_>(M, N, K, A, lda, B, ldb, C, ldc, tm_, tn_, vc, stream)
-    if (va == 4) {
-        err = vb == 4 ? SGEMM_LAUNCH(4, 4) : vb == 2 ? SGEMM_LAUNCH(4, 2) : SGEMM_LAUNCH(4, 1);
-    } else {
-        err = vb == 4 ? SGEMM_LAUNCH(1, 4) : vb == 2 ? SGEMM_LAUNCH(1, 2) : SGEMM_LAUNCH(1, 1);
+    const int v = (va == 4 ? 0 : 3) + (vb == 4 ? 0 : vb == 2 ? 1 : 2);
+    Problem p;
+    p.M = M; p.N = N; p.K = K; p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
+    p.tiles_m = (M + BM - 1) / BM;
+    p.tiles_n = (N + BN - 1) / BN;
+    p.vc = vector_class(C, ldc);
+    const long long T = static_cast<long long>(p.tiles_m) * p.tiles_n;
+    const long long G = static_cast<long long>(info.sk_per_sm[v]) * info.sms;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaError_t err = cudaErrorUnknown;
+    bool done = false;
+    if (flags != nullptr && K > 0 && G > 0 && T > G && T % G != 0 &&
+        flag_bytes >= static_cast<size_t>(T + 1) * sizeof(unsigned)) {
+        // whole waves but the last one run one tile per CTA; the last
+        // T - dp_tiles tiles (between G and 2G of them) are split evenly
+        const long long dp_tiles = (T / G - 1) * G;
+        err = cudaMemsetAsync(flags, 0, static_cast<size_t>(T + 1) * sizeof(unsigned), stream);
+        if (err == cudaSuccess) {
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeCooperative;
+            attr.val.cooperative = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(G));
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            err = cudaLaunchKernelEx(&cfg, kSk[v], p, static_cast<int>(dp_tiles), flags);
+            done = err == cudaSuccess;
+            if (err == cudaErrorCooperativeLaunchTooLarge) {  // fewer SMs free than set up for
+                (void)cudaGetLastError();
+                err = cudaSuccess;
+            }
+            cfg.attrs = nullptr;
+            cfg.numAttrs = 0;
+        }
     }
-#undef SGEMM_LAUNCH
-    if (err != cudaSuccess) {
+    if (!done && err != cudaSuccess && err != cudaErrorUnknown) {
         (void)cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
     }
+    if (!done) {
+        cfg.gridDim = dim3(static_cast<unsigned>(T));
+        err = cudaLaunchKernelEx(&cfg, kDp[v], p);
+        if (err != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_LAUNCH;
+        }
+    }
     return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int sgemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                         cudaStream_t stream) {
+    const int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    return run(M, N, K, A, lda, B, ldb, C, ldc, nullptr, 0, stream);
+}
+
+extern "C" size_t sgemm_f32_workspace_size(int M, int N, int K) {
+    if (M <= 0 || N <= 0 || K < 0) return 0;
+    const long long T = tile_count(M, N);
+    const size_t bytes = static_cast<size_t>(T + 1) * sizeof(unsigned);
+    return (bytes + 255) / 256 * 256;
+}
+
+extern "C" int sgemm_f32_ws(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C,
+                            int ldc, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    if (workspace == nullptr && workspace_bytes != 0) return SGEMM_ERR_NULL_PTR;
+    if (workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 4 != 0) return SGEMM_ERR_INVALID_ARG;
+    const long long wb = static_cast<long long>(workspace_bytes);
+    if (workspace != nullptr &&
+        (ranges_overlap(workspace, wb, C, 4 * extent(M, N, ldc)) ||
+         (K > 0 && (ranges_overlap(workspace, wb, A, 4 * extent(M, K, lda)) ||
+                    ranges_overlap(workspace, wb, B, 4 * extent(K, N, ldb))))))
+        return SGEMM_ERR_ALIAS;
+    return run(M, N, K, A, lda, B, ldb, C, ldc, static_cast<unsigned *>(workspace), workspace_bytes, stream);
 }
 
 extern "C" const char *sgemm_f32_status_string(int status) {

@@ -17,11 +17,13 @@
  * unspecified, so results agree with an exact dot product to FP32 rounding,
  * not bit for bit with another order.
  *
- * All functions are thread-safe.  None allocates device memory.
+ * All functions are thread-safe.  None allocates device memory.  The first call
+ * on a device sets up that device's kernel attributes (once, under a lock).
  */
 #ifndef SGEMM_F32_H
 #define SGEMM_F32_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -68,6 +70,40 @@ int sgemm_f32(int M, int N, int K,
               const float *B, int ldb,
               float *C, int ldc,
               cudaStream_t stream);
+
+/*
+ * sgemm_f32_ws -- the same product, allowed to use a caller-provided device
+ * workspace for a better-balanced schedule.
+ *
+ *   workspace       : DEVICE pointer, 4-byte aligned, or NULL (then
+ *                     workspace_bytes must be 0); must not overlap A, B or C.
+ *   workspace_bytes : its size; sgemm_f32_workspace_size(M, N, K) is enough.
+ *
+ * When the workspace is large enough and the number of 128 x 128 output tiles
+ * does not divide evenly over the CTAs the GPU holds at once, the call runs a
+ * persistent "stream-K" schedule (every CTA gets the same number of 16-deep K
+ * slices; a tile cut between two CTAs is summed in a fixed order, so results
+ * are deterministic).  Otherwise it runs exactly as sgemm_f32.  The call
+ * zero-fills the words it uses at the start of the workspace on `stream` before
+ * the kernel, so the workspace needs no preparation and its contents are not
+ * preserved; calls that share one workspace must not overlap in time.  After
+ * the call completes, the 32-bit word at byte offset
+ * 4 * ceil(M/128) * ceil(N/128) is nonzero only if a CTA gave up waiting for
+ * its partner (about a second; the result is then wrong, nothing hangs).
+ * Other argument checks and errors are those of sgemm_f32, plus
+ * SGEMM_ERR_ALIAS for a workspace overlapping A, B or C and
+ * SGEMM_ERR_INVALID_ARG for a misaligned workspace.
+ */
+int sgemm_f32_ws(int M, int N, int K,
+                 const float *A, int lda,
+                 const float *B, int ldb,
+                 float *C, int ldc,
+                 void *workspace, size_t workspace_bytes,
+                 cudaStream_t stream);
+
+/* Workspace bytes sgemm_f32_ws can use for this shape (0 for an empty or
+ * invalid shape).  Host-only, touches no GPU. */
+size_t sgemm_f32_workspace_size(int M, int N, int K);
 
 /* Static English description of a status code (never NULL). */
 const char *sgemm_f32_status_string(int status);

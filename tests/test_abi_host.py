@@ -77,3 +77,22 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _binding.load_library()
+
+
+def test_workspace_size(lib):
+    assert sg.workspace_size(0, 5, 5) == 0 and sg.workspace_size(5, -1, 5) == 0
+    # one flag per 128 x 128 tile plus an error word, rounded up to 256 bytes
+    assert sg.workspace_size(4096, 4096, 4096) == ((32 * 32 + 1) * 4 + 255) // 256 * 256
+    assert sg.workspace_size(129, 1, 7) == 256
+
+
+@pytest.mark.parametrize("args,code", [
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 64), -3),           # NULL workspace, bytes > 0
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, FAKE * 4 + 2, 64), -7),  # misaligned workspace
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, FAKE * 3 + 8, 64), -4),  # workspace overlaps C
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, FAKE + 60, 8), -4),      # workspace overlaps A
+    ((4, 4, 4, FAKE, 3, FAKE * 2, 4, FAKE * 3, 4, FAKE * 4, 64), -2),      # usual checks still apply
+    ((0, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 0), 0),               # empty: no-op
+])
+def test_workspace_call_rejected_on_host(lib, args, code):
+    assert sg.sgemm_f32_ws(*args, 0) == code

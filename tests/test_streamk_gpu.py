@@ -1,0 +1,129 @@
+"""sgemm_f32_ws (stream-K schedule) vs the FP64 oracle and vs sgemm_f32 (needs a GB300).
+
+Shapes have more 128 x 128 output tiles than the GPU holds CTAs at once (2 per
+SM) and a count that does not divide evenly, so tiles are cut between two
+CTAs and summed through the workspace fix-up.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import dense_fp32_tiled_gb300 as sg
+from dense_fp32_tiled_gb300 import synth
+from tests import _tolerance as tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_fp32_tiled_gb300 import build
+    build.build()
+    sg.load_library()
+
+
+def _tiles(M, N):
+    return ((M + 127) // 128) * ((N + 127) // 128)
+
+
+def _run_ws(M, N, K, A, lda, B, ldb, ldc, a_off=0, b_off=0, c_off=0, ws_fill=0):
+    from tests._gpu import dev_buffer
+    tA, pA = dev_buffer(A, a_off)
+    tB, pB = dev_buffer(B, b_off)
+    c_elems = (M - 1) * ldc + N
+    tC = torch.full((c_elems + c_off + 4,), float("nan"), device="cuda")
+    nbytes = sg.workspace_size(M, N, K)
+    ws = torch.full((nbytes // 4,), ws_fill, dtype=torch.int32, device="cuda")
+    st = sg.sgemm_f32_ws(M, N, K, pA, lda, pB, ldb, tC.data_ptr() + 4 * c_off, ldc, ws.data_ptr(), nbytes,
+                         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    raw = tC.cpu().numpy()[c_off:c_off + c_elems]
+    C = np.stack([raw[i * ldc:i * ldc + N] for i in range(M)])
+    # the call zero-fills and uses the first tiles + 1 words (flags, error word)
+    return st, C, ws.cpu().numpy()[:_tiles(M, N) + 1]
+
+
+@pytest.mark.parametrize("M,N,K,kind", [(2500, 2100, 333, "uniform"), (2432, 2560, 300, "normal"),
+                                        (4096, 1408, 129, "uniform")])
+def test_streamk_full_check(oracle_lib, M, N, K, kind):
+    assert _tiles(M, N) > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    A = synth.matrix(M, K, 17, 0, kind)
+    B = synth.matrix(K, N, 17, 1, kind)
+    st, C, ws = _run_ws(M, N, K, A, K, B, N, N, ws_fill=7)
+    assert st == 0
+    assert not ws.any(), "flags and error word must be zero after a successful call"
+    Cr, Sr = oracle_lib.gemm(A, B)
+    tol.assert_close(C, Cr, Sr, K, f"stream-K {M}x{N}x{K}")
+
+
+def test_streamk_misaligned_strides_and_offsets(oracle_lib):
+    M, N, K = 2401, 2333, 257
+    lda, ldb, ldc = 259, 2335, 2337
+    A = synth.matrix(M, K, 23, 0, ld=lda, pad_value=np.nan)
+    B = synth.matrix(K, N, 23, 1, ld=ldb, pad_value=np.nan)
+    st, C, ws = _run_ws(M, N, K, A, lda, B, ldb, ldc, a_off=1, b_off=3, c_off=2)
+    assert st == 0 and not ws.any()
+    Cr, Sr = oracle_lib.gemm(A, B, M=M, N=N, K=K, lda=lda, ldb=ldb)
+    tol.assert_close(C, Cr, Sr, K, "stream-K misaligned")
+
+
+def test_streamk_integer_inputs_exact_and_equal_to_data_parallel(oracle_lib):
+    M, N, K = 2500, 2100, 1000
+    A = synth.matrix(M, K, 29, 0, "int5")
+    B = synth.matrix(K, N, 29, 1, "int5")
+    st, C, _ = _run_ws(M, N, K, A, K, B, N, N)
+    assert st == 0
+    Cr, _ = oracle_lib.gemm(A, B)
+    np.testing.assert_array_equal(C.astype(np.float64), Cr)
+    from tests._gpu import run
+    st2, C2, _ = run(M, N, K, A, K, B, N)
+    assert st2 == 0
+    np.testing.assert_array_equal(C, C2)
+
+
+def test_streamk_deterministic_4096():
+    A = torch.from_numpy(synth.matrix(4096, 4096, 3, 0)).cuda()
+    B = torch.from_numpy(synth.matrix(4096, 4096, 3, 1)).cuda()
+    C1 = sg.sgemm(A, B)
+    C2 = sg.sgemm(A, B)
+    C3 = sg.sgemm(A, B, balanced=False)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    # same products, different split of the K sum on cut tiles: FP32 rounding only
+    rel = ((C1.double() - C3.double()).norm() / C3.double().norm()).item()
+    assert rel < 1e-6
+
+
+def test_words_past_the_used_ones_are_untouched():
+    M, N, K = 2500, 2100, 40
+    A = synth.matrix(M, K, 37, 0)
+    B = synth.matrix(K, N, 37, 1)
+    from tests._gpu import dev_buffer
+    tA, pA = dev_buffer(A)
+    tB, pB = dev_buffer(B)
+    C = torch.empty(M, N, device="cuda")
+    nbytes = sg.workspace_size(M, N, K)
+    ws = torch.full((nbytes // 4 + 8,), 7, dtype=torch.int32, device="cuda")
+    st = sg.sgemm_f32_ws(M, N, K, pA, K, pB, N, C.data_ptr(), N, ws.data_ptr(), nbytes,
+                         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    used = _tiles(M, N) + 1
+    assert st == 0 and not ws[:used].any() and torch.all(ws[used:] == 7)
+
+
+def test_small_workspace_falls_back_to_one_cta_per_tile(oracle_lib):
+    M, N, K = 2500, 2100, 64
+    A = synth.matrix(M, K, 31, 0)
+    B = synth.matrix(K, N, 31, 1)
+    tA, tB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    C = torch.empty(M, N, device="cuda")
+    ws = torch.zeros(16, dtype=torch.int32, device="cuda")  # too small: ignored
+    st = sg.sgemm_f32_ws(M, N, K, tA.data_ptr(), K, tB.data_ptr(), N, C.data_ptr(), N, ws.data_ptr(), 64,
+                         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == 0 and not ws.any()
+    Cr, Sr = oracle_lib.gemm(A, B)
+    tol.assert_close(C.cpu().numpy(), Cr, Sr, K, "fallback")
