@@ -5,7 +5,9 @@
 ``sgemm_f32(...)`` is the raw C call on device addresses.
 """
 from ._binding import (SGEMM_OK, SgemmError, declared_functions, load_library, sgemm, sgemm_f32,
-                       sgemm_f32_ws, smem_request, smem_shape, status_string, workspace_size)
+                       sgemm_f32_static_scratch, sgemm_f32_ws, smem_request, smem_shape, status_string,
+                       workspace_size)
 
 __all__ = ["SGEMM_OK", "SgemmError", "declared_functions", "load_library", "sgemm", "sgemm_f32",
-           "sgemm_f32_ws", "smem_request", "smem_shape", "status_string", "workspace_size"]
+           "sgemm_f32_static_scratch", "sgemm_f32_ws", "smem_request", "smem_shape", "status_string",
+           "workspace_size"]

@@ -39,6 +39,8 @@ def load_library():
     lib.sgemm_f32.restype = i32
     lib.sgemm_f32_ws.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p, ctypes.c_size_t, p]
     lib.sgemm_f32_ws.restype = i32
+    lib.sgemm_f32_static_scratch.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p]
+    lib.sgemm_f32_static_scratch.restype = i32
     lib.sgemm_f32_workspace_size.argtypes = [i32, i32, i32]
     lib.sgemm_f32_workspace_size.restype = ctypes.c_size_t
     lib.sgemm_f32_status_string.argtypes = [i32]
@@ -81,6 +83,16 @@ def sgemm_f32_ws(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: 
                                        ctypes.c_void_p(int(C) or None), int(ldc),
                                        ctypes.c_void_p(int(workspace) or None), int(workspace_bytes),
                                        ctypes.c_void_p(int(stream) or None))
+
+
+def sgemm_f32_static_scratch(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                             stream: int = 0) -> int:
+    """Raw C-ABI call of the allocation-free entry point (its scratch is a fixed
+    array inside the library); returns the status code."""
+    return load_library().sgemm_f32_static_scratch(int(M), int(N), int(K), ctypes.c_void_p(int(A) or None),
+                                                   int(lda), ctypes.c_void_p(int(B) or None), int(ldb),
+                                                   ctypes.c_void_p(int(C) or None), int(ldc),
+                                                   ctypes.c_void_p(int(stream) or None))
 
 
 def workspace_size(M: int, N: int, K: int) -> int:

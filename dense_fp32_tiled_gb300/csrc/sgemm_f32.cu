@@ -534,6 +534,39 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     return SGEMM_OK;
 }
 
+// ---- fixed scratch for sgemm_f32_static_scratch ----------------------
+// One 32-bit flag per output tile plus the error word, for callers that
+// cannot allocate device memory.  Every GPU that loads this library holds
+// the array (64 KiB) until the process exits.
+constexpr int kStaticScratchWords = 16384;
+constexpr long long kStaticMaxTiles = kStaticScratchWords - 1;
+static __device__ __align__(256) unsigned g_static_scratch[kStaticScratchWords];
+
+std::mutex g_static_mutex;
+unsigned *g_static_ptr[kMaxDevices];   // device address of g_static_scratch
+int g_static_state[kMaxDevices];       // 0 = not yet looked up, 1 = ready, < 0 = status
+
+// Looks up, once per device and with that device current, the device
+// address of g_static_scratch (the host-side name is only a stand-in).
+int static_scratch(int dev, unsigned **out) {
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_state[dev] == 0) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess || ptr == nullptr) {
+            (void)cudaGetLastError();
+            g_static_state[dev] = SGEMM_ERR_DEVICE;
+        } else {
+            g_static_ptr[dev] = static_cast<unsigned *>(ptr);
+            g_static_state[dev] = 1;
+        }
+    }
+    if (g_static_state[dev] < 0) return g_static_state[dev];
+    *out = g_static_ptr[dev];
+    return SGEMM_OK;
+}
+
 }  // namespace
 
 extern "C" int sgemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
@@ -565,6 +598,22 @@ extern "C" int sgemm_f32_ws(int M, int N, int K, const float *A, int lda, const 
     return run(M, N, K, A, lda, B, ldb, C, ldc, static_cast<unsigned *>(workspace), workspace_bytes, stream);
 }
 
+extern "C" int sgemm_f32_static_scratch(int M, int N, int K, const float *A, int lda, const float *B, int ldb,
+                                        float *C, int ldc, cudaStream_t stream) {
+    const int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    if (tile_count(M, N) > kStaticMaxTiles) return SGEMM_ERR_SCRATCH_LIMIT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_DEVICE;
+    }
+    unsigned *scratch = nullptr;
+    const int sst = static_scratch(dev, &scratch);
+    if (sst != SGEMM_OK) return sst;
+    return run(M, N, K, A, lda, B, ldb, C, ldc, scratch, sizeof(g_static_scratch), stream);
+}
+
 extern "C" const char *sgemm_f32_status_string(int status) {
     switch (status) {
         case SGEMM_OK: return "success";
@@ -575,6 +624,8 @@ extern "C" const char *sgemm_f32_status_string(int status) {
         case SGEMM_ERR_LAUNCH: return "kernel launch rejected by the CUDA runtime";
         case SGEMM_ERR_DEVICE: return "current device is not sm_103 or its set-up failed";
         case SGEMM_ERR_INVALID_ARG: return "invalid argument (misaligned pointer or out-of-range value)";
+        case SGEMM_ERR_SCRATCH_LIMIT:
+            return "more than 16383 output tiles of 128 x 128: beyond the fixed scratch of sgemm_f32_static_scratch";
         default: return "unknown status";
     }
 }

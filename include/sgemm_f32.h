@@ -39,7 +39,8 @@ typedef enum {
     SGEMM_ERR_ALIAS = -4,        /* C's address range overlaps A's or B's */
     SGEMM_ERR_LAUNCH = -5,       /* the kernel launch was rejected by the runtime */
     SGEMM_ERR_DEVICE = -6,       /* current device is not sm_103 or its set-up failed */
-    SGEMM_ERR_INVALID_ARG = -7   /* any other out-of-range argument */
+    SGEMM_ERR_INVALID_ARG = -7,  /* any other out-of-range argument */
+    SGEMM_ERR_SCRATCH_LIMIT = -8 /* sgemm_f32_static_scratch: more tiles than its fixed scratch holds */
 } sgemm_status;
 
 /*
@@ -104,6 +105,39 @@ int sgemm_f32_ws(int M, int N, int K,
 /* Workspace bytes sgemm_f32_ws can use for this shape (0 for an empty or
  * invalid shape).  Host-only, touches no GPU. */
 size_t sgemm_f32_workspace_size(int M, int N, int K);
+
+/*
+ * sgemm_f32_static_scratch -- the sgemm_f32_ws product for callers that
+ * cannot allocate device memory.
+ *
+ * This call has no counterpart on the pages; it exists for callers that are
+ * not allowed to allocate.  Examples are code whose device memory is wholly
+ * owned by another allocator (a framework's caching pool or a fixed budget
+ * set up at start-up), and latency-critical paths that must not risk the
+ * implicit device-wide synchronisation a cudaFree can bring.  It allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.  The
+ * caller still passes A, B and C exactly as for sgemm_f32, with the same
+ * meaning, checks and error codes.
+ *
+ * The scratch that sgemm_f32_ws takes from the caller (one flag per 128 x 128
+ * output tile plus an error word) lives here in a fixed array inside the
+ * library, of 16384 32-bit words (64 KiB).  Every GPU that loads the library
+ * holds it until the process exits.  Problems with more than 16383 output
+ * tiles (ceil(M/128) * ceil(N/128); e.g. M = N = 16256 fits, 16384 does not)
+ * are rejected with SGEMM_ERR_SCRATCH_LIMIT before anything is launched.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and keeps it; make that first call before any stream
+ * capture begins.  Every call shares the one array, which keeps whatever the
+ * last call left there: each call zero-fills the words it uses on `stream`
+ * before its kernel, and calls that overlap on the GPU (different streams,
+ * or different host threads) race on the array and must not be issued.
+ */
+int sgemm_f32_static_scratch(int M, int N, int K,
+                             const float *A, int lda,
+                             const float *B, int ldb,
+                             float *C, int ldc,
+                             cudaStream_t stream);
 
 /* Static English description of a status code (never NULL). */
 const char *sgemm_f32_status_string(int status);
