@@ -22,11 +22,14 @@
 //   zero source size, which fills shared memory with 0; stores are guarded.
 //   Misaligned leading dimensions ("对齐也要从数据分配开始") select 8- or
 //   4-byte B copies and C stores instead of 16-byte ones.
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
 #include <cuda_runtime.h>
 
 #include <climits>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "sgemm_f32.h"
 #include "smem_layout.cuh"
@@ -60,6 +63,45 @@ template <int PENDING>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(PENDING) : "memory");
 }
+
+// ---- mbarrier and tensor-memory-access (TMA) copies ---------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// 2-D tiled bulk copy global -> shared; elements outside the tensor read 0.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Polls of one mbarrier phase before a wait is abandoned (each try_wait
+// itself blocks for a while): far beyond any copy's latency.
+constexpr uint32_t kWaitLimit = 1u << 22;
+// Set to 1 by a CTA whose copy wait ran out (the result is then wrong; the
+// kernel still finishes).  Stays set until the process exits.
+__device__ unsigned g_copy_timeout;
+
+// Global memory descriptions of A (dims K x M, box 16 x 128, 64-byte
+// swizzle: the layout of the raw A tile) and B (dims N x K, box 128 x 16, no
+// swizzle: the layout of the B tile).
+struct Maps {
+    CUtensorMap a, b;
+};
 
 struct Problem {
     int M, N, K;
@@ -95,23 +137,31 @@ __device__ __forceinline__ void acc_zero(Acc &acc) {
 
 // Accumulates the product of the CTA's C tile (m0, n0) over K tiles
 // [kt0, kt1) into acc.  VA = A copy width in floats (4 or 1), VB = B copy
-// width in floats (4, 2 or 1), chosen on the host from alignment.
+// width in floats (4, 2 or 1), chosen on the host from alignment; with TMA
+// (both 4) one thread moves each tile by two tensor copies instead.
+//
+// `pipe` counts the tiles this CTA has loaded before this range: load u goes
+// to ring stage u % STAGES (its mbarrier completes phase u / STAGES) and is
+// transposed into As buffer u % 2.
 //
 // Pipeline (one __syncthreads per K tile): at iteration kt
-//   1. wait until the copy group of tile kt+1 has landed (own copies), then
-//      barrier: tile kt+1's raw A and B, and the transposed As of tile kt,
-//      are visible to all; every thread has finished tile kt-1;
+//   1. wait until tile kt+1 has landed (own cp.async copies, or the stage's
+//      mbarrier), then barrier: tile kt+1's raw A and B, and the transposed
+//      As of tile kt, are visible to all; every thread has finished tile kt-1;
 //   2. issue the copies of tile kt+STAGES-1 into the stage tile kt-1 used;
 //   3. transpose tile kt+1's raw A into the As buffer tile kt-1 used;
 //   4. 16 k steps of fragment reads and packed FMAs on tile kt.
-// On return every copy has landed and every thread is past its last shared
-// read, so the caller may start another range at once.
-template <int VA, int VB>
-__device__ __forceinline__ void mma_k_range(const Problem &p, const int m0, const int n0, const int kt0,
-                                            const int kt1, float *smem, Acc &acc) {
+// On return every copy has landed; the caller must __syncthreads() before
+// starting another range (other threads may still read shared memory).
+template <int VA, int VB, bool TMA>
+__device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, const int m0, const int n0,
+                                            const int kt0, const int kt1, uint32_t &pipe, float *smem,
+                                            const uint32_t bars, Acc &acc) {
+    static_assert(!TMA || (VA == 4 && VB == 4), "tensor copies need 16-byte aligned rows");
     const int tid = threadIdx.x;
     const int K = p.K, M = p.M, N = p.N;
     const uint32_t sbase = smem_u32(smem);
+    const uint32_t u0 = pipe - static_cast<uint32_t>(kt0);  // load index of tile kt is u0 + kt
 
     // ---- A copies (global -> raw staging tile).  Rows past M and columns
     // past K are zero-filled by a zero source size ("边界处理会破坏漂亮形状").
@@ -133,34 +183,64 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const int m0, cons
     const float *b_colp = p.B + (b_valid > 0 ? b_col : 0);
 
     auto issue_tile = [&](int kt) {
-        const int stage = kt % STAGES;
+        const uint32_t stage = (u0 + kt) % STAGES;
         const int kb = kt * BK;
+        if constexpr (TMA) {
+            if (tid == 0) {
+                const uint32_t bar = bars + 8 * stage;
+                mbar_expect_tx(bar, STAGE_FLOATS * 4);
+                tma_load_2d(sbase + ar_word(stage, 0, 0) * 4, &maps.a, kb, m0, bar);
+                tma_load_2d(sbase + bs_word(stage, 0, 0) * 4, &maps.b, n0, kb, bar);
+            }
+        } else {
 #pragma unroll
-        for (int q = 0; q < NA; ++q) {
-            int m, k;
-            if constexpr (VA == 4) a_copy16_coord(tid, q, m, k);
-            else a_copy4_coord(tid, q, m, k);
-            const int kg = kb + k;
-            const int left = K - kg;  // valid floats from kg on
-            uint32_t bytes = (m0 + m < M && left > 0) ? (left >= VA ? VA * 4u : left * 4u) : 0u;
-            const float *src = bytes ? a_base + q * a_step + kb : p.A;
-            cp_async<VA * 4>(sbase + ar_word(stage, m, k) * 4, src, bytes);
-        }
+            for (int q = 0; q < NA; ++q) {
+                int m, k;
+                if constexpr (VA == 4) a_copy16_coord(tid, q, m, k);
+                else a_copy4_coord(tid, q, m, k);
+                const int kg = kb + k;
+                const int left = K - kg;  // valid floats from kg on
+                uint32_t bytes = (m0 + m < M && left > 0) ? (left >= VA ? VA * 4u : left * 4u) : 0u;
+                const float *src = bytes ? a_base + q * a_step + kb : p.A;
+                cp_async<VA * 4>(sbase + ar_word(stage, m, k) * 4, src, bytes);
+            }
 #pragma unroll
-        for (int q = 0; q < NB; ++q) {
-            int k, n;
-            b_copy_coord<VB>(tid, q, k, n);
-            const int kg = kb + k;
-            const bool ok = kg < K && b_bytes != 0;
-            const float *src = ok ? b_colp + static_cast<size_t>(kg) * p.ldb : p.B;
-            cp_async<VB * 4>(sbase + bs_word(stage, k, n) * 4, src, ok ? b_bytes : 0u);
+            for (int q = 0; q < NB; ++q) {
+                int k, n;
+                b_copy_coord<VB>(tid, q, k, n);
+                const int kg = kb + k;
+                const bool ok = kg < K && b_bytes != 0;
+                const float *src = ok ? b_colp + static_cast<size_t>(kg) * p.ldb : p.B;
+                cp_async<VB * 4>(sbase + bs_word(stage, k, n) * 4, src, ok ? b_bytes : 0u);
+            }
+            cp_async_commit();
         }
     };
+    // Waits until tile kt's copies are visible to this thread.  cp.async:
+    // PENDING later groups may stay in flight.  TMA: the stage's mbarrier
+    // phase; a wait that runs out records g_copy_timeout and goes on.
+    auto wait_tile = [&](int kt, auto pending) {
+        if constexpr (TMA) {
+            const uint32_t u = u0 + kt;
+            const uint32_t bar = bars + 8 * (u % STAGES);
+            uint32_t polls = 0;
+            while (!mbar_try_wait(bar, (u / STAGES) & 1u)) {
+                if (++polls > kWaitLimit) {
+                    g_copy_timeout = 1u;
+                    break;
+                }
+            }
+        } else {
+            cp_async_wait<decltype(pending)::value>();
+        }
+    };
+    using Pending1 = std::integral_constant<int, STAGES - 2>;
+    using Pending2 = std::integral_constant<int, STAGES - 3>;
 
     // ---- A transpose: raw staging tile -> k-major As buffer
     auto transpose_tile = [&](int kt) {
-        const int stage = kt % STAGES;
-        const int buf = kt & 1;
+        const uint32_t stage = (u0 + kt) % STAGES;
+        const int buf = (u0 + kt) & 1;
 #pragma unroll
         for (int f = 0; f < A_VECS; ++f) {
             int k, m;
@@ -180,23 +260,23 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const int m0, cons
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
         if (kt0 + s < kt1) issue_tile(kt0 + s);
-        cp_async_commit();
+        else if (!TMA) cp_async_commit();  // keep one cp.async group per slot
     }
     if (kt0 < kt1) {
-        cp_async_wait<STAGES - 2>();
+        wait_tile(kt0, Pending1{});
         __syncthreads();
         transpose_tile(kt0);
     }
 
     for (int kt = kt0; kt < kt1; ++kt) {
-        cp_async_wait<STAGES - 3>();
+        if (!TMA || kt + 1 < kt1) wait_tile(kt + 1, Pending2{});
         __syncthreads();
         if (kt + STAGES - 1 < kt1) issue_tile(kt + STAGES - 1);
-        cp_async_commit();
+        else if (!TMA) cp_async_commit();
         if (kt + 1 < kt1) transpose_tile(kt + 1);
 
-        const int stage = kt % STAGES;
-        const int buf = kt & 1;
+        const uint32_t stage = (u0 + kt) % STAGES;
+        const int buf = (u0 + kt) & 1;
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
             const float4 a0 = *reinterpret_cast<const float4 *>(smem + as_word(buf, k, ra));
@@ -218,7 +298,25 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const int m0, cons
                 }
         }
     }
-    cp_async_wait<0>();
+    if (!TMA) cp_async_wait<0>();
+    pipe += static_cast<uint32_t>(kt1 > kt0 ? kt1 - kt0 : 0);
+}
+
+// 1024-byte aligned start of the dynamic shared memory block, and the
+// mbarriers of the copy ring (initialised once per CTA).
+__device__ __forceinline__ float *aligned_smem(float *raw) {
+    const uint32_t s = smem_u32(raw);
+    return raw + ((SMEM_ALIGN - (s & (SMEM_ALIGN - 1))) & (SMEM_ALIGN - 1)) / 4;
+}
+template <bool TMA>
+__device__ __forceinline__ void init_bars(uint32_t bars) {
+    if (TMA) {
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < STAGES; ++s) mbar_init(bars + 8 * s, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        }
+        __syncthreads();
+    }
 }
 
 // Writes the register tile to C tile (m0, n0) with guarded stores,
@@ -266,14 +364,19 @@ __device__ __forceinline__ void store_tile(const Problem &p, const int m0, const
 }
 
 // Data-parallel schedule: one CTA per C tile, the whole K range.
-template <int VA, int VB>
-__global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p) {
-    extern __shared__ __align__(128) float smem[];
+template <int VA, int VB, bool TMA>
+__global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p, const __grid_constant__ Maps maps) {
+    extern __shared__ float smem_raw[];
+    __shared__ __align__(8) uint64_t bar_mem[STAGES];
+    float *smem = aligned_smem(smem_raw);
+    const uint32_t bars = smem_u32(bar_mem);
+    init_bars<TMA>(bars);
     int tm, tn;
     tile_of(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
     Acc acc;
     acc_zero(acc);
-    mma_k_range<VA, VB>(p, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, smem, acc);
+    uint32_t pipe = 0;
+    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
     store_tile<false>(p, tm * BM, tn * BN, acc);
 }
 
@@ -305,10 +408,15 @@ constexpr unsigned kSpinLimit = 1u << 24;  // x ~64 ns sleeps: about a second, t
 // The producer's segment comes first in its range, so no wait can form a
 // cycle.  A wait longer than kSpinLimit polls records error bit 1 in
 // flags[T] and stores without the partial: a wrong result, never a hang.
-template <int VA, int VB>
+template <int VA, int VB, bool TMA>
 __global__ void __launch_bounds__(NT, 2)
-sgemm_f32_streamk_kernel(const Problem p, const int dp_tiles, unsigned *flags) {
-    extern __shared__ __align__(128) float smem[];
+sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles, unsigned *flags) {
+    extern __shared__ float smem_raw[];
+    __shared__ __align__(8) uint64_t bar_mem[STAGES];
+    float *smem = aligned_smem(smem_raw);
+    const uint32_t bars = smem_u32(bar_mem);
+    init_bars<TMA>(bars);
+    uint32_t pipe = 0;
     const int KT = (p.K + BK - 1) / BK;
     const int T = p.tiles_m * p.tiles_n;
     const int G = gridDim.x;
@@ -317,7 +425,7 @@ sgemm_f32_streamk_kernel(const Problem p, const int dp_tiles, unsigned *flags) {
         tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
         Acc acc;
         acc_zero(acc);
-        mma_k_range<VA, VB>(p, tm * BM, tn * BN, 0, KT, smem, acc);
+        mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, 0, KT, pipe, smem, bars, acc);
         store_tile<false>(p, tm * BM, tn * BN, acc);
         __syncthreads();  // shared memory free for the next tile
     }
@@ -333,7 +441,7 @@ sgemm_f32_streamk_kernel(const Problem p, const int dp_tiles, unsigned *flags) {
         tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
         Acc acc;
         acc_zero(acc);
-        mma_k_range<VA, VB>(p, tm * BM, tn * BN, k0, k1, smem, acc);
+        mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
         if (k0 == 0 && k1 == KT) {
             store_tile<false>(p, tm * BM, tn * BN, acc);
         } else if (k0 > 0) {
@@ -368,15 +476,62 @@ sgemm_f32_streamk_kernel(const Problem p, const int dp_tiles, unsigned *flags) {
 // ---------------------------------------------------------------------------
 
 constexpr int kMaxDevices = 64;
-constexpr int kVariants = 6;  // (VA, VB) in {4, 1} x {4, 2, 1}
-using DpKernel = void (*)(Problem);
-using SkKernel = void (*)(Problem, int, unsigned *);
-const DpKernel kDp[kVariants] = {sgemm_f32_tiled_kernel<4, 4>, sgemm_f32_tiled_kernel<4, 2>,
-                                 sgemm_f32_tiled_kernel<4, 1>, sgemm_f32_tiled_kernel<1, 4>,
-                                 sgemm_f32_tiled_kernel<1, 2>, sgemm_f32_tiled_kernel<1, 1>};
-const SkKernel kSk[kVariants] = {sgemm_f32_streamk_kernel<4, 4>, sgemm_f32_streamk_kernel<4, 2>,
-                                 sgemm_f32_streamk_kernel<4, 1>, sgemm_f32_streamk_kernel<1, 4>,
-                                 sgemm_f32_streamk_kernel<1, 2>, sgemm_f32_streamk_kernel<1, 1>};
+constexpr int kVariants = 7;  // (VA, VB) in {4, 1} x {4, 2, 1} with cp.async, and (4, 4) with TMA
+constexpr int kTmaVariant = 6;
+using DpKernel = void (*)(Problem, Maps);
+using SkKernel = void (*)(Problem, Maps, int, unsigned *);
+const DpKernel kDp[kVariants] = {
+    sgemm_f32_tiled_kernel<4, 4, false>, sgemm_f32_tiled_kernel<4, 2, false>, sgemm_f32_tiled_kernel<4, 1, false>,
+    sgemm_f32_tiled_kernel<1, 4, false>, sgemm_f32_tiled_kernel<1, 2, false>, sgemm_f32_tiled_kernel<1, 1, false>,
+    sgemm_f32_tiled_kernel<4, 4, true>};
+const SkKernel kSk[kVariants] = {
+    sgemm_f32_streamk_kernel<4, 4, false>, sgemm_f32_streamk_kernel<4, 2, false>,
+    sgemm_f32_streamk_kernel<4, 1, false>, sgemm_f32_streamk_kernel<1, 4, false>,
+    sgemm_f32_streamk_kernel<1, 2, false>, sgemm_f32_streamk_kernel<1, 1, false>,
+    sgemm_f32_streamk_kernel<4, 4, true>};
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time (no link
+// against libcuda).  Null when unavailable: the cp.async kernels are used.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        else
+            (void)cudaGetLastError();
+    });
+    return g_encode;
+}
+
+// Describes A (K x M elements, rows lda apart; box 16 x 128, 64-byte
+// swizzle) and B (N x K, rows ldb apart; box 128 x 16, no swizzle) for the
+// tensor copies.  Needs 16-byte aligned bases and row strides.
+bool encode_maps(Maps &maps, int M, int N, int K, const float *A, int lda, const float *B, int ldb) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t a_dim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t a_stride[1] = {static_cast<cuuint64_t>(lda) * 4};
+    const cuuint32_t a_box[2] = {BK, BM};
+    const cuuint64_t b_dim[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
+    const cuuint64_t b_stride[1] = {static_cast<cuuint64_t>(ldb) * 4};
+    const cuuint32_t b_box[2] = {BN, BK};
+    const cuuint32_t ones[2] = {1, 1};
+    return enc(&maps.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(A), a_dim, a_stride, a_box, ones,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+           enc(&maps.b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(B), b_dim, b_stride, b_box, ones,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 struct DeviceInfo {
     int state;                    // 0 = not yet set up, 1 = ready, < 0 = status
@@ -481,7 +636,10 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
 
     const int va = K > 0 ? (vector_class(A, lda) == 4 ? 4 : 1) : 4;
     const int vb = K > 0 ? vector_class(B, ldb) : 4;
-    const int v = (va == 4 ? 0 : 3) + (vb == 4 ? 0 : vb == 2 ? 1 : 2);
+    int v = (va == 4 ? 0 : 3) + (vb == 4 ? 0 : vb == 2 ? 1 : 2);
+    Maps maps;
+    memset(&maps, 0, sizeof maps);
+    if (v == 0 && K > 0 && encode_maps(maps, M, N, K, A, lda, B, ldb)) v = kTmaVariant;
     Problem p;
     p.M = M; p.N = N; p.K = K; p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
     p.tiles_m = (M + BM - 1) / BM;
@@ -509,7 +667,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
             cfg.gridDim = dim3(static_cast<unsigned>(G));
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
-            err = cudaLaunchKernelEx(&cfg, kSk[v], p, static_cast<int>(dp_tiles), flags);
+            err = cudaLaunchKernelEx(&cfg, kSk[v], p, maps, static_cast<int>(dp_tiles), flags);
             done = err == cudaSuccess;
             if (err == cudaErrorCooperativeLaunchTooLarge) {  // fewer SMs free than set up for
                 (void)cudaGetLastError();
@@ -525,7 +683,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     }
     if (!done) {
         cfg.gridDim = dim3(static_cast<unsigned>(T));
-        err = cudaLaunchKernelEx(&cfg, kDp[v], p);
+        err = cudaLaunchKernelEx(&cfg, kDp[v], p, maps);
         if (err != cudaSuccess) {
             (void)cudaGetLastError();
             return SGEMM_ERR_LAUNCH;

@@ -51,7 +51,8 @@ constexpr int STAGE_FLOATS = B_STAGE_FLOATS + A_RAW_FLOATS;
 constexpr int AS_FLOATS = BK * BM;
 constexpr int AS_BASE = STAGES * STAGE_FLOATS;  // first As buffer (floats)
 constexpr int SMEM_FLOATS = AS_BASE + 2 * AS_FLOATS;
-constexpr int SMEM_BYTES = SMEM_FLOATS * 4;
+constexpr int SMEM_ALIGN = 1024;  // all offsets above are from a 1024-byte aligned base
+constexpr int SMEM_BYTES = SMEM_FLOATS * 4 + SMEM_ALIGN;  // dynamic size requested, with alignment slack
 constexpr int A_VECS = BM * BK / (4 * NT);  // float4 of A a thread transposes per tile
 
 static_assert(WARPS_M * WARPS_N * 32 == NT, "warp grid");
