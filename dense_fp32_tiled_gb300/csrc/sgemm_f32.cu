@@ -115,24 +115,19 @@ struct Problem {
     int vc;  // C store width in floats (4, 2 or 1)
 };
 
-// The 8 x 8 register tile, paired for the packed FP32 FMA (fma.rn.f32x2).
-// With rows r = 2i+{0,1} and cols c = 2j+{0,1} of the tile,
-//   dg[i][j] = (acc[2i][2j],   acc[2i+1][2j+1])  += (a_2i, a_2i+1) * (b_2j,   b_2j+1)
-//   ad[i][j] = (acc[2i][2j+1], acc[2i+1][2j])    += (a_2i, a_2i+1) * (b_2j+1, b_2j)
-// so both operands are natural register pairs of the 128-bit fragment reads
-// (plus one swapped copy of each B pair): 32 packed FMAs per k.
+// The 8 x 8 register tile, held as 32 column pairs for the packed FP32 FMA
+// (fma.rn.f32x2): c[r][j] = (acc[r][2j], acc[r][2j+1]) += (a_r, a_r) * (b_2j, b_2j+1).
+// The B pairs are natural register pairs of the 128-bit fragment reads and
+// a_r is used twice: 32 packed FMAs per k step.
 struct Acc {
-    float2 dg[TM / 2][TN / 2], ad[TM / 2][TN / 2];
+    float2 c[TM][TN / 2];
 };
 
 __device__ __forceinline__ void acc_zero(Acc &acc) {
 #pragma unroll
-    for (int i = 0; i < TM / 2; ++i)
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < TN / 2; ++j) {
-            acc.dg[i][j] = make_float2(0.0f, 0.0f);
-            acc.ad[i][j] = make_float2(0.0f, 0.0f);
-        }
+        for (int j = 0; j < TN / 2; ++j) acc.c[i][j] = make_float2(0.0f, 0.0f);
 }
 
 // Accumulates the product of the CTA's C tile (m0, n0) over K tiles
@@ -283,19 +278,15 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
             const float4 a1 = *reinterpret_cast<const float4 *>(smem + as_word(buf, k, ra + 16));
             const float4 b0 = *reinterpret_cast<const float4 *>(smem + bs_word(stage, k, cb));
             const float4 b1 = *reinterpret_cast<const float4 *>(smem + bs_word(stage, k, cb + 32));
-            const float2 ap[TM / 2] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
-                                       make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
+            const float a[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const float2 bp[TN / 2] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
                                        make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
-            const float2 bq[TN / 2] = {make_float2(b0.y, b0.x), make_float2(b0.w, b0.z),
-                                       make_float2(b1.y, b1.x), make_float2(b1.w, b1.z)};
 #pragma unroll
-            for (int i = 0; i < TM / 2; ++i)
+            for (int r = 0; r < TM; ++r) {
+                const float2 ar = make_float2(a[r], a[r]);
 #pragma unroll
-                for (int j = 0; j < TN / 2; ++j) {
-                    acc.dg[i][j] = __ffma2_rn(ap[i], bp[j], acc.dg[i][j]);
-                    acc.ad[i][j] = __ffma2_rn(ap[i], bq[j], acc.ad[i][j]);
-                }
+                for (int j = 0; j < TN / 2; ++j) acc.c[r][j] = __ffma2_rn(ar, bp[j], acc.c[r][j]);
+            }
         }
     }
     if (!TMA) cp_async_wait<0>();
@@ -335,11 +326,7 @@ __device__ __forceinline__ void store_tile(const Problem &p, const int m0, const
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = n0 + cb + 32 * h;
-            // row i = 2*ip + r of the tile; cols 4h .. 4h+3 = pairs jp = 2h, 2h+1
-            const int ip = i >> 1, r = i & 1;
-            const float2 d0 = acc.dg[ip][2 * h], x0 = acc.ad[ip][2 * h];
-            const float2 d1 = acc.dg[ip][2 * h + 1], x1 = acc.ad[ip][2 * h + 1];
-            float v[4] = {r ? x0.y : d0.x, r ? d0.y : x0.x, r ? x1.y : d1.x, r ? d1.y : x1.x};
+            float v[4] = {acc.c[i][2 * h].x, acc.c[i][2 * h].y, acc.c[i][2 * h + 1].x, acc.c[i][2 * h + 1].y};
             if (col + 3 < p.N && p.vc == 4) {
                 if (ADD_PARTIAL) {
                     const float4 o = __ldcg(reinterpret_cast<const float4 *>(crow + col));
