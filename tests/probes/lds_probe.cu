@@ -66,6 +66,67 @@ __global__ void lds64_probe(float *out, int iters) {
   }
   out[blockIdx.x * blockDim.x + threadIdx.x] = acc.x + acc.y;
 }
+// 32-bit accesses s[lane * STRIDE] (the bank page's stride law: a full warp
+// touches 32/gcd(stride,32) banks, conflict degree gcd(stride,32)).
+template <int STRIDE>
+__global__ void lds32_stride_probe(float *out, int iters) {
+  __shared__ float s[4096];
+  for (int i = threadIdx.x; i < 4096; i += blockDim.x) s[i] = i;
+  __syncthreads();
+  const int l = threadIdx.x & 31;
+  float acc = 0.0f;
+  for (int it = 0; it < iters; ++it) acc += s[(l * STRIDE + 32 * (it & 63)) & 4095];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = acc;
+}
+template <int STRIDE>
+__global__ void sts32_stride_probe(float *out, int iters) {
+  __shared__ float s[4096];
+  const int l = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  for (int it = 0; it < iters; ++it) s[(l * STRIDE + 32 * ((it + w) & 63)) & 4095] = float(it);
+  __syncthreads();
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s[threadIdx.x];
+}
+// The sgemm kernel's A transpose, in isolation: each warp reads 32 consecutive
+// rows of a 128 x 16 tile stored with the 64-byte XOR swizzle (16-byte
+// groups g at g ^ ((row >> 1) & 3)) and writes the 4 components to a k-major
+// 16 x 128 tile (32 consecutive words per store).  Two raw tiles and two
+// k-major tiles rotate; the accesses are inline PTX so none is merged or
+// hoisted.
+__global__ void xpose_probe(float *out, int iters) {
+  __shared__ __align__(16) float raw[2][128 * 16];
+  __shared__ __align__(16) float kmaj[2][16 * 128];
+  for (int i = threadIdx.x; i < 2 * 2048; i += blockDim.x) (&raw[0][0])[i] = i;
+  __syncthreads();
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int m = 32 * (w & 3) + l;
+  float acc = 0.0f;
+  for (int it = 0; it < iters; ++it) {
+    const int k = 8 * (w >> 2) + 4 * (it & 1);
+    const unsigned src = static_cast<unsigned>(__cvta_generic_to_shared(
+        &raw[(it >> 1) & 1][m * 16 + 4 * ((k >> 2) ^ ((m >> 1) & 3))]));
+    float x, y, z, v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(x), "=f"(y), "=f"(z), "=f"(v) : "r"(src));
+    const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(&kmaj[(it >> 2) & 1][k * 128 + m]));
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst), "f"(x) : "memory");
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + 512), "f"(y) : "memory");
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + 1024), "f"(z) : "memory");
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + 1536), "f"(v) : "memory");
+    acc += x;
+  }
+  __syncthreads();
+  out[blockIdx.x * blockDim.x + threadIdx.x] = acc + kmaj[0][threadIdx.x];
+}
+
+template <int S>
+void run_strides(float *out, int iters) {
+  if constexpr (S <= 33) {
+    lds32_stride_probe<S><<<152, 256>>>(out, iters);
+    sts32_stride_probe<S><<<152, 256>>>(out, iters);
+    run_strides<S + 1>(out, iters);
+  }
+}
+
 int main() {
   float *out;
   cudaMalloc(&out, 1024 * 256 * sizeof(float));
@@ -74,6 +135,8 @@ int main() {
   RUN(0) RUN(1) RUN(2) RUN(3) RUN(4) RUN(5) RUN(6) RUN(7) RUN(8) RUN(9)
   RUN(10) RUN(11) RUN(12) RUN(13) RUN(14) RUN(15) RUN(16) RUN(17) RUN(18) RUN(19)
   RUN(20) RUN(21) RUN(22) RUN(23) RUN(24) RUN(25)
+  run_strides<1>(out, iters);
+  xpose_probe<<<152, 256>>>(out, iters);
   cudaError_t e = cudaDeviceSynchronize();
   printf("probe done: %s\n", cudaGetErrorString(e));
   cudaFree(out);

@@ -121,3 +121,23 @@ def test_wide_accesses(oracle_lib):
     assert r["degree"] == 1 and r["wavefronts"] == 1
     with pytest.raises(ValueError):
         oracle_lib.shared_request([2], 4)
+
+
+def test_measured_stride_sweep_matches_gcd_law_and_model(oracle_lib):
+    """ncu on GB300: 32-bit loads and stores s[lane*stride], stride 1..33."""
+    seen = set()
+    with open(os.path.join(HERE, "golden", "lds32_stride_sm103.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, rhs = line.split("=")
+            op, stride = lhs.split()
+            stride = int(stride)
+            wavefronts, conflicts = (int(x) for x in rhs.split())
+            g = math.gcd(stride, 32)
+            assert wavefronts == g and conflicts == g - 1, (op, stride)
+            r = oracle_lib.shared_request([4 * (l * stride) for l in range(32)], 4)
+            assert r["wavefronts"] == wavefronts
+            seen.add((op, stride))
+    assert seen == {(op, s) for op in ("lds32", "sts32") for s in range(1, 34)}
