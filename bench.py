@@ -209,6 +209,22 @@ def run_reference(a):
     print(json.dumps(line), flush=True)
 
 
+def combine_ranks(ms: float, flops: float, world: int, device=None):
+    """Replica timing across ranks: the slowest rank's ms per step, and the
+    whole-job throughput (world x FLOP per step / that time) in TFLOP/s.
+
+    Each rank runs the full product on its own GPU; the only cross-rank
+    operation is this max-reduction of a scalar (no data-path collective).
+    """
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * flops / (ms / 1e3) / 1e12
+
+
 def _config(w, n, l2):
     return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "lda": w.lda, "ldb": w.ldb, "ldc": w.ldc,
             "inputs": f"{w.kind}{'' if w.kind != 'normal' else f'(0,{w.sigma})'} seed {w.seed}",
@@ -285,13 +301,8 @@ def main():
         t_wall = time.perf_counter() - t_wall
         clk.t1 = time.time()
     times = [st.elapsed_time(en) for st, en in zip(starts, ends)]
-    ms = statistics.mean(times)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     flops = float(w.flops)
-    value = world * flops / (ms / 1e3) / 1e12
+    ms, value = combine_ranks(statistics.mean(times), flops, world, dev)
     clocks = clk.summary()
 
     # ---- end to end: pinned host inputs -> device -> product -> host result
@@ -314,12 +325,8 @@ def main():
             hC.copy_(C, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = e0.elapsed_time(e1) / e_steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * flops / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        e_ms, e_value = combine_ranks(e0.elapsed_time(e1) / e_steps, flops, world, dev)
+        e2e = {"value": e_value, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(A_h.nbytes + B_h.nbytes), "d2h_bytes_per_step": int(c_elems * 4),
                "ms_per_step": e_ms}
 
