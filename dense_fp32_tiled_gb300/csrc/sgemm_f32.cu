@@ -378,26 +378,70 @@ __device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
 }
 constexpr unsigned kSpinLimit = 1u << 24;  // x ~64 ns sleeps: about a second, then give up
 
-// Stream-K schedule with a data-parallel head.  A persistent, co-resident
-// grid of G CTAs first computes tiles 0 .. dp_tiles-1 one whole tile at a time
-// (tile c, c+G, ...: CTAs running together work on neighbouring tiles, which
-// keeps A and B panels in L2), then splits the (tile, K tile) iterations of
-// the remaining T - dp_tiles tiles into G equal contiguous ranges, so every
-// CTA ends with the same amount of FMA work whatever T mod G is.  A tile cut
-// by a range boundary is shared by exactly two CTAs (more remaining tiles
-// than CTAs makes every range longer than a tile):
-//   * the CTA whose range starts inside the tile (its first segment, k from
-//     the cut to the end) stores its partial sums into the tile of C itself
-//     and raises flags[tile];
-//   * the CTA whose range ends inside the tile (its last segment, k from 0
-//     to the cut) waits for the flag, adds the partial to its own sums and
-//     stores the result, then lowers the flag for the next call.
-// The producer's segment comes first in its range, so no wait can form a
-// cycle.  A wait longer than kSpinLimit polls records error bit 1 in
-// flags[T] and stores without the partial: a wrong result, never a hang.
+// Partial sums of a split tile, one 128 x 128 slot per CTA: thread t's 16
+// float4 go to floats 4 * (q * NT + t), q = 0..15, so each warp store
+// covers 512 contiguous bytes.
+__device__ __forceinline__ void store_partial(float *slot, const Acc &acc) {
+#pragma unroll
+    for (int q = 0; q < TM * TN / 4; ++q) {
+        const float2 lo = acc.c[q >> 1][2 * (q & 1)], hi = acc.c[q >> 1][2 * (q & 1) + 1];
+        *reinterpret_cast<float4 *>(slot + 4 * (q * NT + threadIdx.x)) = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+}
+__device__ __forceinline__ void add_partial(const float *slot, Acc &acc) {
+#pragma unroll
+    for (int q = 0; q < TM * TN / 4; ++q) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(slot + 4 * (q * NT + threadIdx.x)));
+        float2 &lo = acc.c[q >> 1][2 * (q & 1)], &hi = acc.c[q >> 1][2 * (q & 1) + 1];
+        lo.x += v.x; lo.y += v.y; hi.x += v.z; hi.y += v.w;
+    }
+}
+// Thread 0 waits for a flag raised by another CTA; a wait longer than
+// kSpinLimit polls sets bit 1 of *error and gives up (wrong result, no hang).
+__device__ __forceinline__ void wait_flag(const unsigned *flag, unsigned *error) {
+    if (threadIdx.x == 0) {
+        unsigned spins = 0;
+        while (ld_acquire(flag) == 0u) {
+            if (++spins > kSpinLimit) {
+                atomicOr(error, 1u);
+                break;
+            }
+            __nanosleep(64);
+        }
+    }
+    __syncthreads();
+}
+__device__ __forceinline__ void raise_flag(unsigned *flag) {
+    __syncthreads();  // every thread's partial stores are issued
+    if (threadIdx.x == 0) {
+        __threadfence();
+        st_release(flag, 1u);
+    }
+}
+
+// Stream-K schedule.  A persistent, co-resident grid of G CTAs first computes
+// tiles 0 .. dp_tiles-1 one whole tile at a time (tile c, c+G, ...: CTAs
+// running together work on neighbouring tiles, which keeps A and B panels in
+// L2), then splits the (tile, K tile) iterations of the remaining tiles into
+// G equal contiguous ranges, so every CTA ends with the same amount of FMA
+// work.  A tile cut by range boundaries is finished by the CTA holding its
+// K = 0 part (the owner, whose last segment it is); every other CTA holding a
+// part of it starts its range there and hands its partial sums over first:
+//   * partials == nullptr (more remaining tiles than CTAs, so every range is
+//     longer than a tile and a tile has at most two parts): the other CTA
+//     stores its partial sums into the tile of C itself and raises
+//     flags[tile]; the owner adds that tile of C to its sums.
+//   * partials != nullptr (any number of parts): CTA c writes its partial
+//     sums to slot c of `partials` and raises flags[c]; the owner adds the
+//     slots of the following CTAs in CTA order.
+// Every hand-over comes first in its CTA's range, so no wait can form a
+// cycle, and the order of the additions is fixed: results are deterministic.
+// A wait longer than kSpinLimit polls records error bit 1 in the word after
+// the flags and stores without that part: a wrong result, never a hang.
 template <int VA, int VB, bool TMA>
 __global__ void __launch_bounds__(NT, 2)
-sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles, unsigned *flags) {
+sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles, unsigned *flags,
+                         float *partials) {
     extern __shared__ float smem_raw[];
     __shared__ __align__(8) uint64_t bar_mem[STAGES];
     float *smem = aligned_smem(smem_raw);
@@ -407,6 +451,7 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
     const int KT = (p.K + BK - 1) / BK;
     const int T = p.tiles_m * p.tiles_n;
     const int G = gridDim.x;
+    unsigned *error = flags + (partials ? G : T);
     for (int lin = blockIdx.x; lin < dp_tiles; lin += G) {
         int tm, tn;
         tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
@@ -431,25 +476,26 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
         mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
         if (k0 == 0 && k1 == KT) {
             store_tile<false>(p, tm * BM, tn * BN, acc);
-        } else if (k0 > 0) {
-            store_tile<false>(p, tm * BM, tn * BN, acc);  // partial sums for k >= cut
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                __threadfence();
-                st_release(flags + lin, 1u);
+        } else if (k0 > 0) {  // hand the partial sums for k >= k0 over to the owner
+            if (partials) {
+                store_partial(partials + static_cast<size_t>(blockIdx.x) * (BM * BN), acc);
+                raise_flag(flags + blockIdx.x);
+            } else {
+                store_tile<false>(p, tm * BM, tn * BN, acc);
+                raise_flag(flags + lin);
             }
-        } else {
-            if (threadIdx.x == 0) {
-                unsigned spins = 0;
-                while (ld_acquire(flags + lin) == 0u) {
-                    if (++spins > kSpinLimit) {
-                        atomicOr(flags + T, 1u);
-                        break;
-                    }
-                    __nanosleep(64);
-                }
+        } else if (partials) {  // owner: add the parts of CTAs blockIdx.x+1 .. c_last
+            const long long last = static_cast<long long>(lin + 1) * KT - 1 - base;
+            const int c_last = static_cast<int>(((last + 1) * G + total_iters - 1) / total_iters - 1);
+            for (int c = blockIdx.x + 1; c <= c_last; ++c) {
+                wait_flag(flags + c, error);
+                add_partial(partials + static_cast<size_t>(c) * (BM * BN), acc);
             }
-            __syncthreads();
+            store_tile<false>(p, tm * BM, tn * BN, acc);
+            if (threadIdx.x == 0)
+                for (int c = blockIdx.x + 1; c <= c_last; ++c) flags[c] = 0u;
+        } else {  // owner of a two-part tile
+            wait_flag(flags + lin, error);
             store_tile<true>(p, tm * BM, tn * BN, acc);
             if (threadIdx.x == 0) flags[lin] = 0u;
         }
@@ -466,7 +512,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kVariants = 7;  // (VA, VB) in {4, 1} x {4, 2, 1} with cp.async, and (4, 4) with TMA
 constexpr int kTmaVariant = 6;
 using DpKernel = void (*)(Problem, Maps);
-using SkKernel = void (*)(Problem, Maps, int, unsigned *);
+using SkKernel = void (*)(Problem, Maps, int, unsigned *, float *);
 const DpKernel kDp[kVariants] = {
     sgemm_f32_tiled_kernel<4, 4, false>, sgemm_f32_tiled_kernel<4, 2, false>, sgemm_f32_tiled_kernel<4, 1, false>,
     sgemm_f32_tiled_kernel<1, 4, false>, sgemm_f32_tiled_kernel<1, 2, false>, sgemm_f32_tiled_kernel<1, 1, false>,
@@ -607,9 +653,57 @@ int check_args(int M, int N, int K, const float *A, int lda, const float *B, int
     return SGEMM_OK;
 }
 
-// Runs one product whose arguments passed check_args (M, N > 0).  Uses the
-// stream-K schedule when `flags` holds at least tiles + 1 words and the tile
-// count does not divide evenly over the co-resident CTAs; else one CTA per tile.
+// How one product is scheduled.  kind 0: one CTA per tile.  kind 1:
+// stream-K over the last wave-and-a-bit of tiles, partial sums handed over
+// through C (needs flags only).  kind 2: stream-K over all tiles with any
+// number of parts per tile, partial sums handed over through per-CTA slots
+// (for fewer tiles than co-resident CTAs).
+struct Plan {
+    int kind;
+    long long grid, dp_tiles;
+    long long flag_words;      // flags plus the error word
+    size_t partials_offset;    // byte offset of the partial slots (kind 2)
+    size_t bytes;              // workspace bytes needed
+};
+constexpr long long kMinItersPerCta = 8;  // K tiles per CTA below which splitting stops paying
+
+// Chooses the schedule for T output tiles of KT K tiles each, with G CTAs
+// resident at once on `sms` multiprocessors.  Cost model, fitted to GB300
+// timings of 340..1024-tile products (K = 4096): one CTA per tile takes
+// floor(T/G) full rounds plus, for a last partial wave, 0.55 of a round when
+// it has at most one CTA per SM (a lone CTA runs faster) or a full round
+// otherwise; the split schedule takes T/G rounds plus about 4.5 %.  It is
+// chosen only when it is at least 3 % better.  With fewer tiles than
+// resident CTAs the multi-part split is used when it adds more than 10 % CTAs.
+Plan plan_schedule(long long T, long long KT, long long G, long long sms) {
+    Plan pl = {0, T, 0, 0, 0, 0};
+    if (KT <= 0 || G <= 0) return pl;
+    if (T > G) {
+        const long long W = T / G, R = T % G;
+        if (R == 0) return pl;  // whole waves: already balanced
+        const double dp_rounds = static_cast<double>(W) + (R <= sms ? 0.55 : 1.0);
+        const double sk_rounds = static_cast<double>(T) / static_cast<double>(G) * 1.045;
+        if (sk_rounds > 0.97 * dp_rounds) return pl;
+        pl.kind = 1;
+        pl.grid = G;
+        pl.dp_tiles = (W - 1) * G;  // the last T - dp_tiles tiles (between G and 2G) are split
+        pl.flag_words = T + 1;
+        pl.bytes = static_cast<size_t>(pl.flag_words) * sizeof(unsigned);
+        return pl;
+    }
+    const long long g = (T * KT / kMinItersPerCta < G) ? T * KT / kMinItersPerCta : G;
+    if (static_cast<double>(g) <= 1.1 * static_cast<double>(T)) return pl;  // too few extra CTAs
+    pl.kind = 2;
+    pl.grid = g;
+    pl.flag_words = g + 1;
+    pl.partials_offset = (static_cast<size_t>(pl.flag_words) * sizeof(unsigned) + 255) / 256 * 256;
+    pl.bytes = pl.partials_offset + static_cast<size_t>(g) * BM * BN * sizeof(float);
+    return pl;
+}
+
+// Runs one product whose arguments passed check_args (M, N > 0).  Uses a
+// stream-K schedule when the workspace `flags` (flag_bytes long) is large
+// enough for the plan chosen for this shape; else one CTA per tile.
 int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
         unsigned *flags, size_t flag_bytes, cudaStream_t stream) {
     int dev = 0;
@@ -634,6 +728,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     p.vc = vector_class(C, ldc);
     const long long T = static_cast<long long>(p.tiles_m) * p.tiles_n;
     const long long G = static_cast<long long>(info.sk_per_sm[v]) * info.sms;
+    const Plan pl = plan_schedule(T, (K + BK - 1) / BK, G, info.sms);
 
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT);
@@ -641,20 +736,18 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     cfg.stream = stream;
     cudaError_t err = cudaErrorUnknown;
     bool done = false;
-    if (flags != nullptr && K > 0 && G > 0 && T > G && T % G != 0 &&
-        flag_bytes >= static_cast<size_t>(T + 1) * sizeof(unsigned)) {
-        // whole waves but the last one run one tile per CTA; the last
-        // T - dp_tiles tiles (between G and 2G of them) are split evenly
-        const long long dp_tiles = (T / G - 1) * G;
-        err = cudaMemsetAsync(flags, 0, static_cast<size_t>(T + 1) * sizeof(unsigned), stream);
+    if (flags != nullptr && pl.kind != 0 && flag_bytes >= pl.bytes) {
+        float *partials =
+            pl.kind == 2 ? reinterpret_cast<float *>(reinterpret_cast<char *>(flags) + pl.partials_offset) : nullptr;
+        err = cudaMemsetAsync(flags, 0, static_cast<size_t>(pl.flag_words) * sizeof(unsigned), stream);
         if (err == cudaSuccess) {
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeCooperative;
             attr.val.cooperative = 1;
-            cfg.gridDim = dim3(static_cast<unsigned>(G));
+            cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
-            err = cudaLaunchKernelEx(&cfg, kSk[v], p, maps, static_cast<int>(dp_tiles), flags);
+            err = cudaLaunchKernelEx(&cfg, kSk[v], p, maps, static_cast<int>(pl.dp_tiles), flags, partials);
             done = err == cudaSuccess;
             if (err == cudaErrorCooperativeLaunchTooLarge) {  // fewer SMs free than set up for
                 (void)cudaGetLastError();
@@ -724,7 +817,17 @@ extern "C" int sgemm_f32(int M, int N, int K, const float *A, int lda, const flo
 extern "C" size_t sgemm_f32_workspace_size(int M, int N, int K) {
     if (M <= 0 || N <= 0 || K < 0) return 0;
     const long long T = tile_count(M, N);
-    const size_t bytes = static_cast<size_t>(T + 1) * sizeof(unsigned);
+    size_t bytes = static_cast<size_t>(T + 1) * sizeof(unsigned);  // flags of the two-part schedule
+    int dev = 0;
+    DeviceInfo info;
+    if (cudaGetDevice(&dev) == cudaSuccess && setup_device(dev, &info) == SGEMM_OK) {
+        int per_sm = 0;
+        for (int v = 0; v < kVariants; ++v) per_sm = info.sk_per_sm[v] > per_sm ? info.sk_per_sm[v] : per_sm;
+        const Plan pl = plan_schedule(T, (K + BK - 1) / BK, static_cast<long long>(per_sm) * info.sms, info.sms);
+        if (pl.bytes > bytes) bytes = pl.bytes;
+    } else {
+        (void)cudaGetLastError();
+    }
     return (bytes + 255) / 256 * 256;
 }
 
@@ -733,7 +836,7 @@ extern "C" int sgemm_f32_ws(int M, int N, int K, const float *A, int lda, const 
     const int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
     if (st != SGEMM_OK || M == 0 || N == 0) return st;
     if (workspace == nullptr && workspace_bytes != 0) return SGEMM_ERR_NULL_PTR;
-    if (workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 4 != 0) return SGEMM_ERR_INVALID_ARG;
+    if (workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SGEMM_ERR_INVALID_ARG;
     const long long wb = static_cast<long long>(workspace_bytes);
     if (workspace != nullptr &&
         (ranges_overlap(workspace, wb, C, 4 * extent(M, N, ldc)) ||

@@ -76,21 +76,30 @@ int sgemm_f32(int M, int N, int K,
  * sgemm_f32_ws -- the same product, allowed to use a caller-provided device
  * workspace for a better-balanced schedule.
  *
- *   workspace       : DEVICE pointer, 4-byte aligned, or NULL (then
+ *   workspace       : DEVICE pointer, 16-byte aligned, or NULL (then
  *                     workspace_bytes must be 0); must not overlap A, B or C.
  *   workspace_bytes : its size; sgemm_f32_workspace_size(M, N, K) is enough.
  *
- * When the workspace is large enough and the number of 128 x 128 output tiles
- * does not divide evenly over the CTAs the GPU holds at once, the call runs a
- * persistent "stream-K" schedule (every CTA gets the same number of 16-deep K
- * slices; a tile cut between two CTAs is summed in a fixed order, so results
- * are deterministic).  Otherwise it runs exactly as sgemm_f32.  The call
- * zero-fills the words it uses at the start of the workspace on `stream` before
- * the kernel, so the workspace needs no preparation and its contents are not
- * preserved; calls that share one workspace must not overlap in time.  After
- * the call completes, the 32-bit word at byte offset
- * 4 * ceil(M/128) * ceil(N/128) is nonzero only if a CTA gave up waiting for
- * its partner (about a second; the result is then wrong, nothing hangs).
+ * When the workspace is large enough, the call balances the work over the
+ * CTAs the GPU holds at once (2 per SM) with a persistent "stream-K"
+ * schedule: every CTA gets the same number of 16-deep K slices, and a 128 x
+ * 128 output tile cut between CTAs is summed in a fixed order, so results are
+ * deterministic.  Two cases use it:
+ *   - more tiles than resident CTAs, not a whole number of waves: the last
+ *     wave and a bit are split, with partial sums handed over through C (the
+ *     workspace holds one flag per tile plus an error word);
+ *   - fewer tiles than resident CTAs: every tile is split into several K
+ *     parts (at least 8 K slices per CTA), with partial sums handed over
+ *     through 64 KiB slots in the workspace (one flag and one slot per CTA).
+ * Otherwise, or with a smaller workspace, it runs exactly as sgemm_f32.
+ * sgemm_f32_workspace_size reports the bytes for the current device.  The
+ * call zero-fills the flag words it uses at the start of the workspace on
+ * `stream` before the kernel, so the workspace needs no preparation and its
+ * contents are not preserved; calls that share one workspace must not overlap
+ * in time.  After the call completes, the 32-bit word following the flags
+ * (word ceil(M/128) * ceil(N/128) in the first case, word G in the second,
+ * G = number of CTAs) is nonzero only if a CTA gave up waiting for a partner
+ * (about a second; the result is then wrong, nothing hangs).
  * Other argument checks and errors are those of sgemm_f32, plus
  * SGEMM_ERR_ALIAS for a workspace overlapping A, B or C and
  * SGEMM_ERR_INVALID_ARG for a misaligned workspace.
@@ -102,8 +111,9 @@ int sgemm_f32_ws(int M, int N, int K,
                  void *workspace, size_t workspace_bytes,
                  cudaStream_t stream);
 
-/* Workspace bytes sgemm_f32_ws can use for this shape (0 for an empty or
- * invalid shape).  Host-only, touches no GPU. */
+/* Workspace bytes sgemm_f32_ws can use for this shape on the current device
+ * (0 for an empty or invalid shape).  Reads device attributes only; with no
+ * usable device it returns the size of the flags-only schedule. */
 size_t sgemm_f32_workspace_size(int M, int N, int K);
 
 /*

@@ -88,9 +88,9 @@ def test_workspace_size(lib):
 
 @pytest.mark.parametrize("args,code", [
     ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 64), -3),           # NULL workspace, bytes > 0
-    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, FAKE * 4 + 2, 64), -7),  # misaligned workspace
-    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, FAKE * 3 + 8, 64), -4),  # workspace overlaps C
-    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, FAKE + 60, 8), -4),      # workspace overlaps A
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, FAKE * 4 + 8, 64), -7),  # workspace not 16-byte aligned
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, FAKE * 3 + 16, 64), -4),  # workspace overlaps C
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, FAKE + 48, 16), -4),     # workspace overlaps A
     ((4, 4, 4, FAKE, 3, FAKE * 2, 4, FAKE * 3, 4, FAKE * 4, 64), -2),      # usual checks still apply
     ((0, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 0), 0),               # empty: no-op
 ])

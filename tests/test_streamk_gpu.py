@@ -127,3 +127,58 @@ def test_small_workspace_falls_back_to_one_cta_per_tile(oracle_lib):
     assert st == 0 and not ws.any()
     Cr, Sr = oracle_lib.gemm(A, B)
     tol.assert_close(C.cpu().numpy(), Cr, Sr, K, "fallback")
+
+
+def _plan_words(M, N, K):
+    """Flag words (with the error word) the multi-part schedule uses for a
+    shape with fewer tiles than resident CTAs, or None if it is not used."""
+    T = _tiles(M, N)
+    G = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    KT = (K + 15) // 16
+    g = min(G, T * KT // 8)
+    return g + 1 if T <= G and g > 1.1 * T else None
+
+
+@pytest.mark.parametrize("M,N,K,lds,kind", [
+    (1024, 1024, 1024, None, "normal"),          # 64 tiles
+    (1000, 1030, 777, (777, 1030, 1030), "uniform"),  # 72 tiles, misaligned rows: cp.async path
+    (256, 256, 256, None, "uniform"),            # 4 tiles
+    (2048, 256, 4096, None, "normal"),           # 32 tiles, deep K
+])
+def test_multipart_split_full_check(oracle_lib, M, N, K, lds, kind):
+    lda, ldb, ldc = lds or (K, N, N)
+    words = _plan_words(M, N, K)
+    assert words is not None, "shape must use the multi-part schedule"
+    A = synth.matrix(M, K, 43, 0, kind, ld=lda)
+    B = synth.matrix(K, N, 43, 1, kind, ld=ldb)
+    from tests._gpu import dev_buffer
+    tA, pA = dev_buffer(A)
+    tB, pB = dev_buffer(B)
+    c_elems = (M - 1) * ldc + N
+    tC = torch.full((c_elems + 4,), float("nan"), device="cuda")
+    nbytes = sg.workspace_size(M, N, K)
+    assert nbytes >= words * 4 + (words - 1) * 128 * 128 * 4
+    ws = torch.full((nbytes // 4,), 5, dtype=torch.int32, device="cuda")
+    st = sg.sgemm_f32_ws(M, N, K, pA, lda, pB, ldb, tC.data_ptr(), ldc, ws.data_ptr(), nbytes,
+                         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == 0
+    assert not ws[:words].any(), "flags and error word must be zero after a successful call"
+    raw = tC.cpu().numpy()[:c_elems]
+    C = np.stack([raw[i * ldc:i * ldc + N] for i in range(M)])
+    Cr, Sr = oracle_lib.gemm(A, B, M=M, N=N, K=K, lda=lda, ldb=ldb)
+    tol.assert_close(C, Cr, Sr, K, f"multi-part {M}x{N}x{K}")
+
+
+def test_multipart_integer_exact_and_deterministic(oracle_lib):
+    M, N, K = 1024, 768, 2048
+    assert _plan_words(M, N, K) is not None
+    A = synth.matrix(M, K, 47, 0, "int5")
+    B = synth.matrix(K, N, 47, 1, "int5")
+    tA, tB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    C1 = sg.sgemm(tA, tB)
+    C2 = sg.sgemm(tA, tB)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    Cr, _ = oracle_lib.gemm(A, B)
+    np.testing.assert_array_equal(C1.cpu().numpy().astype(np.float64), Cr)
