@@ -64,6 +64,8 @@ def _load():
         ip = ctypes.POINTER(ctypes.c_int)
         lib.oracle_shared_request.argtypes = [ctypes.c_int, p, p, ctypes.c_int, ip, ip, ip, ip]
         lib.oracle_shared_request.restype = ctypes.c_int
+        lib.oracle_transpose_f32.argtypes = [i64, i64, p, i64, p, i64]
+        lib.oracle_transpose_f32.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -130,6 +132,24 @@ def gemm_sampled(A, B, rows, cols, M=None, N=None, K=None, lda=None, ldb=None):
     if rc != 0:
         raise ValueError(f"oracle_gemm_sampled_f64 rejected the arguments (rc={rc})")
     return out, absout
+
+
+def transpose(x, rows=None, cols=None, ld_in=None, ld_out=None, out=None):
+    """out[j][i] = x[i][j] for a float32 matrix (dense 2-D, or a flat buffer with
+    an explicit ld_in).  Returns a dense cols x rows array, or fills the flat
+    buffer ``out`` with row stride ``ld_out``."""
+    if rows is None:
+        rows, cols = x.shape
+    x_, ldi = _storage(x, rows, cols, ld_in)
+    if out is None:
+        res = np.zeros((cols, rows), dtype=np.float32)
+        ldo = max(1, rows)
+    else:
+        res, ldo = out, ld_out
+    rc = _load().oracle_transpose_f32(rows, cols, _ptr(x_), ldi, _ptr(res), ldo)
+    if rc != 0:
+        raise ValueError(f"oracle_transpose_f32 rejected the arguments (rc={rc})")
+    return res
 
 
 def bank_of(byte_address: int) -> int:

@@ -292,3 +292,22 @@ int oracle_shared_request(int n_lanes, const uint64_t *byte_address,
     if (distinct) *distinct = nw;
     return 0;
 }
+
+/* ---------------------------------------------------------------------
+ * Matrix transpose (bank page, "放进矩阵转置里看"): the input is a
+ * rows x cols row-major FP32 matrix (row i at in + i*ld_in), the output the
+ * cols x rows matrix with out[j][i] = in[i][j] (row j at out + j*ld_out); the
+ * two must not overlap.  Pure data movement: bit-exact.
+ * Returns 0, or -1 on a bad argument.
+ * ------------------------------------------------------------------- */
+int oracle_transpose_f32(int64_t rows, int64_t cols, const float *in, int64_t ld_in,
+                         float *out, int64_t ld_out) {
+    if (rows < 0 || cols < 0) return -1;
+    if (ld_in < (cols > 1 ? cols : 1) || ld_out < (rows > 1 ? rows : 1)) return -1;
+    if (rows == 0 || cols == 0) return 0;
+    if (in == NULL || out == NULL) return -1;
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < cols; ++j)
+            memcpy(out + j * ld_out + i, in + i * ld_in + j, sizeof(float));
+    return 0;
+}
