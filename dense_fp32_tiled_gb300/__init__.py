@@ -2,12 +2,14 @@
 
 ``sgemm(A, B)`` multiplies CUDA float32 tensors through the C-ABI library
 ``libsgemm_f32.so`` (built by ``dense_fp32_tiled_gb300.build.build()``);
-``sgemm_f32(...)`` is the raw C call on device addresses.
+``sgemm_f32(...)`` is the raw C call on device addresses.  ``transpose(x)`` /
+``transpose_f32(...)`` run the FP32 transpose, the pages' second workload.
 """
 from ._binding import (SGEMM_OK, SgemmError, declared_functions, load_library, sgemm, sgemm_f32,
                        sgemm_f32_static_scratch, sgemm_f32_ws, smem_request, smem_shape, status_string,
+                       transpose, transpose_f32, transpose_smem_request, transpose_status_string,
                        workspace_size)
 
 __all__ = ["SGEMM_OK", "SgemmError", "declared_functions", "load_library", "sgemm", "sgemm_f32",
            "sgemm_f32_static_scratch", "sgemm_f32_ws", "smem_request", "smem_shape", "status_string",
-           "workspace_size"]
+           "transpose", "transpose_f32", "transpose_smem_request", "transpose_status_string", "workspace_size"]

@@ -13,6 +13,7 @@ import re
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libsgemm_f32.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "sgemm_f32.h")
+HEADER_PATHS = [HEADER_PATH, os.path.join(os.path.dirname(_PKG), "include", "transpose_f32.h")]
 
 SGEMM_OK = 0
 _lib = None
@@ -46,6 +47,14 @@ def load_library():
     lib.sgemm_f32_status_string.argtypes = [i32]
     lib.sgemm_f32_status_string.restype = ctypes.c_char_p
     ip = ctypes.POINTER(ctypes.c_int)
+    lib.transpose_f32.argtypes = [i32, i32, p, i32, p, i32, p]
+    lib.transpose_f32.restype = i32
+    lib.transpose_f32_layout.argtypes = [i32, i32, p, i32, p, i32, i32, p]
+    lib.transpose_f32_layout.restype = i32
+    lib.transpose_f32_smem_request.argtypes = [i32, i32, i32, i32, i64p, ip]
+    lib.transpose_f32_smem_request.restype = i32
+    lib.transpose_f32_status_string.argtypes = [i32]
+    lib.transpose_f32_status_string.restype = ctypes.c_char_p
     lib.sgemm_f32_smem_shape.argtypes = [i32, ip, ip, ip]
     lib.sgemm_f32_smem_shape.restype = i32
     lib.sgemm_f32_smem_request.argtypes = [i32, i32, i32, i32, i64p, ip]
@@ -55,11 +64,13 @@ def load_library():
 
 
 def declared_functions() -> list[str]:
-    """Names of the functions include/sgemm_f32.h declares."""
-    with open(HEADER_PATH) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(sgemm_f32\w*)\s*\(", text)))
+    """Names of the functions the headers in include/ declare."""
+    names = set()
+    for path in HEADER_PATHS:
+        with open(path) as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:sgemm|transpose)_f32\w*)\s*\(", text))
+    return sorted(names)
 
 
 def status_string(status: int) -> str:
@@ -173,4 +184,51 @@ def sgemm(A, B, out=None, stream=None, balanced=True):
             st = sgemm_f32(M, N, K, a, lda, b, ldb, c, ldc, s)
     if st != SGEMM_OK:
         raise SgemmError(st)
+    return out
+
+
+# ---- transpose ------------------------------------------------------------
+TRANSPOSE_LAYOUTS = {"padded": 0, "unpadded": 1, "swizzled": 2, "fast": 3}
+
+
+def transpose_f32(rows: int, cols: int, inp: int, ld_in: int, out: int, ld_out: int, stream: int = 0,
+                  layout: str | None = None) -> int:
+    """Raw C-ABI call (transpose_f32, or transpose_f32_layout with a layout name)."""
+    lib = load_library()
+    args = (int(rows), int(cols), ctypes.c_void_p(int(inp) or None), int(ld_in),
+            ctypes.c_void_p(int(out) or None), int(ld_out))
+    if layout is None:
+        return lib.transpose_f32(*args, ctypes.c_void_p(int(stream) or None))
+    return lib.transpose_f32_layout(*args, TRANSPOSE_LAYOUTS[layout], ctypes.c_void_p(int(stream) or None))
+
+
+def transpose_status_string(status: int) -> str:
+    return load_library().transpose_f32_status_string(int(status)).decode()
+
+
+def transpose_smem_request(layout: str, kind: int, warp: int, step: int):
+    out = (ctypes.c_int64 * 32)()
+    width = ctypes.c_int()
+    st = load_library().transpose_f32_smem_request(TRANSPOSE_LAYOUTS[layout], kind, warp, step, out,
+                                                   ctypes.byref(width))
+    if st != 0:
+        raise ValueError(f"transpose_f32_smem_request rejected ({st})")
+    return list(out), width.value
+
+
+def transpose(x, out=None, stream=None):
+    """x.T for a CUDA float32 tensor (row-major, any row stride) via transpose_f32."""
+    import torch
+    if x.dim() != 2:
+        raise ValueError("transpose expects a 2-D tensor")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty((cols, rows), dtype=torch.float32, device=x.device)
+    a, lda = _matrix_args(x, rows, cols, "x")
+    b, ldb = _matrix_args(out, cols, rows, "out")
+    s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
+    with torch.cuda.device(x.device):
+        st = transpose_f32(rows, cols, a, lda, b, ldb, s)
+    if st != 0:
+        raise RuntimeError(f"transpose_f32 failed with status {st}: {transpose_status_string(st)}")
     return out
