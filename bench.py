@@ -9,6 +9,7 @@ Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference]
+  python bench.py --op transpose [--rows R --cols C] [--layout fast|padded|unpadded|swizzled]
 
 Timing: inputs resident in HBM; before every timed step the L2 is flushed by
 writing a 256 MiB buffer (outside the step's events); each step is bracketed
@@ -46,6 +47,12 @@ def _args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["gemm", "transpose"], default="gemm",
+                    help="gemm: the FP32 product (default); transpose: the FP32 transpose workload")
+    ap.add_argument("--rows", type=int, default=8192, help="transpose: input rows")
+    ap.add_argument("--cols", type=int, default=8192, help="transpose: input cols")
+    ap.add_argument("--layout", choices=["fast", "padded", "unpadded", "swizzled"], default="fast",
+                    help="transpose: kernel (fast = transpose_f32, else the 32x32 tile kernel's layout)")
     return ap.parse_args()
 
 
@@ -233,10 +240,72 @@ def _config(w, n, l2):
             "l2": l2, "parallelism": "replicas" if n > 1 else "single GPU"}
 
 
+def run_transpose(a):
+    """FP32 transpose out = in^T: bytes moved (read + write) per second."""
+    import torch
+    import dense_fp32_tiled_gb300 as sg
+    from dense_fp32_tiled_gb300 import build as lib_build
+    from dense_fp32_tiled_gb300 import synth
+    lib_build.build()
+    sg.load_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    rows, cols = a.rows, a.cols
+    x_h = synth.matrix(rows, cols, 61, 0)
+    x = torch.from_numpy(x_h).to(dev)
+    y = torch.empty((cols, rows), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    layout = None if a.layout == "fast" else a.layout
+
+    def step():
+        st = sg.transpose_f32(rows, cols, x.data_ptr(), cols, y.data_ptr(), rows, stream.cuda_stream, layout=layout)
+        if st != 0:
+            raise RuntimeError(sg.transpose_status_string(st))
+    for _ in range(a.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    props = torch.cuda.get_device_properties(dev)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        torch.cuda.synchronize(dev)
+        clk.t0 = time.time()
+        for i in range(a.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        clk.t1 = time.time()
+    ms = statistics.mean(st.elapsed_time(en) for st, en in zip(starts, ends))
+    nbytes = 2.0 * 4 * rows * cols
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak = float(_measured_peaks().get("hbm_gbs") or 6800.0)
+    line = {"metric": "FP32 transpose GB/s (bytes read + written)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"transpose_{rows}x{cols}", "rows": rows, "cols": cols, "kernel": a.layout,
+                       "inputs": "uniform seed 61", "l2": "flushed before every timed step"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "peak_basis": "measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
+            "gpu_launches": a.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     a = _args()
     if a.impl == "reference":
         run_reference(a)
+        return
+    if a.op == "transpose":
+        run_transpose(a)
         return
     import torch
     import torch.distributed as dist

@@ -7,10 +7,8 @@
 // tile to [32][33] so that reading a column of it touches 32 different banks;
 // "Padding 之外的选择" offers an XOR swizzle instead.  transpose_f32_layout
 // runs that kernel shape with the three layouts (padded, unpadded control,
-// swizzled) for measurement.  transpose_f32 is the bandwidth-oriented kernel:
-// 64 x 64 tiles, 128-bit global loads and stores where the alignment class
-// allows, and a tile stored k-major ("transposed on store", vectorised-load
-// page) by 32-bit stores of 32 consecutive words, read back by 128-bit loads.
+// swizzled) for measurement.  transpose_f32 is the same design scaled up for
+// bandwidth: 64 x 64 tiles padded to [64][65], 16 elements per thread.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -57,74 +55,41 @@ __global__ void __launch_bounds__(T32 *T32_ROWS) transpose_tile32_kernel(const f
 }
 
 // ---- bandwidth-oriented 64 x 64 kernel -----------------------------------
-constexpr int TT = 64;        // tile rows and cols
-constexpr int TNT = 256;      // threads
-constexpr int TT_STRIDE = TT; // k-major tile row stride (floats)
+// The pages' kernel scaled up so that more bytes are in flight per SM: a
+// 64 x 64 tile padded to [64][65] ("多一列": row stride 65 puts the 32
+// consecutive rows of a column read in 32 different banks), block (32, 8),
+// each thread moving 16 elements.  A warp reads and writes 128 contiguous
+// bytes of one row per instruction on both sides; 4-byte accesses need no
+// alignment class.
+constexpr int TT = 64;         // tile rows and cols
+constexpr int TT_STRIDE = TT + 1;
+constexpr int TT_ROWS = 8;     // block (32, 8)
 
-// Load map: float4 q (0..3) of thread t covers input rows r = 32*(w & 1) + l
-// (w = t / 32, l = t % 32) and columns 4*(4*(w >> 1) + q) .. +3: a warp load
-// touches one 16-byte group in 32 consecutive rows, and the 4 components go
-// to the k-major tile as 32-bit stores of 32 consecutive words.
-__host__ __device__ __forceinline__ void tt_load_coord(int tid, int q, int &r, int &c) {
-    const int w = tid >> 5, l = tid & 31;
-    r = 32 * (w & 1) + l;
-    c = 4 * (4 * (w >> 1) + q);
-}
-// k-major tile: logical (r, c) of the input tile at word c * TT_STRIDE + r.
-__host__ __device__ __forceinline__ int tt_word(int r, int c) { return c * TT_STRIDE + r; }
-// Store map: float4 q (0..3) of thread t is output row (tile column)
-// c = 16q + t/16 and output columns (tile rows) 4*(t % 16) .. +3.
-__host__ __device__ __forceinline__ void tt_store_coord(int tid, int q, int &c, int &r) {
-    c = 16 * q + (tid >> 4);
-    r = 4 * (tid & 15);
-}
+__host__ __device__ __forceinline__ int tt_word(int r, int c) { return r * TT_STRIDE + c; }
 
-template <int VI, int VO>  // 4 or 1: 128-bit or 32-bit global access for in / out
-__global__ void __launch_bounds__(TNT) transpose_f32_kernel(const float *__restrict__ in, int ld_in,
-                                                            float *__restrict__ out, int ld_out, int rows,
-                                                            int cols, int tiles_c) {
-    __shared__ __align__(16) float tile[TT * TT_STRIDE];
-    const int tid = threadIdx.x;
+__global__ void __launch_bounds__(32 * TT_ROWS) transpose_f32_kernel(const float *__restrict__ in, int ld_in,
+                                                                     float *__restrict__ out, int ld_out,
+                                                                     int rows, int cols, int tiles_c) {
+    __shared__ float tile[TT * TT_STRIDE];
+    const int tx = threadIdx.x, ty = threadIdx.y;
     const int tr = blockIdx.x / tiles_c, tc = blockIdx.x - tr * tiles_c;
     const int r0 = tr * TT, c0 = tc * TT;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        int r, c;
-        tt_load_coord(tid, q, r, c);
-        const int gr = r0 + r, gc = c0 + c;
-        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (gr < rows) {
-            const float *p = in + static_cast<size_t>(gr) * ld_in + gc;
-            if (VI == 4 && gc + 3 < cols) {
-                v = __ldg(reinterpret_cast<const float4 *>(p));
-            } else {
-                if (gc + 0 < cols) v.x = __ldg(p + 0);
-                if (gc + 1 < cols) v.y = __ldg(p + 1);
-                if (gc + 2 < cols) v.z = __ldg(p + 2);
-                if (gc + 3 < cols) v.w = __ldg(p + 3);
-            }
-        }
-        tile[tt_word(r, c + 0)] = v.x;
-        tile[tt_word(r, c + 1)] = v.y;
-        tile[tt_word(r, c + 2)] = v.z;
-        tile[tt_word(r, c + 3)] = v.w;
-    }
-    __syncthreads();
+    for (int h = 0; h < TT; h += 32) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        int c, r;
-        tt_store_coord(tid, q, c, r);
-        const int orow = c0 + c, ocol = r0 + r;  // out[orow][ocol] = in[ocol][orow]
-        if (orow >= cols) continue;
-        const float4 v = *reinterpret_cast<const float4 *>(tile + tt_word(r, c));
-        float *p = out + static_cast<size_t>(orow) * ld_out + ocol;
-        if (VO == 4 && ocol + 3 < rows) {
-            *reinterpret_cast<float4 *>(p) = v;
-        } else {
-            if (ocol + 0 < rows) p[0] = v.x;
-            if (ocol + 1 < rows) p[1] = v.y;
-            if (ocol + 2 < rows) p[2] = v.z;
-            if (ocol + 3 < rows) p[3] = v.w;
+        for (int j = 0; j < TT; j += TT_ROWS) {
+            const int r = r0 + ty + j, c = c0 + tx + h;
+            if (r < rows && c < cols) tile[tt_word(ty + j, tx + h)] = __ldg(in + static_cast<size_t>(r) * ld_in + c);
+        }
+    }
+    __syncthreads();  // every thread reaches it, edge tiles included
+#pragma unroll
+    for (int h = 0; h < TT; h += 32) {
+#pragma unroll
+        for (int j = 0; j < TT; j += TT_ROWS) {
+            const int orow = c0 + ty + j, ocol = r0 + tx + h;  // out[orow][ocol] = in[ocol][orow]
+            if (orow < cols && ocol < rows)
+                out[static_cast<size_t>(orow) * ld_out + ocol] = tile[tt_word(tx + h, ty + j)];
         }
     }
 }
@@ -159,13 +124,8 @@ extern "C" int transpose_f32(int rows, int cols, const float *in, int ld_in, flo
     if (st != TRANSPOSE_OK || rows == 0 || cols == 0) return st;
     const long long tiles_r = (rows + TT - 1) / TT, tiles_c = (cols + TT - 1) / TT;
     if (tiles_r * tiles_c > INT_MAX) return TRANSPOSE_ERR_INVALID_DIM;
-    const int vi = vec_class(in, ld_in), vo = vec_class(out, ld_out);
-    const dim3 grid(static_cast<unsigned>(tiles_r * tiles_c)), block(TNT);
-    const int tc = static_cast<int>(tiles_c);
-    if (vi == 4 && vo == 4) transpose_f32_kernel<4, 4><<<grid, block, 0, stream>>>(in, ld_in, out, ld_out, rows, cols, tc);
-    else if (vi == 4) transpose_f32_kernel<4, 1><<<grid, block, 0, stream>>>(in, ld_in, out, ld_out, rows, cols, tc);
-    else if (vo == 4) transpose_f32_kernel<1, 4><<<grid, block, 0, stream>>>(in, ld_in, out, ld_out, rows, cols, tc);
-    else transpose_f32_kernel<1, 1><<<grid, block, 0, stream>>>(in, ld_in, out, ld_out, rows, cols, tc);
+    transpose_f32_kernel<<<static_cast<unsigned>(tiles_r * tiles_c), dim3(32, TT_ROWS), 0, stream>>>(
+        in, ld_in, out, ld_out, rows, cols, static_cast<int>(tiles_c));
     return cudaPeekAtLastError() == cudaSuccess ? TRANSPOSE_OK : (cudaGetLastError(), TRANSPOSE_ERR_LAUNCH);
 }
 
@@ -197,19 +157,15 @@ extern "C" int transpose_f32_smem_request(int layout, int kind, int warp, int st
                                           int *width_bytes) {
     if (byte_offset == nullptr || (kind != 0 && kind != 1) || warp < 0 || step < 0) return TRANSPOSE_ERR_INVALID_ARG;
     if (layout == TRANSPOSE_LAYOUT_FAST) {
-        if (warp >= TNT / 32 || step >= (kind == 0 ? 16 : 4)) return TRANSPOSE_ERR_INVALID_ARG;
+        // block (32, 8): warp w is threadIdx.y == w; step s = 8 * h32 + j8 covers
+        // tile rows (writes) or tile columns (reads) w + 8 * j8 at lane offset 32 * h32
+        if (warp >= TT_ROWS || step >= (TT / 32) * (TT / TT_ROWS)) return TRANSPOSE_ERR_INVALID_ARG;
+        const int h = 32 * (step / (TT / TT_ROWS)), j = TT_ROWS * (step % (TT / TT_ROWS));
         for (int lane = 0; lane < 32; ++lane) {
-            const int tid = warp * 32 + lane;
-            int r, c;
-            if (kind == 0) {  // 32-bit stores of component step % 4 of float4 step / 4
-                tt_load_coord(tid, step >> 2, r, c);
-                byte_offset[lane] = 4 * static_cast<int64_t>(tt_word(r, c + (step & 3)));
-            } else {  // 128-bit reads
-                tt_store_coord(tid, step, c, r);
-                byte_offset[lane] = 4 * static_cast<int64_t>(tt_word(r, c));
-            }
+            const int word = kind == 0 ? tt_word(warp + j, lane + h) : tt_word(lane + h, warp + j);
+            byte_offset[lane] = 4 * static_cast<int64_t>(word);
         }
-        if (width_bytes) *width_bytes = kind == 0 ? 4 : 16;
+        if (width_bytes) *width_bytes = 4;
         return TRANSPOSE_OK;
     }
     if (layout != TRANSPOSE_LAYOUT_PADDED && layout != TRANSPOSE_LAYOUT_UNPADDED &&

@@ -41,7 +41,7 @@ typedef enum {
     TRANSPOSE_LAYOUT_PADDED = 0,    /* tile[32][33]: +1 padding ("多一列") */
     TRANSPOSE_LAYOUT_UNPADDED = 1,  /* tile[32][32]: the control, 32-way column conflicts */
     TRANSPOSE_LAYOUT_SWIZZLED = 2,  /* tile[r][c ^ r] ("Padding 之外的选择") */
-    TRANSPOSE_LAYOUT_FAST = 3       /* transpose_f32's 64 x 64 k-major tile */
+    TRANSPOSE_LAYOUT_FAST = 3       /* transpose_f32's 64 x 64 tile, padded to [64][65] */
 } transpose_layout;
 
 /*
@@ -52,8 +52,8 @@ typedef enum {
  *   out, ld_out: DEVICE pointer, row-major cols x rows, row j at out + j*ld_out,
  *                ld_out >= max(1, rows); elements past `rows` in each row are
  *                not touched.
- * Any 4-byte alignment is accepted; 16-byte aligned pointers with leading
- * dimensions that are multiples of 4 use 128-bit global accesses.
+ * Any 4-byte alignment is accepted.  The kernel is the pages' shape scaled up
+ * for bandwidth: 64 x 64 tiles padded to [64][65], block (32, 8).
  */
 int transpose_f32(int rows, int cols, const float *in, int ld_in, float *out, int ld_out,
                   cudaStream_t stream);
@@ -74,12 +74,11 @@ int transpose_f32_layout(int rows, int cols, const float *in, int ld_in, float *
  * the kernel uses, for checking the layout against the bank rule
  * bank = (byte_address / 4) % 32.  Touches no GPU.
  *   layout : PADDED, UNPADDED or SWIZZLED (32 x 32 kernel: warp 0..7, step
- *            0..3) or FAST (64 x 64 kernel: warp 0..7; kind 0 step 0..15,
- *            kind 1 step 0..3).
+ *            0..3) or FAST (64 x 64 kernel: warp 0..7, step 0..15).
  *   kind   : 0 = the tile write that follows the global read,
  *            1 = the tile read that precedes the global write.
  *   byte_offset[32] (out): byte offset each lane touches in the tile.
- *   width_bytes (out): 4 or 16.
+ *   width_bytes (out): 4.
  * Returns TRANSPOSE_OK or TRANSPOSE_ERR_INVALID_ARG.
  */
 int transpose_f32_smem_request(int layout, int kind, int warp, int step, int64_t byte_offset[32],

@@ -38,7 +38,7 @@ def test_unknown_layout_rejected(lib):
 
 
 def _requests(layout, kind):
-    n_steps = {("fast", 0): 16, ("fast", 1): 4}.get((layout, kind), 4)
+    n_steps = 16 if layout == "fast" else 4
     for warp in range(8):
         for step in range(n_steps):
             yield sg.transpose_smem_request(layout, kind, warp, step)
