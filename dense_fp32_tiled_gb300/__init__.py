@@ -6,10 +6,11 @@
 ``transpose_f32(...)`` run the FP32 transpose, the pages' second workload.
 """
 from ._binding import (SGEMM_OK, SgemmError, declared_functions, load_library, sgemm, sgemm_f32,
-                       sgemm_f32_static_scratch, sgemm_f32_ws, smem_request, smem_shape, status_string,
-                       transpose, transpose_f32, transpose_smem_request, transpose_status_string,
-                       workspace_size)
+                       sgemm_f32_3xtf32, sgemm_f32_static_scratch, sgemm_f32_ws, sgemm_tc, smem_request,
+                       smem_shape, status_string, tc_timeouts, tc_workspace_size, transpose, transpose_f32,
+                       transpose_smem_request, transpose_status_string, workspace_size)
 
-__all__ = ["SGEMM_OK", "SgemmError", "declared_functions", "load_library", "sgemm", "sgemm_f32",
+__all__ = ["SGEMM_OK", "SgemmError", "declared_functions", "load_library", "sgemm", "sgemm_f32", "sgemm_f32_3xtf32",
+           "sgemm_tc", "tc_timeouts", "tc_workspace_size",
            "sgemm_f32_static_scratch", "sgemm_f32_ws", "smem_request", "smem_shape", "status_string",
            "transpose", "transpose_f32", "transpose_smem_request", "transpose_status_string", "workspace_size"]

@@ -42,6 +42,12 @@ def load_library():
     lib.sgemm_f32_ws.restype = i32
     lib.sgemm_f32_static_scratch.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p]
     lib.sgemm_f32_static_scratch.restype = i32
+    lib.sgemm_f32_3xtf32.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p, ctypes.c_size_t, p]
+    lib.sgemm_f32_3xtf32.restype = i32
+    lib.sgemm_f32_3xtf32_workspace_size.argtypes = [i32, i32, i32]
+    lib.sgemm_f32_3xtf32_workspace_size.restype = ctypes.c_size_t
+    lib.sgemm_f32_3xtf32_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.sgemm_f32_3xtf32_timeouts.restype = i32
     lib.sgemm_f32_workspace_size.argtypes = [i32, i32, i32]
     lib.sgemm_f32_workspace_size.restype = ctypes.c_size_t
     lib.sgemm_f32_status_string.argtypes = [i32]
@@ -104,6 +110,57 @@ def sgemm_f32_static_scratch(M: int, N: int, K: int, A: int, lda: int, B: int, l
                                                    int(lda), ctypes.c_void_p(int(B) or None), int(ldb),
                                                    ctypes.c_void_p(int(C) or None), int(ldc),
                                                    ctypes.c_void_p(int(stream) or None))
+
+
+def sgemm_f32_3xtf32(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                     workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    """Raw C-ABI call of the tensor-core (3xTF32) variant; returns the status code."""
+    return load_library().sgemm_f32_3xtf32(int(M), int(N), int(K), ctypes.c_void_p(int(A) or None), int(lda),
+                                           ctypes.c_void_p(int(B) or None), int(ldb),
+                                           ctypes.c_void_p(int(C) or None), int(ldc),
+                                           ctypes.c_void_p(int(workspace) or None), int(workspace_bytes),
+                                           ctypes.c_void_p(int(stream) or None))
+
+
+def tc_workspace_size(M: int, N: int, K: int) -> int:
+    return int(load_library().sgemm_f32_3xtf32_workspace_size(int(M), int(N), int(K)))
+
+
+def tc_timeouts() -> int:
+    n = ctypes.c_uint()
+    st = load_library().sgemm_f32_3xtf32_timeouts(ctypes.byref(n))
+    if st != SGEMM_OK:
+        raise SgemmError(st, "sgemm_f32_3xtf32_timeouts")
+    return n.value
+
+
+_tc_workspaces = {}
+
+
+def sgemm_tc(A, B, out=None, stream=None):
+    """C = A @ B through the tensor-core 3xTF32 variant (same FP32 tolerance,
+    not bit-identical to sgemm); the workspace is a cached torch buffer."""
+    import torch
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shape mismatch: {tuple(A.shape)} @ {tuple(B.shape)}")
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    a, lda = _matrix_args(A, M, K, "A")
+    b, ldb = _matrix_args(B, K, N, "B")
+    c, ldc = _matrix_args(out, M, N, "out")
+    nbytes = tc_workspace_size(M, N, K)
+    ws = _tc_workspaces.get(A.device)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=A.device)
+        _tc_workspaces[A.device] = ws
+    s = (stream or torch.cuda.current_stream(A.device)).cuda_stream
+    with torch.cuda.device(A.device):
+        st = sgemm_f32_3xtf32(M, N, K, a, lda, b, ldb, c, ldc, ws.data_ptr(), ws.numel(), s)
+    if st != SGEMM_OK:
+        raise SgemmError(st, "sgemm_f32_3xtf32")
+    return out
 
 
 def workspace_size(M: int, N: int, K: int) -> int:

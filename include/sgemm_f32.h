@@ -149,6 +149,44 @@ int sgemm_f32_static_scratch(int M, int N, int K,
                              float *C, int ldc,
                              cudaStream_t stream);
 
+/*
+ * sgemm_f32_3xtf32 -- the same product on the tensor cores (tcgen05.mma,
+ * TF32 inputs, FP32 accumulation in tensor memory), by the 3xTF32 split:
+ * each FP32 operand x becomes hi = round_to_nearest_tf32(x) and
+ * lo = round_to_nearest_tf32(x - hi), and C = Ahi.Bhi + (Ahi.Blo + Alo.Bhi),
+ * the two groups accumulated separately and added in FP32.  The pages
+ * describe only the CUDA-core path; this variant of the same product meets
+ * the same FP32 acceptance bound as sgemm_f32 but is not bit-identical to it
+ * (different rounding of the partial sums).
+ *
+ *   A, B, C, M, N, K, lda, ldb, ldc : as for sgemm_f32 (any 4-byte alignment).
+ *   workspace       : DEVICE pointer, 256-byte aligned, not overlapping A, B
+ *                     or C, at least sgemm_f32_3xtf32_workspace_size(M,N,K)
+ *                     bytes: it receives the split operands A_hi, A_lo (M x Kp)
+ *                     and the transposed B_hi, B_lo (N x Kp), Kp = K rounded
+ *                     up to 4.  Its contents are not preserved.
+ *   stream          : CUDA stream; two kernels are enqueued (split, MMA).
+ *
+ * Errors are those of sgemm_f32, plus SGEMM_ERR_INVALID_ARG for a missing,
+ * misaligned or too small workspace and SGEMM_ERR_DEVICE when no tensor map
+ * can be encoded.  K == 0 writes C = 0 as sgemm_f32 does.  Every wait inside
+ * the kernel is bounded: a wait that runs out (about a second) leaves C wrong
+ * and increments the counter sgemm_f32_3xtf32_timeouts reports; nothing hangs.
+ */
+int sgemm_f32_3xtf32(int M, int N, int K,
+                     const float *A, int lda,
+                     const float *B, int ldb,
+                     float *C, int ldc,
+                     void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
+/* Workspace bytes sgemm_f32_3xtf32 needs (0 for an empty shape).  Host-only. */
+size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K);
+
+/* Copies into *count whether any tensor-core kernel on the current device gave
+ * up a wait since the library was loaded (0 = never).  Synchronous. */
+int sgemm_f32_3xtf32_timeouts(unsigned *count);
+
 /* Static English description of a status code (never NULL). */
 const char *sgemm_f32_status_string(int status);
 
