@@ -47,6 +47,7 @@ def _args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-tc", action="store_true", help="skip the tensor-core 3xTF32 variant")
     ap.add_argument("--op", choices=["gemm", "transpose"], default="gemm",
                     help="gemm: the FP32 product (default); transpose: the FP32 transpose workload")
     ap.add_argument("--rows", type=int, default=8192, help="transpose: input rows")
@@ -417,6 +418,43 @@ def main():
     if clocks.get("sm_mhz"):
         roofline["frac_at_sampled_clock"] = achieved / (peak * clocks["sm_mhz"] / sm_max)
 
+    # ---- the tensor-core 3xTF32 variant of the same product (same inputs,
+    # same timing protocol); reported beside the CUDA-core path
+    tc = None
+    if not a.no_tc:
+        tc_bytes = sg.tc_workspace_size(w.M, w.N, w.K)
+        tc_ws = torch.empty(max(tc_bytes, 256), dtype=torch.uint8, device=dev)
+
+        def tc_step():
+            st = sg.sgemm_f32_3xtf32(w.M, w.N, w.K, A.data_ptr(), w.lda, B.data_ptr(), w.ldb, C.data_ptr(),
+                                     w.ldc, tc_ws.data_ptr(), tc_bytes, s)
+            if st != 0:
+                raise sg.SgemmError(st, "sgemm_f32_3xtf32")
+        for _ in range(a.warmup):
+            flush.zero_()
+            tc_step()
+        tc_steps = max(3, min(a.steps, 200))
+        t_starts = [torch.cuda.Event(enable_timing=True) for _ in range(tc_steps)]
+        t_ends = [torch.cuda.Event(enable_timing=True) for _ in range(tc_steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(tc_steps):
+            flush.zero_()
+            t_starts[i].record(stream)
+            tc_step()
+            t_ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        tc_ms, tc_value = combine_ranks(statistics.mean(x.elapsed_time(y) for x, y in zip(t_starts, t_ends)),
+                                        flops, world, dev)
+        tf32_peak = float(peaks.get("bf16_tflops") or 1895.4) * 1.1 / 2.25
+        tc_achieved = 3.0 * flops / (tc_ms / 1e3) / 1e12
+        tc = {"value": tc_value, "unit": "TFLOP/s", "ms_per_step": tc_ms, "steps": tc_steps,
+              "entry_point": "sgemm_f32_3xtf32 (split pre-pass + tcgen05 kind::tf32 MMA kernel; timed together)",
+              "gpu_launches": 2 * tc_steps,
+              "roofline": {"bound": "tensor", "achieved": tc_achieved, "peak": tf32_peak, "unit": "TFLOP/s",
+                           "frac": tc_achieved / tf32_peak,
+                           "peak_basis": "TF32 dense = measured bf16 burst x 1.1/2.25 (nominal ratio); "
+                                         "achieved counts the 3 TF32 products per FP32 product"}}
+
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         cpu, _ = cpu_baseline(w, a.cpu_seconds)
@@ -427,7 +465,7 @@ def main():
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": _config(w, world, "flushed before every timed step (256 MiB write, outside the events)"),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": a.steps,
-                "clocks": clocks, "pct_of_fp32_peak": 100.0 * achieved / peak,
+                "clocks": clocks, "pct_of_fp32_peak": 100.0 * achieved / peak, "tensor_core_variant": tc,
                 "ms_min": min(times), "ms_max": max(times), "wall_s_timed_region": t_wall}
         print(json.dumps(line), flush=True)
     if world > 1:
