@@ -140,10 +140,10 @@ class ClockSampler:
                 "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
-def _traffic_from_profile(stamp: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel as built now (same source stamp); else None."""
-    p = os.path.join(ROOT, "profiles", "sgemm_f32_tiled_4096.md")
+def _traffic_from_profile(profile: str, stamp: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the kernel as built now (same kernel source stamp); else None."""
+    p = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(p):
         return None
     vals = {}
@@ -413,7 +413,7 @@ def main():
     peak = sms * FMA_PER_CLK_PER_SM * 2 * sm_max * 1e6 / 1e12
     achieved = flops / (ms / 1e3) / 1e12 if world == 1 else value / world
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": _traffic_from_profile(_stamp()),
+                "traffic": _traffic_from_profile("sgemm_f32_tiled_4096.md", _stamp(SIMT_SOURCES)),
                 "peak_basis": f"{sms} SMs x 128 FP32 FMA/clk x 2 FLOP x {sm_max:.0f} MHz (max SM clock)"}
     if clocks.get("sm_mhz"):
         roofline["frac_at_sampled_clock"] = achieved / (peak * clocks["sm_mhz"] / sm_max)
@@ -452,6 +452,7 @@ def main():
               "gpu_launches": 2 * tc_steps,
               "roofline": {"bound": "tensor", "achieved": tc_achieved, "peak": tf32_peak, "unit": "TFLOP/s",
                            "frac": tc_achieved / tf32_peak,
+                           "traffic": _traffic_from_profile("sgemm_3xtf32_4096.md", _stamp(TC_SOURCES)),
                            "peak_basis": "TF32 dense = measured bf16 burst x 1.1/2.25 (nominal ratio); "
                                          "achieved counts the 3 TF32 products per FP32 product"}}
 
@@ -472,9 +473,13 @@ def main():
         dist.destroy_process_group()
 
 
-def _stamp():
+SIMT_SOURCES = ("sgemm_f32.cu", "smem_layout.cuh")
+TC_SOURCES = ("sgemm_3xtf32.cu",)
+
+
+def _stamp(names):
     from dense_fp32_tiled_gb300 import build as lib_build
-    return lib_build._stamp()
+    return lib_build.kernel_stamp(names)
 
 
 if __name__ == "__main__":

@@ -1,7 +1,7 @@
 """Build step for the CUDA library libsgemm_f32.so (sm_103a only).
 
-Compiles csrc/sgemm_f32.cu with nvcc into the package directory (in-tree, so
-the library that runs is the one built from this checkout).  A stamp of the
+Compiles every csrc/*.cu with one nvcc call into the package directory
+(in-tree, so the library that runs is the one built from this checkout).  A stamp of the
 source hash and flags skips the compile when nothing changed.  The ptxas
 report (registers, spills, shared memory) is kept in _build/ptxas.log.
 """
@@ -39,6 +39,18 @@ def _stamp() -> str:
     for p in _sources():
         h.update(os.path.basename(p).encode())
         with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(FLAGS).encode())
+    return h.hexdigest()
+
+
+def kernel_stamp(names) -> str:
+    """Hash of the named csrc files and the compile flags: identifies one
+    kernel's code, so a profile taken on it can be matched to the build."""
+    h = hashlib.sha256()
+    for n in sorted(names):
+        h.update(n.encode())
+        with open(os.path.join(CSRC, n), "rb") as f:
             h.update(f.read())
     h.update(" ".join(FLAGS).encode())
     return h.hexdigest()
