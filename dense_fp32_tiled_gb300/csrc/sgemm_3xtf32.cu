@@ -3,26 +3,24 @@
 //
 // Each FP32 operand x is split into two TF32 values, hi = rna_tf32(x) and
 // lo = rna_tf32(x - hi), so x = hi + lo + e with |e| <= 2^-22 |x|; then
-//   A.B ~= Ahi.Bhi + (Ahi.Blo + Alo.Bhi)
-// (the dropped Alo.Blo is below 2^-22 |a||b| per product).  The two groups
-// accumulate in separate FP32 TMEM accumulators and are added in FP32 at
-// the end.  The pages describe only the SIMT path (the textbook product
-// C = A x B, vectorised-load page, "这一篇放进 GEMM 路径里看"); this is an
-// additional implementation of the same product, checked against the same
-// FP32 tolerance.
+//   A.B ~= Ahi.Bhi + Ahi.Blo + Alo.Bhi
+// (the dropped Alo.Blo is below 2^-22 |a||b| per product).  The pages
+// describe only the SIMT path (the textbook product C = A x B, vectorised-load
+// page, "这一篇放进 GEMM 路径里看"); this is an additional implementation of
+// the same product, checked against the same FP32 tolerance.
 //
 // Two kernels:
 //   1. split: A -> A_hi, A_lo (M x Kp, row-major) and B -> Bt_hi, Bt_lo
 //      (N x Kp: B transposed, so both operands are K-major), Kp = K rounded
 //      up to 4, in the caller's workspace; the K padding is written as 0.
-//   2. mma: one CTA per 128 x 128 tile of C.  One thread issues TMA copies
-//      (128 x 32 boxes, 128-byte swizzle) of the four operand tiles into a
-//      3-stage ring; one thread issues, per 8-deep K step,
-//        main += Ahi.Bhi,  corr += Ahi.Blo,  corr += Alo.Bhi
-//      (tcgen05.mma kind::tf32, M = 128, N = 128) and releases each stage
-//      with tcgen05.commit; the accumulators restart every 256 K in one of two
-//      tensor-memory buffer sets, and four warps add each finished block into
-//      FP32 registers (tcgen05.ld) and finally store C.
+//   2. mma: one CTA pair (cluster of 2) per 256 x 256 tile of C.  In each CTA
+//      one thread issues TMA copies (128 x 32 boxes, 128-byte swizzle) of its
+//      halves of the four operand panels into a 3-stage ring; one thread of
+//      CTA 0 issues, per 8-deep K step, tcgen05.mma.cta_group::2.kind::tf32
+//      (M = N = 256) for Ahi.Bhi, Ahi.Blo and Alo.Bhi into one accumulator,
+//      which restarts every 128 K in one of two tensor-memory buffer sets;
+//      eight warps per CTA add each finished block into FP32 registers
+//      (tcgen05.ld) and finally store C.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -96,24 +94,37 @@ __global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ A,
 }
 
 // ---- tensor-core kernel ------------------------------------------------------
-constexpr int TBM = 128, TBN = 128, TBK = 32;  // tile; 32 FP32 = one 128-byte swizzle row
+// A CTA pair (a cluster of 2, placed by the hardware on one TPC) computes a
+// 256 x 256 tile of C with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 8).
+// CTA r of the pair holds rows 128r .. 128r+127 of the tile's A panel and rows
+// 128r .. 128r+127 of its Bt panel (C columns n0+128r ..) in shared memory;
+// the tensor core of each SM reads its own A half and both B halves, and
+// writes the accumulator for its 128 rows of C, all 256 columns, into its own
+// tensor memory.  Per SM this reads 8 KiB of operands from shared memory per
+// 128 x 256 x 8 MMA (the 1-CTA 128 x 128 shape needs the same 8 KiB for half
+// the work), which keeps operand traffic below the shared-memory bandwidth.
+constexpr int PM = 256, PN = 256;               // pair tile
+constexpr int TBM = 128, TBK = 32;              // per-CTA box: 128 rows x 32 K (one 128-byte swizzle row)
 constexpr int TSTAGES = 3;
-constexpr int TILE_BYTES = TBM * TBK * 4;      // 16 KiB per operand tile (TBN == TBM)
-constexpr int STAGE_BYTES = 4 * TILE_BYTES;    // A_hi, A_lo, Bt_hi, Bt_lo
+constexpr int BOX_BYTES = TBM * TBK * 4;        // 16 KiB
+constexpr int STAGE_BYTES = 4 * BOX_BYTES;      // halves of A_hi, A_lo, Bt_hi, Bt_lo
 constexpr int MMA_SMEM = TSTAGES * STAGE_BYTES + 1024;  // + alignment slack
-constexpr int KBLK = 8;                        // K tiles (256 K) per tensor-memory block
-constexpr int TMEM_COLS = 512;                 // 2 buffer sets x (main, corr) x 128 columns
-constexpr int TC_THREADS = 192;                // warps 0-3 sum and store, 4 copies, 5 MMAs
+constexpr int KBLK = 4;                         // K tiles (128 K) per accumulation block
+constexpr int ACC_COLS = PN;                    // one FP32 accumulator per column of C
+constexpr int TMEM_COLS = 2 * ACC_COLS;         // two buffer sets
+constexpr int EPI_WARPS = 8;                    // warp w: TMEM lanes 32(w%4).., columns 128(w/4)..
+constexpr int COPY_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
+constexpr int TC_THREADS = (EPI_WARPS + 2) * 32;
 constexpr uint32_t kWaitPolls = 1u << 22;
-static_assert(TBM == TBN, "one tile size for both operands");
+static_assert(PM == 2 * TBM && PN == 2 * TBM, "each CTA holds half of both panels");
 
-// Shared-memory matrix descriptor for a K-major operand tile of 128 rows x
+// Shared-memory matrix descriptor for a K-major operand box of 128 rows x
 // 128 bytes stored with the 128-byte swizzle (the layout a TMA copy with
 // CU_TENSOR_MAP_SWIZZLE_128B writes): 8-row groups of 1024 bytes, start
 // address in 16-byte units (bits 0-13), leading-dimension offset (bits 16-29,
 // unused for this layout, set to 1), stride between 8-row groups (bits
 // 32-45, 1024 bytes), descriptor version 1 (bits 46-47), base offset 0
-// (1024-byte aligned tiles), layout 2 = 128-byte swizzle (bits 61-63).
+// (1024-byte aligned boxes), layout 2 = 128-byte swizzle (bits 61-63).
 __host__ __device__ constexpr uint64_t smem_desc_sw128(uint32_t smem_addr) {
     return (static_cast<uint64_t>((smem_addr >> 4) & 0x3FFF)) | (static_cast<uint64_t>(1) << 16) |
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
@@ -130,19 +141,35 @@ __host__ __device__ constexpr uint32_t instr_desc_tf32(int m, int n) {
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+// Arrive on a barrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
         : "r"(bar), "r"(parity)
         : "memory");
@@ -158,72 +185,90 @@ __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, unsigne
         }
     }
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+// TMA box load into this CTA's shared memory; completion is counted on
+// `cluster_bar`, which may belong to the other CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t cluster_bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];\n" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar)
         : "memory");
 }
-__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
+__device__ __forceinline__ void umma_tf32_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        " tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+// Arrive once on the barrier at this shared address in both CTAs of the pair
+// when all tcgen05 operations issued so far by this thread are complete.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    const uint16_t both = 0x3;
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n" ::"r"(
+            bar),
+        "h"(both)
+        : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns of tensor memory -> 16 registers
+// per thread (thread i gets lane base + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];\n"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 struct TcMaps {
     CUtensorMap a_hi, a_lo, b_hi, b_lo;
 };
 
-// Warps 0-3 read tensor memory (warp w: lanes = tile rows 32w .. 32w+31),
-// warp 4 lane 0 issues the copies, warp 5 owns the TMEM allocation and its
-// lane 0 issues the MMAs.
+// Warps 0-7 read tensor memory and own the C tile, warp 8 lane 0 issues the
+// copies, warp 9 holds the tensor-memory allocation and, in CTA 0 of the
+// pair, its lane 0 issues the MMAs for both CTAs.
 //
-// Tensor memory holds two buffer sets, each a (main, corr) pair of 128 x 128
-// FP32 accumulators.  The K range is cut into blocks of KBLK K tiles; block b
-// accumulates from zero in set b % 2, and warps 0-3 add each finished block
-// (main + corr) into FP32 registers with round-to-nearest adds while the
-// tensor core works on the next block.  The tensor core's own accumulation
-// thus never runs over more than 256 K, which keeps its rounding bias from
-// growing with K.
-__global__ void __launch_bounds__(TC_THREADS, 1)
+// Tensor memory holds two buffer sets of 128 x 256 FP32 accumulators.  The K
+// range is cut into blocks of KBLK K tiles; block b accumulates
+// Ahi.Bhi + Ahi.Blo + Alo.Bhi from zero in set b % 2, and warps 0-7 of both
+// CTAs add each finished block into FP32 registers with round-to-nearest
+// adds while the tensor cores work on the next block.  The tensor core's own
+// accumulation thus never spans more than 128 K, which bounds the rounding
+// bias of its accumulator adds.
+//
+// Barriers: full[s] (CTA 0 only) completes when both CTAs' copies of stage s
+// have landed; empty[s] (both CTAs) when the MMAs reading stage s are done;
+// blk_full[set] (both) when a block's MMAs are done; blk_empty[set] (CTA 0)
+// when the 16 summing warps of the pair have read the set.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, int ldc, int M, int N, int KT,
                     int tiles_m, int tiles_n, int vc, unsigned *timeout_flag) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[TSTAGES], empty_bar[TSTAGES], blk_full[2], blk_empty[2];
     __shared__ uint32_t tmem_base_slot;
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    // same offset in both CTAs: the MMA addresses the peer's boxes with this CTA's descriptors
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
     const int NB = (KT + KBLK - 1) / KBLK;
 
-    // rasterise 8 tile rows at a time
+    // pair tile, rasterised 8 pair-tile rows at a time
+    const int pair = blockIdx.x >> 1;
     const int per_group = 8 * tiles_n;
-    const int g = blockIdx.x / per_group, first = g * 8;
+    const int g = pair / per_group, first = g * 8;
     const int rows_in_group = (tiles_m - first) < 8 ? (tiles_m - first) : 8;
-    const int r_in = blockIdx.x - g * per_group;
+    const int r_in = pair - g * per_group;
     const int tm = first + r_in % rows_in_group, tn = r_in / rows_in_group;
-    const int m0 = tm * TBM, n0 = tn * TBN;
+    const int m0 = tm * PM + static_cast<int>(rank) * TBM;  // this CTA's rows of C and A
+    const int n0 = tn * PN;                                 // the pair tile's first column of C
+    const int nb = n0 + static_cast<int>(rank) * TBM;       // this CTA's rows of Bt
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TSTAGES; ++s) {
@@ -232,39 +277,44 @@ sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, 
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&blk_full[b]), 1);
-            mbar_init(smem_u32(&blk_empty[b]), 128);
+            mbar_init(smem_u32(&blk_empty[b]), 2 * EPI_WARPS);
         }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
-    if (warp == 5) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+    if (warp == MMA_WARP) {  // one warp of each CTA allocates, collectively, in both
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                          smem_u32(&tmem_base_slot)),
                      "n"(TMEM_COLS)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
     __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised before any remote arrive or copy
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
     const uint32_t tmem = tmem_base_slot;
 
-    if (warp == 4) {
-        if (lane == 0) {  // copies
+    if (warp == COPY_WARP) {
+        if (lane == 0) {
+            const uint32_t full0 = peer_addr(smem_u32(&full_bar[0]), 0);  // CTA 0 counts both CTAs' bytes
             for (int kt = 0; kt < KT; ++kt) {
                 const int s = kt % TSTAGES;
                 if (kt >= TSTAGES) mbar_wait(smem_u32(&empty_bar[s]), ((kt / TSTAGES) - 1) & 1, timeout_flag);
-                const uint32_t bar = smem_u32(&full_bar[s]);
+                if (rank == 0) mbar_expect_tx(smem_u32(&full_bar[s]), 2 * STAGE_BYTES);
+                const uint32_t bar = full0 + 8u * s;
                 const uint32_t st = sbase + s * STAGE_BYTES;
-                mbar_expect_tx(bar, STAGE_BYTES);
-                tma_load_2d(st + 0 * TILE_BYTES, &maps.a_hi, kt * TBK, m0, bar);
-                tma_load_2d(st + 1 * TILE_BYTES, &maps.a_lo, kt * TBK, m0, bar);
-                tma_load_2d(st + 2 * TILE_BYTES, &maps.b_hi, kt * TBK, n0, bar);
-                tma_load_2d(st + 3 * TILE_BYTES, &maps.b_lo, kt * TBK, n0, bar);
+                tma_load_2d_pair(st + 0 * BOX_BYTES, &maps.a_hi, kt * TBK, m0, bar);
+                tma_load_2d_pair(st + 1 * BOX_BYTES, &maps.a_lo, kt * TBK, m0, bar);
+                tma_load_2d_pair(st + 2 * BOX_BYTES, &maps.b_hi, kt * TBK, nb, bar);
+                tma_load_2d_pair(st + 3 * BOX_BYTES, &maps.b_lo, kt * TBK, nb, bar);
             }
+            // let the last releases of every stage land before this CTA can exit
+            for (int kt = KT > TSTAGES ? KT - TSTAGES : 0; kt < KT; ++kt)
+                mbar_wait(smem_u32(&empty_bar[kt % TSTAGES]), (kt / TSTAGES) & 1, timeout_flag);
         }
-    } else if (warp == 5) {
-        if (lane == 0) {  // MMAs
-            constexpr uint32_t idesc = instr_desc_tf32(TBM, TBN);
+    } else if (warp == MMA_WARP) {
+        if (rank == 0 && lane == 0) {
+            constexpr uint32_t idesc = instr_desc_tf32(PM, PN);
             for (int kt = 0; kt < KT; ++kt) {
                 const int b = kt / KBLK, set = b & 1;
                 const bool block_start = kt % KBLK == 0;
@@ -272,65 +322,69 @@ sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, 
                 const int s = kt % TSTAGES;
                 mbar_wait(smem_u32(&full_bar[s]), (kt / TSTAGES) & 1, timeout_flag);
                 asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-                const uint32_t t_main = tmem + set * 2 * TBN, t_corr = t_main + TBN;
+                const uint32_t t_acc = tmem + set * ACC_COLS;
                 const uint32_t st = sbase + s * STAGE_BYTES;
 #pragma unroll
                 for (int j = 0; j < TBK / 8; ++j) {  // 8 TF32 = 32 bytes per MMA along K
-                    const uint64_t ahi = smem_desc_sw128(st + 0 * TILE_BYTES + 32 * j);
-                    const uint64_t alo = smem_desc_sw128(st + 1 * TILE_BYTES + 32 * j);
-                    const uint64_t bhi = smem_desc_sw128(st + 2 * TILE_BYTES + 32 * j);
-                    const uint64_t blo = smem_desc_sw128(st + 3 * TILE_BYTES + 32 * j);
-                    const uint32_t acc = (!block_start || j > 0) ? 1u : 0u;
-                    umma_tf32(t_main, ahi, bhi, idesc, acc);
-                    umma_tf32(t_corr, ahi, blo, idesc, acc);
-                    umma_tf32(t_corr, alo, bhi, idesc, 1u);
+                    const uint64_t ahi = smem_desc_sw128(st + 0 * BOX_BYTES + 32 * j);
+                    const uint64_t alo = smem_desc_sw128(st + 1 * BOX_BYTES + 32 * j);
+                    const uint64_t bhi = smem_desc_sw128(st + 2 * BOX_BYTES + 32 * j);
+                    const uint64_t blo = smem_desc_sw128(st + 3 * BOX_BYTES + 32 * j);
+                    umma_tf32_pair(t_acc, ahi, bhi, idesc, (!block_start || j > 0) ? 1u : 0u);
+                    umma_tf32_pair(t_acc, ahi, blo, idesc, 1u);
+                    umma_tf32_pair(t_acc, alo, bhi, idesc, 1u);
                 }
-                umma_commit(smem_u32(&empty_bar[s]));  // stage s free once these MMAs are done
-                if (kt % KBLK == KBLK - 1 || kt == KT - 1) umma_commit(smem_u32(&blk_full[set]));
+                umma_commit_pair(smem_u32(&empty_bar[s]));  // stage s free in both CTAs once these are done
+                if (kt % KBLK == KBLK - 1 || kt == KT - 1) umma_commit_pair(smem_u32(&blk_full[set]));
             }
         }
     } else {
-        // warps 0-3: sum the blocks, then store C = sum
-        float total[TBN];
+        // warps 0-7: sum the blocks, then store C = sum
+        const int q = warp & 3, h = warp >> 2;
+        float total[PN / 2];
 #pragma unroll
-        for (int c = 0; c < TBN; ++c) total[c] = 0.0f;
-        const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+        for (int c = 0; c < PN / 2; ++c) total[c] = 0.0f;
+        const uint32_t t_off = (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(h * (PN / 2));
+        const uint32_t empty0 = peer_addr(smem_u32(&blk_empty[0]), 0);
         for (int b = 0; b < NB; ++b) {
             const int set = b & 1;
             mbar_wait(smem_u32(&blk_full[set]), (b / 2) & 1, timeout_flag);
             __syncwarp();
             asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-            const uint32_t t_main = tmem + set * 2 * TBN + lane_off;  // corr follows at + TBN
+            const uint32_t t_set = tmem + set * ACC_COLS + t_off;
 #pragma unroll
-            for (int c = 0; c < 2 * TBN; c += 32) {  // main columns, then corr columns
-                float v[32];
-                tmem_ld32(t_main + c, v);
+            for (int c = 0; c < PN / 2; c += 16) {
+                float v[16];
+                tmem_ld16(t_set + c, v);
                 asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-                for (int e = 0; e < 32; ++e) total[(c % TBN) + e] += v[e];
+                for (int e = 0; e < 16; ++e) total[c + e] += v[e];
             }
             asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-            mbar_arrive(smem_u32(&blk_empty[set]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(empty0 + 8u * set);
         }
-        const int row = m0 + 32 * warp + lane;
-        if (row < M) {
-            float *crow = C + static_cast<size_t>(row) * ldc + n0;
-            const int left = N - n0;
-            if (vc == 4 && left >= TBN) {
+        const int row = m0 + 32 * q + lane;
+        const int col0 = n0 + h * (PN / 2);
+        if (row < M && col0 < N) {
+            float *crow = C + static_cast<size_t>(row) * ldc + col0;
+            const int left = N - col0;
+            if (vc == 4 && left >= PN / 2) {
 #pragma unroll
-                for (int e = 0; e < TBN; e += 4)
+                for (int e = 0; e < PN / 2; e += 4)
                     *reinterpret_cast<float4 *>(crow + e) = make_float4(total[e], total[e + 1], total[e + 2], total[e + 3]);
             } else {
 #pragma unroll
-                for (int e = 0; e < TBN; ++e)
+                for (int e = 0; e < PN / 2; ++e)
                     if (e < left) crow[e] = total[e];
             }
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
     __syncthreads();
-    if (warp == 5) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "n"(TMEM_COLS)
+    cluster_sync();  // no remote arrive or tensor-memory read of either CTA is still pending
+    if (warp == MMA_WARP) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "n"(TMEM_COLS)
                      : "memory");
     }
 }
@@ -362,7 +416,7 @@ bool encode_operand(CUtensorMap &map, const float *base, int rows, int Kp) {
     if (enc == nullptr) return false;
     const cuuint64_t dim[2] = {static_cast<cuuint64_t>(Kp), static_cast<cuuint64_t>(rows)};
     const cuuint64_t stride[1] = {static_cast<cuuint64_t>(Kp) * 4};
-    const cuuint32_t box[2] = {TBK, TBM};
+    const cuuint32_t box[2] = {TBK, TBM};  // 32 K x 128 rows
     const cuuint32_t ones[2] = {1, 1};
     return enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dim, stride, box, ones,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -427,8 +481,8 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, co
     const auto sw = span(workspace, static_cast<long long>(sgemm_f32_3xtf32_workspace_size(M, N, K)));
     if (overl(sc, sa) || overl(sc, sb)) return SGEMM_ERR_ALIAS;
     if (overl(sw, sa) || overl(sw, sb) || overl(sw, sc)) return SGEMM_ERR_ALIAS;
-    const long long tiles = ((static_cast<long long>(M) + TBM - 1) / TBM) * ((N + TBN - 1) / TBN);
-    if (tiles > INT_MAX) return SGEMM_ERR_INVALID_DIM;
+    const long long pairs = ((static_cast<long long>(M) + PM - 1) / PM) * ((N + PN - 1) / PN);
+    if (2 * pairs > INT_MAX) return SGEMM_ERR_INVALID_DIM;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -465,9 +519,9 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, co
         (void)cudaGetLastError();
         return SGEMM_ERR_DEVICE;
     }
-    const int tiles_m = (M + TBM - 1) / TBM, tiles_n = (N + TBN - 1) / TBN;
+    const int tiles_m = (M + PM - 1) / PM, tiles_n = (N + PN - 1) / PN;
     const int vc = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 4 : 1;
-    sgemm_3xtf32_kernel<<<static_cast<unsigned>(tiles), TC_THREADS, MMA_SMEM, stream>>>(
+    sgemm_3xtf32_kernel<<<static_cast<unsigned>(2 * pairs), TC_THREADS, MMA_SMEM, stream>>>(
         maps, C, ldc, M, N, (Kp + TBK - 1) / TBK, tiles_m, tiles_n, vc, timeout);
     if (cudaPeekAtLastError() != cudaSuccess) {
         (void)cudaGetLastError();

@@ -153,11 +153,12 @@ int sgemm_f32_static_scratch(int M, int N, int K,
  * sgemm_f32_3xtf32 -- the same product on the tensor cores (tcgen05.mma,
  * TF32 inputs, FP32 accumulation in tensor memory), by the 3xTF32 split:
  * each FP32 operand x becomes hi = round_to_nearest_tf32(x) and
- * lo = round_to_nearest_tf32(x - hi), and C = Ahi.Bhi + (Ahi.Blo + Alo.Bhi),
- * the two groups accumulated separately and added in FP32.  The pages
- * describe only the CUDA-core path; this variant of the same product meets
- * the same FP32 acceptance bound as sgemm_f32 but is not bit-identical to it
- * (different rounding of the partial sums).
+ * lo = round_to_nearest_tf32(x - hi), and C = Ahi.Bhi + Ahi.Blo + Alo.Bhi.
+ * The tensor cores accumulate each 128-deep K block from zero; the blocks are
+ * added in FP32 with round-to-nearest.  The pages describe only the CUDA-core
+ * path; this variant of the same product meets the same FP32 acceptance bound
+ * as sgemm_f32 but is not bit-identical to it (different rounding of the
+ * partial sums).
  *
  *   A, B, C, M, N, K, lda, ldb, ldc : as for sgemm_f32 (any 4-byte alignment).
  *   workspace       : DEVICE pointer, 256-byte aligned, not overlapping A, B
