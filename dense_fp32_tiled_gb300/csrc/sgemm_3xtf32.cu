@@ -112,7 +112,8 @@ constexpr int MMA_SMEM = TSTAGES * STAGE_BYTES + 1024;  // + alignment slack
 constexpr int KBLK = 4;                         // K tiles (128 K) per accumulation block
 constexpr int ACC_COLS = PN;                    // one FP32 accumulator per column of C
 constexpr int TMEM_COLS = 2 * ACC_COLS;         // two buffer sets
-constexpr int EPI_WARPS = 8;                    // warp w: TMEM lanes 32(w%4).., columns 128(w/4)..
+constexpr int EPI_WARPS = 8;                    // warp w: TMEM lanes 32(w%4).., columns EPI_COLS(w/4)..
+constexpr int EPI_COLS = PN * 4 / EPI_WARPS;    // accumulator columns per summing thread
 constexpr int COPY_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
 constexpr int TC_THREADS = (EPI_WARPS + 2) * 32;
 constexpr uint32_t kWaitPolls = 1u << 22;
@@ -213,33 +214,108 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
         "h"(both)
         : "memory");
 }
-// 32 lanes x 16 consecutive 32-bit columns of tensor memory -> 16 registers
-// per thread (thread i gets lane base + i).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
+// 32 lanes x 8 consecutive 32-bit columns of tensor memory -> 8 registers per
+// thread (thread i reads lane base + i).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 struct TcMaps {
     CUtensorMap a_hi, a_lo, b_hi, b_lo;
 };
 
-// Warps 0-7 read tensor memory and own the C tile, warp 8 lane 0 issues the
+// Schedule (persistent grid of P CTA pairs).  The first dp_tiles pair tiles
+// (whole waves, a multiple of P) run data-parallel: pair p takes tiles p,
+// p + P, ..., so the tiles in flight at one time are neighbours in the
+// rasterised order and share their operand panels in L2.  The remaining
+// tiles (the last partial wave plus one full wave) are cut into units
+// (tile, K block), NB = ceil(KT / KBLK) blocks per tile, and pair p takes
+// units [floor(pU/Psk), floor((p+1)U/Psk)) of them (stream-K; pairs p >= Psk
+// take none), so every pair ends at the same time whatever the tile count.  A tile whose blocks all fall in
+// one pair is stored directly; a tile cut between pairs is finished by
+// whichever of its parts arrives last (an atomic count per tile half), which
+// adds all parts in part order, so the result does not depend on timing and
+// no CTA waits for another.
+struct SkPlan {
+    int U;         // stream-K units = (T - dp_tiles) * NB (checked on the host to fit an int)
+    int P;         // CTA pairs
+    int Psk;       // pairs that share the stream-K units (<= P, each gets at least MIN_UNITS)
+    int NB;        // K blocks per tile
+    int KT;        // K tiles (TBK deep) per tile
+    int dp_tiles;  // tiles run data-parallel, round-robin over the pairs
+    int tiles_m;   // pair-tile rows
+    int tiles_n;   // pair-tile columns
+};
+
+__device__ __forceinline__ int unit_start(int p, const SkPlan &pl) {
+    return p >= pl.Psk ? pl.U : static_cast<int>(static_cast<long long>(p) * pl.U / pl.Psk);
+}
+// The pair whose stream-K range holds unit u: the largest p with unit_start(p) <= u.
+__device__ __forceinline__ int pair_of_unit(int u, const SkPlan &pl) {
+    return static_cast<int>((static_cast<long long>(u + 1) * pl.Psk - 1) / pl.U);
+}
+// Pair tile t -> (row, column) of pair tiles, walking 8 rows at a time.
+__device__ __forceinline__ void pair_tile_coords(int t, const SkPlan &pl, int &tm, int &tn) {
+    const int per_group = 8 * pl.tiles_n;
+    const int g = t / per_group, first = g * 8;
+    const int rows_in_group = (pl.tiles_m - first) < 8 ? (pl.tiles_m - first) : 8;
+    const int r_in = t - g * per_group;
+    tm = first + r_in % rows_in_group;
+    tn = r_in / rows_in_group;
+}
+// Partial-sum slot of pair p's part of stream-K tile ts (counted from the
+// first stream-K tile): 2p for the pair's first tile, 2p + 1 for its last
+// (tiles in between are whole).
+__device__ __forceinline__ int part_slot(int p, int ts, const SkPlan &pl) {
+    return 2 * p + (ts == unit_start(p, pl) / pl.NB ? 0 : 1);
+}
+// The pair's segments in order: its data-parallel tiles, then its stream-K
+// range cut at tile boundaries.  Segment = tile t, K blocks [kb0, kb1).
+struct SegIter {
+    int dp_next, dp_left;  // next data-parallel tile, how many remain
+    int u, u_end;          // stream-K units still to cover
+    __device__ SegIter(int pair, const SkPlan &pl)
+        : dp_next(pair),
+          dp_left(pl.dp_tiles > pair ? (pl.dp_tiles - pair + pl.P - 1) / pl.P : 0),
+          u(unit_start(pair, pl)),
+          u_end(unit_start(pair + 1, pl)) {}
+    __device__ bool next(const SkPlan &pl, int &t, int &kb0, int &kb1) {
+        if (dp_left > 0) {
+            t = dp_next;
+            kb0 = 0;
+            kb1 = pl.NB;
+            dp_next += pl.P;
+            --dp_left;
+            return true;
+        }
+        if (u >= u_end) return false;
+        const int ts = u / pl.NB;
+        const int seg_end = min(u_end, (ts + 1) * pl.NB);
+        t = pl.dp_tiles + ts;
+        kb0 = u - ts * pl.NB;
+        kb1 = seg_end - ts * pl.NB;
+        u = seg_end;
+        return true;
+    }
+};
+constexpr int SLOT_FLOATS = TBM * PN;  // one CTA's half of a pair tile
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;\n" ::"n"(EPI_WARPS * 32) : "memory"); }
+
+// Warps 0-7 read tensor memory and own the C rows, warp 8 lane 0 issues the
 // copies, warp 9 holds the tensor-memory allocation and, in CTA 0 of the
 // pair, its lane 0 issues the MMAs for both CTAs.
 //
-// Tensor memory holds two buffer sets of 128 x 256 FP32 accumulators.  The K
-// range is cut into blocks of KBLK K tiles; block b accumulates
-// Ahi.Bhi + Ahi.Blo + Alo.Bhi from zero in set b % 2, and warps 0-7 of both
-// CTAs add each finished block into FP32 registers with round-to-nearest
-// adds while the tensor cores work on the next block.  The tensor core's own
+// Tensor memory holds two buffer sets of 128 x 256 FP32 accumulators.  Block
+// g (counted over the pair's whole range) accumulates Ahi.Bhi + Ahi.Blo +
+// Alo.Bhi over its K tiles from zero in set g % 2, and warps 0-7 of both CTAs
+// add each finished block into FP32 registers with round-to-nearest adds
+// while the tensor cores work on the next block.  The tensor core's own
 // accumulation thus never spans more than 128 K, which bounds the rounding
 // bias of its accumulator adds.
 //
@@ -247,28 +323,23 @@ struct TcMaps {
 // have landed; empty[s] (both CTAs) when the MMAs reading stage s are done;
 // blk_full[set] (both) when a block's MMAs are done; blk_empty[set] (CTA 0)
 // when the 16 summing warps of the pair have read the set.
+//
+// Workspace: counts[2T] (zeroed before each launch) and partials[2P][2]
+// [128 x 256], each slot stored 4-column chunk by chunk so that a warp's 32
+// rows write 512 contiguous bytes.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
-sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, int ldc, int M, int N, int KT,
-                    int tiles_m, int tiles_n, int vc, unsigned *timeout_flag) {
+sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, int ldc, int M, int N,
+                    const SkPlan pl, unsigned *__restrict__ counts, float *__restrict__ partials, int vc,
+                    unsigned *timeout_flag) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[TSTAGES], empty_bar[TSTAGES], blk_full[2], blk_empty[2];
     __shared__ uint32_t tmem_base_slot;
+    __shared__ int last_part;
     // same offset in both CTAs: the MMA addresses the peer's boxes with this CTA's descriptors
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
-    const int NB = (KT + KBLK - 1) / KBLK;
-
-    // pair tile, rasterised 8 pair-tile rows at a time
     const int pair = blockIdx.x >> 1;
-    const int per_group = 8 * tiles_n;
-    const int g = pair / per_group, first = g * 8;
-    const int rows_in_group = (tiles_m - first) < 8 ? (tiles_m - first) : 8;
-    const int r_in = pair - g * per_group;
-    const int tm = first + r_in % rows_in_group, tn = r_in / rows_in_group;
-    const int m0 = tm * PM + static_cast<int>(rank) * TBM;  // this CTA's rows of C and A
-    const int n0 = tn * PN;                                 // the pair tile's first column of C
-    const int nb = n0 + static_cast<int>(rank) * TBM;       // this CTA's rows of Bt
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TSTAGES; ++s) {
@@ -297,86 +368,157 @@ sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, 
     if (warp == COPY_WARP) {
         if (lane == 0) {
             const uint32_t full0 = peer_addr(smem_u32(&full_bar[0]), 0);  // CTA 0 counts both CTAs' bytes
-            for (int kt = 0; kt < KT; ++kt) {
-                const int s = kt % TSTAGES;
-                if (kt >= TSTAGES) mbar_wait(smem_u32(&empty_bar[s]), ((kt / TSTAGES) - 1) & 1, timeout_flag);
-                if (rank == 0) mbar_expect_tx(smem_u32(&full_bar[s]), 2 * STAGE_BYTES);
-                const uint32_t bar = full0 + 8u * s;
-                const uint32_t st = sbase + s * STAGE_BYTES;
-                tma_load_2d_pair(st + 0 * BOX_BYTES, &maps.a_hi, kt * TBK, m0, bar);
-                tma_load_2d_pair(st + 1 * BOX_BYTES, &maps.a_lo, kt * TBK, m0, bar);
-                tma_load_2d_pair(st + 2 * BOX_BYTES, &maps.b_hi, kt * TBK, nb, bar);
-                tma_load_2d_pair(st + 3 * BOX_BYTES, &maps.b_lo, kt * TBK, nb, bar);
+            uint32_t it = 0;                                               // K tiles issued so far
+            SegIter seg(pair, pl);
+            int t, kb0, kb1;
+            while (seg.next(pl, t, kb0, kb1)) {
+                int tm, tn;
+                pair_tile_coords(t, pl, tm, tn);
+                const int m0 = tm * PM + static_cast<int>(rank) * TBM, nb = tn * PN + static_cast<int>(rank) * TBM;
+                const int kt1 = min(kb1 * KBLK, pl.KT);
+                for (int kt = kb0 * KBLK; kt < kt1; ++kt, ++it) {
+                    const uint32_t s = it % TSTAGES;
+                    if (it >= TSTAGES) mbar_wait(smem_u32(&empty_bar[s]), ((it / TSTAGES) - 1) & 1, timeout_flag);
+                    if (rank == 0) mbar_expect_tx(smem_u32(&full_bar[s]), 2 * STAGE_BYTES);
+                    const uint32_t bar = full0 + 8u * s;
+                    const uint32_t st = sbase + s * STAGE_BYTES;
+                    tma_load_2d_pair(st + 0 * BOX_BYTES, &maps.a_hi, kt * TBK, m0, bar);
+                    tma_load_2d_pair(st + 1 * BOX_BYTES, &maps.a_lo, kt * TBK, m0, bar);
+                    tma_load_2d_pair(st + 2 * BOX_BYTES, &maps.b_hi, kt * TBK, nb, bar);
+                    tma_load_2d_pair(st + 3 * BOX_BYTES, &maps.b_lo, kt * TBK, nb, bar);
+                }
             }
             // let the last releases of every stage land before this CTA can exit
-            for (int kt = KT > TSTAGES ? KT - TSTAGES : 0; kt < KT; ++kt)
-                mbar_wait(smem_u32(&empty_bar[kt % TSTAGES]), (kt / TSTAGES) & 1, timeout_flag);
+            for (uint32_t j = it > TSTAGES ? it - TSTAGES : 0; j < it; ++j)
+                mbar_wait(smem_u32(&empty_bar[j % TSTAGES]), (j / TSTAGES) & 1, timeout_flag);
         }
     } else if (warp == MMA_WARP) {
         if (rank == 0 && lane == 0) {
             constexpr uint32_t idesc = instr_desc_tf32(PM, PN);
-            for (int kt = 0; kt < KT; ++kt) {
-                const int b = kt / KBLK, set = b & 1;
-                const bool block_start = kt % KBLK == 0;
-                if (block_start && b >= 2) mbar_wait(smem_u32(&blk_empty[set]), ((b / 2) - 1) & 1, timeout_flag);
-                const int s = kt % TSTAGES;
-                mbar_wait(smem_u32(&full_bar[s]), (kt / TSTAGES) & 1, timeout_flag);
-                asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-                const uint32_t t_acc = tmem + set * ACC_COLS;
-                const uint32_t st = sbase + s * STAGE_BYTES;
+            uint32_t it = 0, g = 0;  // K tiles and blocks consumed so far
+            SegIter seg(pair, pl);
+            int t, kb0, kb1;
+            while (seg.next(pl, t, kb0, kb1)) {
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                    const int kt0 = kb * KBLK, kt1 = min(kt0 + KBLK, pl.KT);
+                    const uint32_t set = g & 1;
+                    if (g >= 2) mbar_wait(smem_u32(&blk_empty[set]), ((g / 2) - 1) & 1, timeout_flag);
+                    const uint32_t t_acc = tmem + set * ACC_COLS;
+                    for (int kt = kt0; kt < kt1; ++kt, ++it) {
+                        const uint32_t s = it % TSTAGES;
+                        mbar_wait(smem_u32(&full_bar[s]), (it / TSTAGES) & 1, timeout_flag);
+                        asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+                        const uint32_t st = sbase + s * STAGE_BYTES;
 #pragma unroll
-                for (int j = 0; j < TBK / 8; ++j) {  // 8 TF32 = 32 bytes per MMA along K
-                    const uint64_t ahi = smem_desc_sw128(st + 0 * BOX_BYTES + 32 * j);
-                    const uint64_t alo = smem_desc_sw128(st + 1 * BOX_BYTES + 32 * j);
-                    const uint64_t bhi = smem_desc_sw128(st + 2 * BOX_BYTES + 32 * j);
-                    const uint64_t blo = smem_desc_sw128(st + 3 * BOX_BYTES + 32 * j);
-                    umma_tf32_pair(t_acc, ahi, bhi, idesc, (!block_start || j > 0) ? 1u : 0u);
-                    umma_tf32_pair(t_acc, ahi, blo, idesc, 1u);
-                    umma_tf32_pair(t_acc, alo, bhi, idesc, 1u);
+                        for (int j = 0; j < TBK / 8; ++j) {  // 8 TF32 = 32 bytes per MMA along K
+                            const uint64_t ahi = smem_desc_sw128(st + 0 * BOX_BYTES + 32 * j);
+                            const uint64_t alo = smem_desc_sw128(st + 1 * BOX_BYTES + 32 * j);
+                            const uint64_t bhi = smem_desc_sw128(st + 2 * BOX_BYTES + 32 * j);
+                            const uint64_t blo = smem_desc_sw128(st + 3 * BOX_BYTES + 32 * j);
+                            umma_tf32_pair(t_acc, ahi, bhi, idesc, (kt > kt0 || j > 0) ? 1u : 0u);
+                            umma_tf32_pair(t_acc, ahi, blo, idesc, 1u);
+                            umma_tf32_pair(t_acc, alo, bhi, idesc, 1u);
+                        }
+                        umma_commit_pair(smem_u32(&empty_bar[s]));  // stage s free in both CTAs once these are done
+                    }
+                    umma_commit_pair(smem_u32(&blk_full[set]));
                 }
-                umma_commit_pair(smem_u32(&empty_bar[s]));  // stage s free in both CTAs once these are done
-                if (kt % KBLK == KBLK - 1 || kt == KT - 1) umma_commit_pair(smem_u32(&blk_full[set]));
             }
         }
     } else {
-        // warps 0-7: sum the blocks, then store C = sum
+        // summing warps: per tile segment, sum its blocks, then store or hand over
         const int q = warp & 3, h = warp >> 2;
-        float total[PN / 2];
-#pragma unroll
-        for (int c = 0; c < PN / 2; ++c) total[c] = 0.0f;
-        const uint32_t t_off = (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(h * (PN / 2));
+        const int rloc = 32 * q + lane;  // this thread's row within the CTA's 128
+        const uint32_t t_off = (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(h * (EPI_COLS));
         const uint32_t empty0 = peer_addr(smem_u32(&blk_empty[0]), 0);
-        for (int b = 0; b < NB; ++b) {
-            const int set = b & 1;
-            mbar_wait(smem_u32(&blk_full[set]), (b / 2) & 1, timeout_flag);
-            __syncwarp();
-            asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-            const uint32_t t_set = tmem + set * ACC_COLS + t_off;
+        uint32_t g = 0;
+        SegIter seg(pair, pl);
+        int t, kb0, kb1;
+        while (seg.next(pl, t, kb0, kb1)) {
+            float total[EPI_COLS];
 #pragma unroll
-            for (int c = 0; c < PN / 2; c += 16) {
-                float v[16];
-                tmem_ld16(t_set + c, v);
-                asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+            for (int c = 0; c < EPI_COLS; ++c) total[c] = 0.0f;
+            for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                const uint32_t set = g & 1;
+                mbar_wait(smem_u32(&blk_full[set]), (g / 2) & 1, timeout_flag);
+                __syncwarp();
+                asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+                const uint32_t t_set = tmem + set * ACC_COLS + t_off;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) total[c + e] += v[e];
+                for (int c = 0; c < EPI_COLS; c += 8) {
+                    float v[8];
+                    tmem_ld8(t_set + c, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) total[c + e] += v[e];
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty0 + 8u * set);
             }
-            asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(empty0 + 8u * set);
-        }
-        const int row = m0 + 32 * q + lane;
-        const int col0 = n0 + h * (PN / 2);
-        if (row < M && col0 < N) {
-            float *crow = C + static_cast<size_t>(row) * ldc + col0;
-            const int left = N - col0;
-            if (vc == 4 && left >= PN / 2) {
+            bool store = true;
+            if (kb0 != 0 || kb1 != pl.NB) {
+                // a stream-K tile cut between pairs: hand over or finish
+                const int ts = t - pl.dp_tiles;
+                const int p_first = pair_of_unit(ts * pl.NB, pl), p_last = pair_of_unit((ts + 1) * pl.NB - 1, pl);
+                const int nparts = p_last - p_first + 1;
+                float *mine = partials + (static_cast<size_t>(part_slot(pair, ts, pl)) * 2 + rank) * SLOT_FLOATS;
 #pragma unroll
-                for (int e = 0; e < PN / 2; e += 4)
-                    *reinterpret_cast<float4 *>(crow + e) = make_float4(total[e], total[e + 1], total[e + 2], total[e + 3]);
-            } else {
+                for (int c = 0; c < EPI_COLS; c += 4) {
+                    const int chunk = (h * (EPI_COLS) + c) / 4;
+                    __stcg(reinterpret_cast<float4 *>(mine + (static_cast<size_t>(chunk) * TBM + rloc) * 4),
+                           make_float4(total[c], total[c + 1], total[c + 2], total[c + 3]));
+                }
+                __threadfence();
+                epi_bar();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    unsigned *cnt = counts + 2 * static_cast<size_t>(t) + rank;
+                    const unsigned before = atomicAdd(cnt, 1u);
+                    __threadfence();
+                    last_part = before == static_cast<unsigned>(nparts - 1) ? 1 : 0;
+                }
+                epi_bar();
+                store = last_part != 0;
+                if (store) {
+                    // C = sum of the parts in part order, all read back from the workspace
 #pragma unroll
-                for (int e = 0; e < PN / 2; ++e)
-                    if (e < left) crow[e] = total[e];
+                    for (int c = 0; c < EPI_COLS; ++c) total[c] = 0.0f;
+                    for (int k = 0; k < nparts; ++k) {
+                        const float *slot =
+                            partials + (static_cast<size_t>(part_slot(p_first + k, ts, pl)) * 2 + rank) * SLOT_FLOATS;
+#pragma unroll
+                        for (int c = 0; c < EPI_COLS; c += 4) {
+                            const int chunk = (h * (EPI_COLS) + c) / 4;
+                            const float4 v =
+                                __ldcg(reinterpret_cast<const float4 *>(slot + (static_cast<size_t>(chunk) * TBM + rloc) * 4));
+                            total[c] += v.x;
+                            total[c + 1] += v.y;
+                            total[c + 2] += v.z;
+                            total[c + 3] += v.w;
+                        }
+                    }
+                }
+            }
+            if (store) {
+                int tm, tn;
+                pair_tile_coords(t, pl, tm, tn);
+                const int row = tm * PM + static_cast<int>(rank) * TBM + rloc;
+                const int col0 = tn * PN + h * (EPI_COLS);
+                if (row < M && col0 < N) {
+                    float *crow = C + static_cast<size_t>(row) * ldc + col0;
+                    const int left = N - col0;
+                    if (vc == 4 && left >= EPI_COLS) {
+#pragma unroll
+                        for (int e = 0; e < EPI_COLS; e += 4)
+                            *reinterpret_cast<float4 *>(crow + e) =
+                                make_float4(total[e], total[e + 1], total[e + 2], total[e + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < EPI_COLS; ++e)
+                            if (e < left) crow[e] = total[e];
+                    }
+                }
             }
         }
     }
@@ -425,24 +567,74 @@ bool encode_operand(CUtensorMap &map, const float *base, int rows, int Kp) {
 
 size_t region_bytes(long long rows, long long Kp) { return (static_cast<size_t>(rows * Kp) * 4 + 255) / 256 * 256; }
 
+// A pair gets at least this many K blocks (MIN_UNITS x 128 K), so that small
+// products do not spread thinner than the pipeline can fill.
+constexpr int MIN_UNITS = 2;
+// Cost of handing a split tile over, in 128-K block-times (fitted to timings
+// of 2048^3 .. 8192^3, 16384 x 256 x 4096 and 1024 x 1024 x 8192).
+constexpr int SK_FIXUP_BLOCKS = 6;
+
 std::mutex g_setup_mutex;
 int g_setup_state[64];
+int g_max_pairs[64];
 
+// Per device: the architecture check, the shared-memory opt-in and the number
+// of CTA pairs that fit on the GPU at once (the persistent grid).
 int setup(int dev) {
     if (dev < 0 || dev >= 64) return SGEMM_ERR_DEVICE;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (g_setup_state[dev] == 0) {
-        int major = 0, minor = 0, st = SGEMM_OK;
+        int major = 0, minor = 0, sms = 0, st = SGEMM_OK;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess || major != 10 ||
-            minor != 3 ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || major != 10 ||
+            minor != 3 || sms < 2 ||
             cudaFuncSetAttribute(sgemm_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM) !=
                 cudaSuccess)
             st = SGEMM_ERR_DEVICE;
+        int pairs = sms / 2;
+        if (st == SGEMM_OK) {
+            cudaLaunchConfig_t cfg;
+            memset(&cfg, 0, sizeof cfg);
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = 2;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+            cfg.blockDim = dim3(TC_THREADS);
+            cfg.dynamicSmemBytes = MMA_SMEM;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, sgemm_3xtf32_kernel, &cfg) == cudaSuccess && clusters > 0)
+                pairs = clusters < pairs ? clusters : pairs;
+            else
+                (void)cudaGetLastError();
+        }
         if (st != SGEMM_OK) (void)cudaGetLastError();
+        g_max_pairs[dev] = pairs;
         g_setup_state[dev] = st == SGEMM_OK ? 1 : st;
     }
     return g_setup_state[dev] > 0 ? SGEMM_OK : g_setup_state[dev];
+}
+
+// Workspace layout: A_hi, A_lo (M x Kp), Bt_hi, Bt_lo (N x Kp), the tile
+// counts (2 per pair tile) and the partial-sum slots (2 per pair, 2 halves).
+struct WsLayout {
+    size_t a_lo, bt_hi, bt_lo, counts, partials, bytes;
+};
+WsLayout ws_layout(int M, int N, int K, int pairs) {
+    const long long Kp = (static_cast<long long>(K) + 3) / 4 * 4;
+    const long long T = ((static_cast<long long>(M) + PM - 1) / PM) * ((static_cast<long long>(N) + PN - 1) / PN);
+    WsLayout w;
+    w.a_lo = region_bytes(M, Kp);
+    w.bt_hi = 2 * region_bytes(M, Kp);
+    w.bt_lo = w.bt_hi + region_bytes(N, Kp);
+    w.counts = w.bt_lo + region_bytes(N, Kp);
+    w.partials = w.counts + (static_cast<size_t>(2 * T) * sizeof(unsigned) + 255) / 256 * 256;
+    w.bytes = w.partials + static_cast<size_t>(pairs) * 4 * SLOT_FLOATS * sizeof(float);
+    return w;
 }
 
 // device-side timeout word of the last call, per library instance
@@ -452,8 +644,12 @@ __device__ unsigned g_tc_timeout;
 
 extern "C" size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    const long long Kp = (static_cast<long long>(K) + 3) / 4 * 4;
-    return 2 * region_bytes(M, Kp) + 2 * region_bytes(N, Kp);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return ws_layout(M, N, K, sms / 2 > 0 ? sms / 2 : 1).bytes;
 }
 
 extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C,
@@ -481,8 +677,8 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, co
     const auto sw = span(workspace, static_cast<long long>(sgemm_f32_3xtf32_workspace_size(M, N, K)));
     if (overl(sc, sa) || overl(sc, sb)) return SGEMM_ERR_ALIAS;
     if (overl(sw, sa) || overl(sw, sb) || overl(sw, sc)) return SGEMM_ERR_ALIAS;
-    const long long pairs = ((static_cast<long long>(M) + PM - 1) / PM) * ((N + PN - 1) / PN);
-    if (2 * pairs > INT_MAX) return SGEMM_ERR_INVALID_DIM;
+    const long long T = ((static_cast<long long>(M) + PM - 1) / PM) * ((N + PN - 1) / PN);  // pair tiles
+    if (2 * T > INT_MAX) return SGEMM_ERR_INVALID_DIM;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -493,11 +689,14 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, co
     if (st != SGEMM_OK) return st;
 
     const int Kp = (K + 3) / 4 * 4;
+    const WsLayout wl = ws_layout(M, N, K, g_max_pairs[dev]);
     char *ws = static_cast<char *>(workspace);
     float *a_hi = reinterpret_cast<float *>(ws);
-    float *a_lo = reinterpret_cast<float *>(ws + region_bytes(M, Kp));
-    float *bt_hi = reinterpret_cast<float *>(ws + 2 * region_bytes(M, Kp));
-    float *bt_lo = reinterpret_cast<float *>(ws + 2 * region_bytes(M, Kp) + region_bytes(N, Kp));
+    float *a_lo = reinterpret_cast<float *>(ws + wl.a_lo);
+    float *bt_hi = reinterpret_cast<float *>(ws + wl.bt_hi);
+    float *bt_lo = reinterpret_cast<float *>(ws + wl.bt_lo);
+    unsigned *counts = reinterpret_cast<unsigned *>(ws + wl.counts);
+    float *partials = reinterpret_cast<float *>(ws + wl.partials);
     TcMaps maps;
     memset(&maps, 0, sizeof maps);
     if (!encode_operand(maps.a_hi, a_hi, M, Kp) || !encode_operand(maps.a_lo, a_lo, M, Kp) ||
@@ -519,10 +718,41 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, co
         (void)cudaGetLastError();
         return SGEMM_ERR_DEVICE;
     }
-    const int tiles_m = (M + PM - 1) / PM, tiles_n = (N + PN - 1) / PN;
+    SkPlan pl;
+    pl.tiles_m = (M + PM - 1) / PM;
+    pl.tiles_n = (N + PN - 1) / PN;
+    pl.KT = (Kp + TBK - 1) / TBK;
+    pl.NB = (pl.KT + KBLK - 1) / KBLK;
+    if (T * pl.NB > INT_MAX) return SGEMM_ERR_INVALID_DIM;
+    const long long want = (T * pl.NB + MIN_UNITS - 1) / MIN_UNITS;
+    pl.P = static_cast<int>(want < g_max_pairs[dev] ? want : g_max_pairs[dev]);
+    // Data-parallel takes ceil(T/P) tiles of NB blocks on the longest pair;
+    // splitting the partial last wave takes floor(T/P) tiles plus an equal
+    // share of the rest, plus the hand-over of split tiles (measured at about
+    // SK_FIXUP_BLOCKS block-times).  Pick the shorter.
+    const long long waves = T / pl.P, rest = T % pl.P;
+    const long long sk_units = rest * pl.NB;
+    long long psk = sk_units / MIN_UNITS;
+    psk = psk < 1 ? 1 : (psk > pl.P ? pl.P : psk);
+    const long long dp_cost = (waves + (rest != 0 ? 1 : 0)) * pl.NB;
+    const long long sk_cost = waves * pl.NB + (sk_units + psk - 1) / psk + SK_FIXUP_BLOCKS;
+    if (rest == 0 || sk_cost >= dp_cost) {
+        pl.dp_tiles = static_cast<int>(T);
+        if (T < pl.P) pl.P = static_cast<int>(T);  // one tile per pair, no idle pairs
+        pl.Psk = 1;
+        pl.U = 0;
+    } else {
+        pl.dp_tiles = static_cast<int>(waves * pl.P);
+        pl.Psk = static_cast<int>(psk);
+        pl.U = static_cast<int>(sk_units);
+    }
+    if (cudaMemsetAsync(counts, 0, static_cast<size_t>(2 * T) * sizeof(unsigned), stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
     const int vc = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 4 : 1;
-    sgemm_3xtf32_kernel<<<static_cast<unsigned>(2 * pairs), TC_THREADS, MMA_SMEM, stream>>>(
-        maps, C, ldc, M, N, (Kp + TBK - 1) / TBK, tiles_m, tiles_n, vc, timeout);
+    sgemm_3xtf32_kernel<<<static_cast<unsigned>(2 * pl.P), TC_THREADS, MMA_SMEM, stream>>>(
+        maps, C, ldc, M, N, pl, counts, partials, vc, timeout);
     if (cudaPeekAtLastError() != cudaSuccess) {
         (void)cudaGetLastError();
         return SGEMM_ERR_LAUNCH;

@@ -97,3 +97,62 @@ def test_workspace_checks():
     assert sg.sgemm_f32_3xtf32(64, 64, 64, p, 64, p, 64, C.data_ptr(), 64, ws.data_ptr() + 16, need, 0) == -7
     assert sg.sgemm_f32_3xtf32(64, 64, 64, p, 64, p, 64, C.data_ptr(), 64, ws.data_ptr(), need - 4, 0) == -7
     assert sg.sgemm_f32_3xtf32(64, 64, 64, p, 64, p, 64, p, 64, ws.data_ptr(), need, 0) == -4
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 500, 2048), (129, 255, 4097), (1024, 1024, 1024), (2048, 2048, 2048)])
+def test_split_tiles_deterministic(oracle_lib, M, N, K):
+    """Shapes whose tiles are cut between CTA pairs (2 to 17 parts per tile):
+    the parts are added in part order, so repeated calls are bit-identical,
+    and the result meets the FP32 acceptance bound."""
+    A = synth.matrix(M, K, 77, 0, "normal")
+    B = synth.matrix(K, N, 77, 1, "normal")
+    C1 = _tc(A, B).clone()
+    C2 = _tc(A, B)
+    assert torch.equal(C1, C2)
+    if M * N * K <= 2048 ** 3 // 4:
+        Cr, Sr = oracle_lib.gemm(A, B)
+        tol.assert_close(C1.cpu().numpy(), Cr, Sr, K, f"split {M}x{N}x{K}")
+    else:
+        rows, cols = synth.sample_indices(M, N, 2048, 77)
+        Cs = C1[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
+        ref, S = oracle_lib.gemm_sampled(A, B, rows, cols)
+        tol.assert_close(Cs, ref, S, K, f"split {M}x{N}x{K} sampled")
+    assert sg.tc_timeouts() == 0
+
+
+def test_dirty_workspace(oracle_lib):
+    """A reused workspace full of stale bytes (counts and partial sums
+    included) does not leak into C."""
+    M, N, K = 1000, 1030, 777
+    A = synth.matrix(M, K, 79, 0)
+    B = synth.matrix(K, N, 79, 1)
+    need = sg.tc_workspace_size(M, N, K)
+    ws = torch.full(((need + 3) // 4,), float("nan"), device="cuda")
+    Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    C = torch.empty(M, N, device="cuda")
+    st = sg.sgemm_f32_3xtf32(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), N, C.data_ptr(), N, ws.data_ptr(),
+                             ws.numel() * 4, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    Cr, Sr = oracle_lib.gemm(A, B)
+    tol.assert_close(C.cpu().numpy(), Cr, Sr, K, "dirty workspace")
+    assert sg.tc_timeouts() == 0
+
+
+def test_short_split_region(oracle_lib):
+    """One full wave of CTA pairs plus two tiles: the split region holds fewer
+    K blocks than there are pairs, so only some pairs share it."""
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    M, N, K = 256 * (pairs + 2), 200, 4096
+    A = synth.matrix(M, K, 81, 0, "normal")
+    B = synth.matrix(K, N, 81, 1, "normal")
+    C1 = _tc(A, B).clone()
+    C2 = _tc(A, B)
+    assert torch.equal(C1, C2)
+    rows, cols = synth.sample_indices(M, N, 2048, 81)
+    rows = np.concatenate([rows, np.arange(M - 256, M, dtype=rows.dtype)])  # every row of the last tile
+    cols = np.concatenate([cols, np.full(256, N - 1, dtype=cols.dtype)])
+    Cs = C1[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
+    ref, S = oracle_lib.gemm_sampled(A, B, rows, cols)
+    tol.assert_close(Cs, ref, S, K, "short split region")
+    assert sg.tc_timeouts() == 0
