@@ -118,7 +118,8 @@ struct Problem {
 // The 8 x 8 register tile, held as 32 column pairs for the packed FP32 FMA
 // (fma.rn.f32x2): c[r][j] = (acc[r][2j], acc[r][2j+1]) += (a_r, a_r) * (b_2j, b_2j+1).
 // The B pairs are natural register pairs of the 128-bit fragment reads and
-// a_r is used twice: 32 packed FMAs per k step.
+// a_r is used twice: 32 packed FMAs per k step, issued column pair by column
+// pair so that consecutive ones share their B operand.
 struct Acc {
     float2 c[TM][TN / 2];
 };
@@ -281,11 +282,12 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
             const float a[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const float2 bp[TN / 2] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
                                        make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+            // column pair outermost: consecutive packed FMAs share the B register
+            // pair, so each reads only its A value and its accumulator pair
 #pragma unroll
-            for (int r = 0; r < TM; ++r) {
-                const float2 ar = make_float2(a[r], a[r]);
+            for (int j = 0; j < TN / 2; ++j) {
 #pragma unroll
-                for (int j = 0; j < TN / 2; ++j) acc.c[r][j] = __ffma2_rn(ar, bp[j], acc.c[r][j]);
+                for (int r = 0; r < TM; ++r) acc.c[r][j] = __ffma2_rn(make_float2(a[r], a[r]), bp[j], acc.c[r][j]);
             }
         }
     }
