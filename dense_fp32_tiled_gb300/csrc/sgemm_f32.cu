@@ -454,23 +454,28 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
     const int T = p.tiles_m * p.tiles_n;
     const int G = gridDim.x;
     unsigned *error = flags + (partials ? G : T);
-    for (int lin = blockIdx.x; lin < dp_tiles; lin += G) {
-        int tm, tn;
-        tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
-        Acc acc;
-        acc_zero(acc);
-        mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, 0, KT, pipe, smem, bars, acc);
-        store_tile<false>(p, tm * BM, tn * BN, acc);
-        __syncthreads();  // shared memory free for the next tile
-    }
     const long long total_iters = static_cast<long long>(T - dp_tiles) * KT;
     const long long base = static_cast<long long>(dp_tiles) * KT;
     const long long it_end = base + total_iters * (blockIdx.x + 1) / G;
     long long it = base + total_iters * blockIdx.x / G;
-    while (it < it_end) {
-        const int lin = static_cast<int>(it / KT);
-        const int k0 = static_cast<int>(it % KT);
-        const int k1 = static_cast<int>(k0 + (it_end - it) < KT ? k0 + (it_end - it) : KT);
+    int dp_lin = blockIdx.x;
+    // One loop over segments (whole data-parallel tiles first, then this CTA's
+    // stream-K range cut at tile boundaries), so the main loop is inlined once.
+    for (;;) {
+        int lin, k0, k1;
+        if (dp_lin < dp_tiles) {
+            lin = dp_lin;
+            k0 = 0;
+            k1 = KT;
+            dp_lin += G;
+        } else if (it < it_end) {
+            lin = static_cast<int>(it / KT);
+            k0 = static_cast<int>(it % KT);
+            k1 = static_cast<int>(k0 + (it_end - it) < KT ? k0 + (it_end - it) : KT);
+            it += k1 - k0;
+        } else {
+            break;
+        }
         int tm, tn;
         tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
         Acc acc;
@@ -501,8 +506,7 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
             store_tile<true>(p, tm * BM, tn * BN, acc);
             if (threadIdx.x == 0) flags[lin] = 0u;
         }
-        it += k1 - k0;
-        __syncthreads();  // shared memory free for the next range
+        __syncthreads();  // shared memory free for the next segment
     }
 }
 
