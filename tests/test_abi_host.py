@@ -96,3 +96,30 @@ def test_workspace_size(lib):
 ])
 def test_workspace_call_rejected_on_host(lib, args, code):
     assert sg.sgemm_f32_ws(*args, 0) == code
+
+
+# sgemm_f32_3xtf32: the same host checks, plus the workspace rules; all run
+# before any CUDA call.  (The workspace-overlap check needs the workspace
+# size, which depends on the device: it is tested on the GPU.)  Argument order: M, N, K, A, lda, B, ldb, C, ldc,
+# workspace, workspace_bytes, stream.
+WS = 0x100000  # 256-byte aligned, far from FAKE .. FAKE * 3
+
+
+@pytest.mark.parametrize("args,code", [
+    ((-1, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, WS, 1 << 20), -1),
+    ((4, 4, 8, FAKE, 7, FAKE * 2, 4, FAKE * 3, 4, WS, 1 << 20), -2),      # lda < K
+    ((4, 5, 8, FAKE, 8, FAKE * 2, 5, FAKE * 3, 4, WS, 1 << 20), -2),      # ldc < N
+    ((4, 4, 4, 0, 4, FAKE * 2, 4, FAKE * 3, 4, WS, 1 << 20), -3),         # A null
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, 0, 4, WS, 1 << 20), -3),             # C null
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 1 << 20), -3),       # no workspace
+    ((4, 4, 4, FAKE + 2, 4, FAKE * 2, 4, FAKE * 3, 4, WS, 1 << 20), -7),  # A not 4-byte aligned
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, WS + 16, 1 << 20), -7), # workspace not 256-byte aligned
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE + 16, 4, WS, 1 << 20), -4),     # C overlaps A
+])
+def test_tc_invalid_calls_rejected_on_host(lib, args, code):
+    assert sg.sgemm_f32_3xtf32(*args, 0) == code
+
+
+def test_tc_empty_product_is_a_no_op(lib):
+    assert sg.sgemm_f32_3xtf32(0, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 0, 0) == 0
+    assert sg.sgemm_f32_3xtf32(4, 0, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 0, 0) == 0

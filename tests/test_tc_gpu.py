@@ -97,6 +97,10 @@ def test_workspace_checks():
     assert sg.sgemm_f32_3xtf32(64, 64, 64, p, 64, p, 64, C.data_ptr(), 64, ws.data_ptr() + 16, need, 0) == -7
     assert sg.sgemm_f32_3xtf32(64, 64, 64, p, 64, p, 64, C.data_ptr(), 64, ws.data_ptr(), need - 4, 0) == -7
     assert sg.sgemm_f32_3xtf32(64, 64, 64, p, 64, p, 64, p, 64, ws.data_ptr(), need, 0) == -4
+    # the workspace may not overlap an operand
+    big = torch.empty(need // 4 + 64 * 64 + 64, device="cuda")
+    wsp = (big.data_ptr() + 255) // 256 * 256
+    assert sg.sgemm_f32_3xtf32(64, 64, 64, wsp + need - 256, 64, p, 64, C.data_ptr(), 64, wsp, need, 0) == -4
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 500, 2048), (129, 255, 4097), (1024, 1024, 1024), (2048, 2048, 2048)])
