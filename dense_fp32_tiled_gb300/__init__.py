@@ -2,15 +2,17 @@
 
 ``sgemm(A, B)`` multiplies CUDA float32 tensors through the C-ABI library
 ``libsgemm_f32.so`` (built by ``dense_fp32_tiled_gb300.build.build()``);
-``sgemm_f32(...)`` is the raw C call on device addresses.  ``transpose(x)`` /
+``sgemm_f32(...)`` is the raw C call on device addresses.  ``sgemm_host(A, B)``
+takes CPU tensors (``sgemm_f32_host``: copies overlapped with the product).  ``transpose(x)`` /
 ``transpose_f32(...)`` run the FP32 transpose, the pages' second workload.
 """
-from ._binding import (SGEMM_OK, SgemmError, declared_functions, load_library, sgemm, sgemm_f32,
-                       sgemm_f32_3xtf32, sgemm_f32_static_scratch, sgemm_f32_ws, sgemm_tc, smem_request,
+from ._binding import (SGEMM_OK, SgemmError, declared_functions, host_workspace_size, load_library, sgemm,
+                       sgemm_f32, sgemm_f32_3xtf32, sgemm_f32_host, sgemm_host, sgemm_f32_static_scratch, sgemm_f32_ws, sgemm_tc, smem_request,
                        smem_shape, status_string, tc_timeouts, tc_workspace_size, transpose, transpose_f32,
                        transpose_smem_request, transpose_status_string, workspace_size)
 
-__all__ = ["SGEMM_OK", "SgemmError", "declared_functions", "load_library", "sgemm", "sgemm_f32", "sgemm_f32_3xtf32",
+__all__ = ["SGEMM_OK", "SgemmError", "declared_functions", "host_workspace_size", "load_library", "sgemm",
+           "sgemm_f32", "sgemm_f32_3xtf32", "sgemm_f32_host", "sgemm_host",
            "sgemm_tc", "tc_timeouts", "tc_workspace_size",
            "sgemm_f32_static_scratch", "sgemm_f32_ws", "smem_request", "smem_shape", "status_string",
            "transpose", "transpose_f32", "transpose_smem_request", "transpose_status_string", "workspace_size"]

@@ -48,6 +48,10 @@ def load_library():
     lib.sgemm_f32_3xtf32_workspace_size.restype = ctypes.c_size_t
     lib.sgemm_f32_3xtf32_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.sgemm_f32_3xtf32_timeouts.restype = i32
+    lib.sgemm_f32_host.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p, ctypes.c_size_t, p]
+    lib.sgemm_f32_host.restype = i32
+    lib.sgemm_f32_host_workspace_size.argtypes = [i32, i32, i32]
+    lib.sgemm_f32_host_workspace_size.restype = ctypes.c_size_t
     lib.sgemm_f32_workspace_size.argtypes = [i32, i32, i32]
     lib.sgemm_f32_workspace_size.restype = ctypes.c_size_t
     lib.sgemm_f32_status_string.argtypes = [i32]
@@ -120,6 +124,57 @@ def sgemm_f32_3xtf32(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int,
                                            ctypes.c_void_p(int(C) or None), int(ldc),
                                            ctypes.c_void_p(int(workspace) or None), int(workspace_bytes),
                                            ctypes.c_void_p(int(stream) or None))
+
+
+def sgemm_f32_host(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                   workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    """Raw C-ABI call for HOST operands (device workspace); returns the status code."""
+    return load_library().sgemm_f32_host(int(M), int(N), int(K), ctypes.c_void_p(int(A) or None), int(lda),
+                                         ctypes.c_void_p(int(B) or None), int(ldb),
+                                         ctypes.c_void_p(int(C) or None), int(ldc),
+                                         ctypes.c_void_p(int(workspace) or None), int(workspace_bytes),
+                                         ctypes.c_void_p(int(stream) or None))
+
+
+def host_workspace_size(M: int, N: int, K: int) -> int:
+    return int(load_library().sgemm_f32_host_workspace_size(int(M), int(N), int(K)))
+
+
+def _host_matrix_args(t, rows: int, cols: int, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.is_cuda:
+        raise TypeError(f"{name} must be a CPU float32 tensor")
+    if t.dim() != 2 or tuple(t.shape) != (rows, cols):
+        raise ValueError(f"{name} must have shape ({rows}, {cols}), got {tuple(t.shape)}")
+    if cols > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major with unit column stride")
+    ld = t.stride(0) if rows > 1 else max(1, cols)
+    return t.data_ptr(), max(ld, cols, 1)
+
+
+def sgemm_host(A, B, out=None, device=None, stream=None):
+    """C = A @ B for CPU float32 tensors through sgemm_f32_host (copies in,
+    product on the GPU, copy back).  Pinned tensors give asynchronous copies;
+    the call synchronises the stream before returning, so `out` is ready."""
+    import torch
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shape mismatch: {tuple(A.shape)} @ {tuple(B.shape)}")
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, pin_memory=A.is_pinned())
+    a, lda = _host_matrix_args(A, M, K, "A")
+    b, ldb = _host_matrix_args(B, K, N, "B")
+    c, ldc = _host_matrix_args(out, M, N, "out")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        ws = _workspace(dev, host_workspace_size(M, N, K))
+        st_obj = stream or torch.cuda.current_stream(dev)
+        st = sgemm_f32_host(M, N, K, a, lda, b, ldb, c, ldc, ws.data_ptr(), ws.numel(), st_obj.cuda_stream)
+        if st != SGEMM_OK:
+            raise SgemmError(st, "sgemm_f32_host")
+        st_obj.synchronize()
+    return out
 
 
 def tc_workspace_size(M: int, N: int, K: int) -> int:

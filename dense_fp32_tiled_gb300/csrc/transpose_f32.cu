@@ -112,10 +112,6 @@ int check(int rows, int cols, const float *in, int ld_in, const float *out, int 
     return TRANSPOSE_OK;
 }
 
-int vec_class(const void *p, int ld) {
-    return (reinterpret_cast<uintptr_t>(p) % 16 == 0 && ld % 4 == 0) ? 4 : 1;
-}
-
 }  // namespace
 
 extern "C" int transpose_f32(int rows, int cols, const float *in, int ld_in, float *out, int ld_out,

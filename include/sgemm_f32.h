@@ -117,6 +117,43 @@ int sgemm_f32_ws(int M, int N, int K,
 size_t sgemm_f32_workspace_size(int M, int N, int K);
 
 /*
+ * sgemm_f32_host -- the same product for operands in HOST memory: copies A
+ * and B to the device, multiplies with sgemm_f32_ws, and copies C back.
+ * B goes first; A goes in row panels of about 1024 rows (at most 4), and each
+ * panel's product starts as soon as that panel has landed.  Each finished panel
+ * of C is copied back while the next one computes.  The copies run on two
+ * internal non-blocking streams (created once per device), the products on
+ * `stream`.  The pages have no counterpart: this entry point is the path's
+ * public interface for host-resident data.
+ *   A, B, C, M, N, K, lda, ldb, ldc : as for sgemm_f32, but HOST pointers.
+ *                     Page-locked memory gives asynchronous copies at full
+ *                     speed; pageable memory works, staged by the runtime.
+ *   workspace       : DEVICE pointer, 256-byte aligned, at least
+ *                     sgemm_f32_host_workspace_size(M,N,K) bytes.  It holds
+ *                     dense device copies of B, A and C and the product's
+ *                     own workspace.  Its contents are not preserved, and calls
+ *                     sharing a workspace are ordered by `stream`.
+ *   stream          : work queued on `stream` before the call completes
+ *                     before the workspace is touched; work queued after
+ *                     the call sees C complete in host memory.  The host
+ *                     buffers must stay valid and unchanged until then
+ *                     (e.g. cudaStreamSynchronize(stream)).
+ * Returns the status codes of sgemm_f32_ws, plus SGEMM_ERR_INVALID_ARG for a
+ * missing, misaligned or too small workspace, and SGEMM_ERR_LAUNCH when a copy
+ * cannot be queued.
+ */
+int sgemm_f32_host(int M, int N, int K,
+                   const float *A, int lda,
+                   const float *B, int ldb,
+                   float *C, int ldc,
+                   void *workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
+/* Device workspace bytes sgemm_f32_host needs (0 for an empty or invalid
+ * shape).  Reads device attributes only. */
+size_t sgemm_f32_host_workspace_size(int M, int N, int K);
+
+/*
  * sgemm_f32_static_scratch -- the sgemm_f32_ws product for callers that
  * cannot allocate device memory.
  *

@@ -123,3 +123,23 @@ def test_tc_invalid_calls_rejected_on_host(lib, args, code):
 def test_tc_empty_product_is_a_no_op(lib):
     assert sg.sgemm_f32_3xtf32(0, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 0, 0) == 0
     assert sg.sgemm_f32_3xtf32(4, 0, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 0, 0) == 0
+
+
+# sgemm_f32_host: host-side argument checks (same order as sgemm_f32's, then
+# the device workspace); all return before any CUDA call.
+@pytest.mark.parametrize("args,code", [
+    ((-1, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, WS, 1 << 30), -1),
+    ((4, 4, 8, FAKE, 7, FAKE * 2, 4, FAKE * 3, 4, WS, 1 << 30), -2),       # lda < K
+    ((4, 4, 4, 0, 4, FAKE * 2, 4, FAKE * 3, 4, WS, 1 << 30), -3),          # A null
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 1 << 30), -3),        # no workspace
+    ((4, 4, 4, FAKE, 4, FAKE * 2 + 2, 4, FAKE * 3, 4, WS, 1 << 30), -7),   # B not 4-byte aligned
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, WS + 64, 1 << 30), -7),  # workspace not 256-byte aligned
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 2 + 16, 4, WS, 1 << 30), -4),  # C overlaps B
+    ((4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, WS, 16), -7),            # workspace too small
+])
+def test_host_invalid_calls_rejected_on_host(lib, args, code):
+    assert sg.sgemm_f32_host(*args, 0) == code
+
+
+def test_host_empty_product_is_a_no_op(lib):
+    assert sg.sgemm_f32_host(0, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, 0, 0) == 0
