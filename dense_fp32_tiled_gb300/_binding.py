@@ -300,7 +300,7 @@ def sgemm(A, B, out=None, stream=None, balanced=True):
 
 
 # ---- transpose ------------------------------------------------------------
-TRANSPOSE_LAYOUTS = {"padded": 0, "unpadded": 1, "swizzled": 2, "fast": 3}
+TRANSPOSE_LAYOUTS = {"padded": 0, "unpadded": 1, "swizzled": 2, "fast": 3, "fast_vec": 4}
 
 
 def transpose_f32(rows: int, cols: int, inp: int, ld_in: int, out: int, ld_out: int, stream: int = 0,

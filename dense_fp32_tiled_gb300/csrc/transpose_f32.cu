@@ -8,7 +8,9 @@
 // "Padding 之外的选择" offers an XOR swizzle instead.  transpose_f32_layout
 // runs that kernel shape with the three layouts (padded, unpadded control,
 // swizzled) for measurement.  transpose_f32 is the same design scaled up for
-// bandwidth: 64 x 64 tiles padded to [64][65], 16 elements per thread.
+// bandwidth: 64 x 64 tiles, 16 elements per thread, with 16-byte vector
+// accesses and a chunk-swizzled tile when rows are 16-byte aligned, else
+// scalar accesses and a [64][65] padded tile.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -94,6 +96,61 @@ __global__ void __launch_bounds__(32 * TT_ROWS) transpose_f32_kernel(const float
     }
 }
 
+// ---- 16-byte vector kernel (aligned rows, sizes multiples of 4) -----------
+// Same 64 x 64 tile and block, but every global access is a 16-byte vector:
+// a warp reads 2 input rows x 256 bytes per instruction and writes 4 output
+// rows x 128 bytes.  The tile is stored unpadded, its 16-byte chunks
+// XOR-swizzled by row ("Padding 之外的选择"): element (r, c) at word
+//   64 r + 4 ((c / 4) ^ ((r / 4) % 8)) + c % 4,
+// so that the 128-bit tile writes of a quarter-warp cover 8 distinct chunk
+// positions, and the scalar tile reads (lane l: rows 4(l/4) + e apart by 4,
+// column 4j + l % 4) fall in 32 distinct banks.
+__host__ __device__ __forceinline__ int tv_word(int r, int c) {
+    return r * TT + 4 * ((c >> 2) ^ ((r >> 2) & 7)) + (c & 3);
+}
+// Thread t's q-th tile write: input row r, columns 4 c4 .. 4 c4 + 3.
+__host__ __device__ __forceinline__ void tv_load_coord(int t, int q, int &r, int &c4) {
+    const int idx = q * 256 + t;
+    r = idx >> 4;
+    c4 = idx & 15;
+}
+// Lane l of warp w, q-th output vector: output row (tile column) C, output
+// columns (tile rows) 4 oc4 .. 4 oc4 + 3.
+__host__ __device__ __forceinline__ void tv_store_coord(int w, int l, int q, int &C, int &oc4) {
+    const int i = w * 4 + q;
+    C = 4 * (i >> 1) + (l & 3);
+    oc4 = (l >> 2) + 8 * (i & 1);
+}
+
+__global__ void __launch_bounds__(32 * TT_ROWS) transpose_f32_vec_kernel(const float *__restrict__ in, int ld_in,
+                                                                         float *__restrict__ out, int ld_out,
+                                                                         int rows, int cols, int tiles_c) {
+    __shared__ __align__(16) float tile[TT * TT];
+    const int t = threadIdx.y * 32 + threadIdx.x;
+    const int tr = blockIdx.x / tiles_c, tc = blockIdx.x - tr * tiles_c;
+    const int r0 = tr * TT, c0 = tc * TT;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        int r, c4;
+        tv_load_coord(t, q, r, c4);
+        if (r0 + r < rows && c0 + 4 * c4 < cols)
+            *reinterpret_cast<float4 *>(tile + tv_word(r, 4 * c4)) =
+                __ldg(reinterpret_cast<const float4 *>(in + static_cast<size_t>(r0 + r) * ld_in + c0 + 4 * c4));
+    }
+    __syncthreads();  // every thread reaches it, edge tiles included
+    const int w = threadIdx.y, l = threadIdx.x;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        int C, oc4;
+        tv_store_coord(w, l, q, C, oc4);
+        if (c0 + C < cols && r0 + 4 * oc4 < rows) {
+            const float4 v = make_float4(tile[tv_word(4 * oc4 + 0, C)], tile[tv_word(4 * oc4 + 1, C)],
+                                         tile[tv_word(4 * oc4 + 2, C)], tile[tv_word(4 * oc4 + 3, C)]);
+            *reinterpret_cast<float4 *>(out + static_cast<size_t>(c0 + C) * ld_out + r0 + 4 * oc4) = v;
+        }
+    }
+}
+
 bool overlap(const void *p, long long pb, const void *q, long long qb) {
     if (pb <= 0 || qb <= 0) return false;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), b0 = reinterpret_cast<uintptr_t>(q);
@@ -120,8 +177,14 @@ extern "C" int transpose_f32(int rows, int cols, const float *in, int ld_in, flo
     if (st != TRANSPOSE_OK || rows == 0 || cols == 0) return st;
     const long long tiles_r = (rows + TT - 1) / TT, tiles_c = (cols + TT - 1) / TT;
     if (tiles_r * tiles_c > INT_MAX) return TRANSPOSE_ERR_INVALID_DIM;
-    transpose_f32_kernel<<<static_cast<unsigned>(tiles_r * tiles_c), dim3(32, TT_ROWS), 0, stream>>>(
-        in, ld_in, out, ld_out, rows, cols, static_cast<int>(tiles_c));
+    const bool vec = (reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16 == 0 &&
+                     ld_in % 4 == 0 && ld_out % 4 == 0 && rows % 4 == 0 && cols % 4 == 0;
+    if (vec)
+        transpose_f32_vec_kernel<<<static_cast<unsigned>(tiles_r * tiles_c), dim3(32, TT_ROWS), 0, stream>>>(
+            in, ld_in, out, ld_out, rows, cols, static_cast<int>(tiles_c));
+    else
+        transpose_f32_kernel<<<static_cast<unsigned>(tiles_r * tiles_c), dim3(32, TT_ROWS), 0, stream>>>(
+            in, ld_in, out, ld_out, rows, cols, static_cast<int>(tiles_c));
     return cudaPeekAtLastError() == cudaSuccess ? TRANSPOSE_OK : (cudaGetLastError(), TRANSPOSE_ERR_LAUNCH);
 }
 
@@ -162,6 +225,26 @@ extern "C" int transpose_f32_smem_request(int layout, int kind, int warp, int st
             byte_offset[lane] = 4 * static_cast<int64_t>(word);
         }
         if (width_bytes) *width_bytes = 4;
+        return TRANSPOSE_OK;
+    }
+    if (layout == TRANSPOSE_LAYOUT_FAST_VEC) {
+        // kind 0: step q = 0..3, one 128-bit write per lane; kind 1: step
+        // 4 q + e = 0..15, the scalar read of component e of the q-th vector
+        if (warp >= TT_ROWS || step >= (kind == 0 ? 4 : 16)) return TRANSPOSE_ERR_INVALID_ARG;
+        for (int lane = 0; lane < 32; ++lane) {
+            int word;
+            if (kind == 0) {
+                int r, c4;
+                tv_load_coord(warp * 32 + lane, step, r, c4);
+                word = tv_word(r, 4 * c4);
+            } else {
+                int C, oc4;
+                tv_store_coord(warp, lane, step >> 2, C, oc4);
+                word = tv_word(4 * oc4 + (step & 3), C);
+            }
+            byte_offset[lane] = 4 * static_cast<int64_t>(word);
+        }
+        if (width_bytes) *width_bytes = kind == 0 ? 16 : 4;
         return TRANSPOSE_OK;
     }
     if (layout != TRANSPOSE_LAYOUT_PADDED && layout != TRANSPOSE_LAYOUT_UNPADDED &&

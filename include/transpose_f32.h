@@ -41,7 +41,9 @@ typedef enum {
     TRANSPOSE_LAYOUT_PADDED = 0,    /* tile[32][33]: +1 padding ("多一列") */
     TRANSPOSE_LAYOUT_UNPADDED = 1,  /* tile[32][32]: the control, 32-way column conflicts */
     TRANSPOSE_LAYOUT_SWIZZLED = 2,  /* tile[r][c ^ r] ("Padding 之外的选择") */
-    TRANSPOSE_LAYOUT_FAST = 3       /* transpose_f32's 64 x 64 tile, padded to [64][65] */
+    TRANSPOSE_LAYOUT_FAST = 3,      /* transpose_f32's scalar path: 64 x 64 tile padded to [64][65] */
+    TRANSPOSE_LAYOUT_FAST_VEC = 4   /* transpose_f32's 16-byte path: 64 x 64 tile, 16-byte chunks
+                                       of row r XOR-swizzled by (r / 4) % 8 */
 } transpose_layout;
 
 /*
@@ -53,7 +55,11 @@ typedef enum {
  *                ld_out >= max(1, rows); elements past `rows` in each row are
  *                not touched.
  * Any 4-byte alignment is accepted.  The kernel is the pages' shape scaled up
- * for bandwidth: 64 x 64 tiles padded to [64][65], block (32, 8).
+ * for bandwidth: 64 x 64 tiles, block (32, 8).  When in and out are 16-byte
+ * aligned and ld_in, ld_out, rows and cols are multiples of 4, every global
+ * access is a 16-byte vector and the tile's 16-byte chunks are XOR-swizzled
+ * (TRANSPOSE_LAYOUT_FAST_VEC); otherwise accesses are 4-byte and the tile is
+ * padded to [64][65] (TRANSPOSE_LAYOUT_FAST).
  */
 int transpose_f32(int rows, int cols, const float *in, int ld_in, float *out, int ld_out,
                   cudaStream_t stream);
@@ -74,11 +80,13 @@ int transpose_f32_layout(int rows, int cols, const float *in, int ld_in, float *
  * the kernel uses, for checking the layout against the bank rule
  * bank = (byte_address / 4) % 32.  Touches no GPU.
  *   layout : PADDED, UNPADDED or SWIZZLED (32 x 32 kernel: warp 0..7, step
- *            0..3) or FAST (64 x 64 kernel: warp 0..7, step 0..15).
+ *            0..3), FAST (64 x 64 scalar kernel: warp 0..7, step 0..15) or
+ *            FAST_VEC (64 x 64 vector kernel: warp 0..7, step 0..3 for
+ *            kind 0, 0..15 for kind 1).
  *   kind   : 0 = the tile write that follows the global read,
  *            1 = the tile read that precedes the global write.
  *   byte_offset[32] (out): byte offset each lane touches in the tile.
- *   width_bytes (out): 4.
+ *   width_bytes (out): bytes per lane access (16 for FAST_VEC writes, else 4).
  * Returns TRANSPOSE_OK or TRANSPOSE_ERR_INVALID_ARG.
  */
 int transpose_f32_smem_request(int layout, int kind, int warp, int step, int64_t byte_offset[32],

@@ -81,3 +81,18 @@ def test_alias_rejected_with_device_pointers():
     t = torch.zeros(64 * 64 * 2, device="cuda")
     p = t.data_ptr()
     assert sg.transpose_f32(64, 64, p, 64, p + 4 * 100, 64, 0) == -4
+
+
+@pytest.mark.parametrize("rows,cols,ld_in,ld_out,in_off,out_off", [
+    (4, 4, 4, 4, 0, 0), (64, 64, 64, 64, 0, 0), (68, 132, 132, 68, 0, 0), (1000, 1032, 1036, 1004, 4, 8),
+    (4096, 260, 264, 4100, 0, 4), (260, 4096, 4096, 260, 8, 0)])
+def test_vector_path_bit_exact(oracle_lib, rows, cols, ld_in, ld_out, in_off, out_off):
+    """16-byte aligned rows, sizes multiples of 4: transpose_f32 takes the
+    16-byte vector kernel (swizzled tile), ragged edge tiles included, and
+    leaves the padding of both matrices untouched."""
+    x = synth.matrix(rows, cols, 59, 0, "normal", ld=ld_in, pad_value=np.nan)
+    st, got = _run(x, rows, cols, ld_in, ld_out, None, in_off, out_off, fill=-3.0)
+    assert st == 0
+    ref = np.full((cols - 1) * ld_out + rows, -3.0, dtype=np.float32)
+    oracle_lib.transpose(x, rows=rows, cols=cols, ld_in=ld_in, ld_out=ld_out, out=ref)
+    np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))

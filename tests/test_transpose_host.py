@@ -38,13 +38,13 @@ def test_unknown_layout_rejected(lib):
 
 
 def _requests(layout, kind):
-    n_steps = 16 if layout == "fast" else 4
+    n_steps = 16 if layout == "fast" or (layout == "fast_vec" and kind == 1) else 4
     for warp in range(8):
         for step in range(n_steps):
             yield sg.transpose_smem_request(layout, kind, warp, step)
 
 
-@pytest.mark.parametrize("layout", ["padded", "swizzled", "fast"])
+@pytest.mark.parametrize("layout", ["padded", "swizzled", "fast", "fast_vec"])
 @pytest.mark.parametrize("kind", [0, 1])
 def test_conflict_free_layouts(lib, oracle_lib, layout, kind):
     for offs, width in _requests(layout, kind):
@@ -60,9 +60,17 @@ def test_unpadded_column_reads_are_32_way(lib, oracle_lib):
 
 
 def test_tiles_are_bijections(lib):
-    for layout, words in (("padded", 32 * 32), ("unpadded", 32 * 32), ("swizzled", 32 * 32), ("fast", 64 * 64)):
+    for layout, words in (("padded", 32 * 32), ("unpadded", 32 * 32), ("swizzled", 32 * 32), ("fast", 64 * 64),
+                          ("fast_vec", 64 * 64)):
         for kind in (0, 1):
             seen = []
             for offs, width in _requests(layout, kind):
                 seen += [o // 4 + w for o in offs for w in range(width // 4)]
             assert len(seen) == words and len(set(seen)) == words, (layout, kind)
+
+
+def test_vector_tile_writes_are_128_bit(lib):
+    for warp in range(8):
+        for step in range(4):
+            offs, width = sg.transpose_smem_request("fast_vec", 0, warp, step)
+            assert width == 16 and all(o % 16 == 0 for o in offs)
