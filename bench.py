@@ -289,13 +289,16 @@ def run_transpose(a):
     nbytes = 2.0 * 4 * rows * cols
     gbs = nbytes / (ms / 1e3) / 1e9
     peak = float(_measured_peaks().get("hbm_gbs") or 6800.0)
+    # DRAM bytes per launch from the committed ncu summary (taken on the 8192 x 8192 vector path)
+    traffic = (_traffic_from_profile("transpose_f32_8192.md", _stamp(TRANSPOSE_SOURCES))
+               if a.layout == "fast" and (rows, cols) == (8192, 8192) else None)
     line = {"metric": "FP32 transpose GB/s (bytes read + written)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"transpose_{rows}x{cols}", "rows": rows, "cols": cols, "kernel": a.layout,
                        "inputs": "uniform seed 61", "l2": "flushed before every timed step"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "traffic": None, "peak_basis": "measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
+                         "traffic": traffic, "peak_basis": "measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
             "gpu_launches": a.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
@@ -481,6 +484,7 @@ def main():
 
 SIMT_SOURCES = ("sgemm_f32.cu", "smem_layout.cuh")
 TC_SOURCES = ("sgemm_3xtf32.cu",)
+TRANSPOSE_SOURCES = ("transpose_f32.cu",)
 
 
 def _stamp(names):
