@@ -27,6 +27,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -48,6 +49,7 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-tc", action="store_true", help="skip the tensor-core 3xTF32 variant")
+    ap.add_argument("--clocks-csv", default=None, help="keep the raw nvidia-smi samples in this file")
     ap.add_argument("--op", choices=["gemm", "transpose"], default="gemm",
                     help="gemm: the FP32 product (default); transpose: the FP32 transpose workload")
     ap.add_argument("--rows", type=int, default=8192, help="transpose: input rows")
@@ -76,11 +78,11 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, uuid: str | None):
+    def __init__(self, uuid: str | None, path: str | None = None):
         self.uuid = uuid
         self.proc = None
         self.t0 = self.t1 = None  # wall-clock bounds of the timed region
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(), f"sgemm_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -275,7 +277,7 @@ def run_transpose(a):
         uuid = "GPU-" + str(props.uuid)
     except Exception:
         pass
-    with ClockSampler(uuid) as clk:
+    with ClockSampler(uuid, a.clocks_csv) as clk:
         torch.cuda.synchronize(dev)
         clk.t0 = time.time()
         for i in range(a.steps):
@@ -363,7 +365,7 @@ def main():
         pass
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
-    with ClockSampler(uuid) as clk:
+    with ClockSampler(uuid, a.clocks_csv) as clk:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
