@@ -52,6 +52,9 @@ def load_library():
     lib.sgemm_f32_host.restype = i32
     lib.sgemm_f32_host_workspace_size.argtypes = [i32, i32, i32]
     lib.sgemm_f32_host_workspace_size.restype = ctypes.c_size_t
+    lib.sgemm_f32_ws_schedule.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, ctypes.POINTER(ctypes.c_int),
+                                          ctypes.POINTER(ctypes.c_longlong)]
+    lib.sgemm_f32_ws_schedule.restype = i32
     lib.sgemm_f32_workspace_size.argtypes = [i32, i32, i32]
     lib.sgemm_f32_workspace_size.restype = ctypes.c_size_t
     lib.sgemm_f32_status_string.argtypes = [i32]
@@ -216,6 +219,17 @@ def sgemm_tc(A, B, out=None, stream=None):
     if st != SGEMM_OK:
         raise SgemmError(st, "sgemm_f32_3xtf32")
     return out
+
+
+def ws_schedule(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int):
+    """(status, kind, words): the schedule sgemm_f32_ws uses for these arguments
+    and the leading workspace words it zero-fills and leaves zero (host-only)."""
+    kind, words = ctypes.c_int(), ctypes.c_longlong()
+    st = load_library().sgemm_f32_ws_schedule(int(M), int(N), int(K), ctypes.c_void_p(int(A) or None), int(lda),
+                                              ctypes.c_void_p(int(B) or None), int(ldb),
+                                              ctypes.c_void_p(int(C) or None), int(ldc), ctypes.byref(kind),
+                                              ctypes.byref(words))
+    return st, kind.value, words.value
 
 
 def workspace_size(M: int, N: int, K: int) -> int:

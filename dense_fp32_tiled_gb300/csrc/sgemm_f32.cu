@@ -357,6 +357,9 @@ template <int VA, int VB, bool TMA>
 __global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p, const __grid_constant__ Maps maps) {
     extern __shared__ float smem_raw[];
     __shared__ __align__(8) uint64_t bar_mem[STAGES];
+    // a split-tail grid queued behind this one may start as SMs free up: it
+    // writes other tiles and reads nothing this grid writes
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     float *smem = aligned_smem(smem_raw);
     const uint32_t bars = smem_u32(bar_mem);
     init_bars<TMA>(bars);
@@ -510,6 +513,51 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
     }
 }
 
+// Split tail.  The last R = T mod G tiles (G = co-resident CTAs) would leave
+// a partial last wave; instead each is cut into S equal K ranges and the S*R
+// CTAs of this grid, queued behind the one-CTA-per-tile grid of the other
+// tiles, start as soon as SMs free up (programmatic dependent launch).  CTA
+// c computes part c % S of tile dp_tiles + c / S into partial-sum slot c and
+// counts itself in counts[c / S]; the part that arrives last adds all S
+// slots in part order and stores the tile: deterministic, and no CTA waits
+// for another.
+template <int VA, int VB, bool TMA>
+__global__ void __launch_bounds__(NT, 2)
+sgemm_f32_tail_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles, const int parts,
+                      unsigned *counts, float *slots) {
+    extern __shared__ float smem_raw[];
+    __shared__ __align__(8) uint64_t bar_mem[STAGES];
+    __shared__ int last;
+    float *smem = aligned_smem(smem_raw);
+    const uint32_t bars = smem_u32(bar_mem);
+    init_bars<TMA>(bars);
+    const int c = blockIdx.x, tile = c / parts, part = c - tile * parts;
+    const int KT = (p.K + BK - 1) / BK;
+    const int k0 = static_cast<int>(static_cast<long long>(KT) * part / parts);
+    const int k1 = static_cast<int>(static_cast<long long>(KT) * (part + 1) / parts);
+    int tm, tn;
+    tile_of(dp_tiles + tile, p.tiles_m, p.tiles_n, tm, tn);
+    Acc acc;
+    acc_zero(acc);
+    uint32_t pipe = 0;
+    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
+    store_partial(slots + static_cast<size_t>(c) * (BM * BN), acc);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned before = atomicAdd(counts + tile, 1u);
+        __threadfence();
+        last = before == static_cast<unsigned>(parts - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (last) {
+        if (threadIdx.x == 0) counts[tile] = 0u;  // every part has counted itself: leave the word zero
+        acc_zero(acc);
+        for (int k = 0; k < parts; ++k) add_partial(slots + static_cast<size_t>(tile * parts + k) * (BM * BN), acc);
+        store_tile<false>(p, tm * BM, tn * BN, acc);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -528,6 +576,8 @@ const SkKernel kSk[kVariants] = {
     sgemm_f32_streamk_kernel<4, 1, false>, sgemm_f32_streamk_kernel<1, 4, false>,
     sgemm_f32_streamk_kernel<1, 2, false>, sgemm_f32_streamk_kernel<1, 1, false>,
     sgemm_f32_streamk_kernel<4, 4, true>};
+using TailKernel = void (*)(Problem, Maps, int, int, unsigned *, float *);
+const TailKernel kTail = sgemm_f32_tail_kernel<4, 4, true>;  // tensor-copy variant only
 
 // cuTensorMapEncodeTiled, fetched from the driver at run time (no link
 // against libcuda).  Null when unavailable: the cp.async kernels are used.
@@ -608,6 +658,11 @@ int setup_device(int dev, DeviceInfo *out) {
                         cudaSuccess)
                     st = SGEMM_ERR_DEVICE;
             }
+            if (st == SGEMM_OK &&
+                (cudaFuncSetAttribute(kTail, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
+                 cudaFuncSetAttribute(kTail, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      cudaSharedmemCarveoutMaxShared) != cudaSuccess))
+                st = SGEMM_ERR_DEVICE;
         }
         if (st != SGEMM_OK) (void)cudaGetLastError();  // do not leave our failure sticky for the caller
         d.state = st == SGEMM_OK ? 1 : st;
@@ -663,30 +718,53 @@ int check_args(int M, int N, int K, const float *A, int lda, const float *B, int
 // stream-K over the last wave-and-a-bit of tiles, partial sums handed over
 // through C (needs flags only).  kind 2: stream-K over all tiles with any
 // number of parts per tile, partial sums handed over through per-CTA slots
-// (for fewer tiles than co-resident CTAs).
+// (for fewer tiles than co-resident CTAs).  kind 3: one CTA per tile for
+// all whole waves, and the R leftover tiles cut into S parts each in a
+// split-tail grid (tensor-copy variant only).
 struct Plan {
     int kind;
     long long grid, dp_tiles;
-    long long flag_words;      // flags plus the error word
-    size_t partials_offset;    // byte offset of the partial slots (kind 2)
+    long long flag_words;      // flags (tile counts for kind 3) plus the error word
+    size_t partials_offset;    // byte offset of the partial slots (kinds 2 and 3)
     size_t bytes;              // workspace bytes needed
+    int tail_parts;            // S (kind 3)
+    long long tail_tiles;      // R (kind 3)
 };
 constexpr long long kMinItersPerCta = 8;  // K tiles per CTA below which splitting stops paying
 
 // Chooses the schedule for T output tiles of KT K tiles each, with G CTAs
-// resident at once on `sms` multiprocessors.  Cost model, fitted to GB300
-// timings of 340..1024-tile products (K = 4096): one CTA per tile takes
-// floor(T/G) full rounds plus, for a last partial wave, 0.55 of a round when
-// it has at most one CTA per SM (a lone CTA runs faster) or a full round
-// otherwise; the split schedule takes T/G rounds plus about 4.5 %.  It is
-// chosen only when it is at least 3 % better.  With fewer tiles than
-// resident CTAs the multi-part split is used when it adds more than 10 % CTAs.
-Plan plan_schedule(long long T, long long KT, long long G, long long sms) {
-    Plan pl = {0, T, 0, 0, 0, 0};
+// resident at once on `sms` multiprocessors.
+//   More tiles than resident CTAs, with a partial last wave (R = T mod G):
+//   with `allow_tail`, kind 3.  Measured on GB300 for 2500x2100x4096 ..
+//   8192^3 it beat one CTA per tile everywhere (+0.7 % .. +5.5 %).  S = 4
+//   parts when R <= sms, else min(8, 4G/R): within about 1 % of the best S
+//   at every shape measured, and the partial-sum slots stay below 4G tiles.
+//   Without it, the cost model fitted to timings of 340..1024-tile products:
+//   one CTA per tile takes floor(T/G) full rounds plus, for a last partial
+//   wave, 0.55 of a round when it has at most one CTA per SM (a lone CTA runs
+//   faster) or a full round otherwise; the split schedule takes T/G rounds
+//   plus about 4.5 %, and is chosen only when it is at least 3 % better.
+//   Fewer tiles than resident CTAs: the multi-part split is used when it
+//   adds more than 10 % CTAs.
+Plan plan_schedule(long long T, long long KT, long long G, long long sms, bool allow_tail) {
+    Plan pl = {0, T, 0, 0, 0, 0, 0, 0};
     if (KT <= 0 || G <= 0) return pl;
     if (T > G) {
         const long long W = T / G, R = T % G;
         if (R == 0) return pl;  // whole waves: already balanced
+        if (allow_tail && KT >= 2) {
+            long long S = R <= sms ? 4 : (4 * G / R < 4 ? 4 : (4 * G / R > 8 ? 8 : 4 * G / R));
+            if (S > KT) S = KT;
+            pl.kind = 3;
+            pl.grid = S * R;
+            pl.dp_tiles = T - R;
+            pl.tail_parts = static_cast<int>(S);
+            pl.tail_tiles = R;
+            pl.flag_words = R;
+            pl.partials_offset = (static_cast<size_t>(R) * sizeof(unsigned) + 255) / 256 * 256;
+            pl.bytes = pl.partials_offset + static_cast<size_t>(S * R) * BM * BN * sizeof(float);
+            return pl;
+        }
         const double dp_rounds = static_cast<double>(W) + (R <= sms ? 0.55 : 1.0);
         const double sk_rounds = static_cast<double>(T) / static_cast<double>(G) * 1.045;
         if (sk_rounds > 0.97 * dp_rounds) return pl;
@@ -707,6 +785,18 @@ Plan plan_schedule(long long T, long long KT, long long G, long long sms) {
     return pl;
 }
 
+// Kernel variant for these operands: copy widths by alignment class, and
+// the tensor-copy variant when both are 16-byte aligned and the tensor maps
+// encode (then filled into `maps`).
+int choose_variant(int M, int N, int K, const float *A, int lda, const float *B, int ldb, Maps &maps) {
+    const int va = K > 0 ? (vector_class(A, lda) == 4 ? 4 : 1) : 4;
+    const int vb = K > 0 ? vector_class(B, ldb) : 4;
+    int v = (va == 4 ? 0 : 3) + (vb == 4 ? 0 : vb == 2 ? 1 : 2);
+    memset(&maps, 0, sizeof maps);
+    if (v == 0 && K > 0 && encode_maps(maps, M, N, K, A, lda, B, ldb)) v = kTmaVariant;
+    return v;
+}
+
 // Runs one product whose arguments passed check_args (M, N > 0).  Uses a
 // stream-K schedule when the workspace `flags` (flag_bytes long) is large
 // enough for the plan chosen for this shape; else one CTA per tile.
@@ -721,12 +811,8 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     const int st = setup_device(dev, &info);
     if (st != SGEMM_OK) return st;
 
-    const int va = K > 0 ? (vector_class(A, lda) == 4 ? 4 : 1) : 4;
-    const int vb = K > 0 ? vector_class(B, ldb) : 4;
-    int v = (va == 4 ? 0 : 3) + (vb == 4 ? 0 : vb == 2 ? 1 : 2);
     Maps maps;
-    memset(&maps, 0, sizeof maps);
-    if (v == 0 && K > 0 && encode_maps(maps, M, N, K, A, lda, B, ldb)) v = kTmaVariant;
+    const int v = choose_variant(M, N, K, A, lda, B, ldb, maps);
     Problem p;
     p.M = M; p.N = N; p.K = K; p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
     p.tiles_m = (M + BM - 1) / BM;
@@ -734,12 +820,42 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     p.vc = vector_class(C, ldc);
     const long long T = static_cast<long long>(p.tiles_m) * p.tiles_n;
     const long long G = static_cast<long long>(info.sk_per_sm[v]) * info.sms;
-    const Plan pl = plan_schedule(T, (K + BK - 1) / BK, G, info.sms);
+    const long long KT = (K + BK - 1) / BK;
+    Plan pl = plan_schedule(T, KT, G, info.sms, v == kTmaVariant);
 
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
+    if (pl.kind == 3) {
+        if (flags != nullptr && flag_bytes >= pl.bytes) {
+            unsigned *counts = flags;
+            float *slots = reinterpret_cast<float *>(reinterpret_cast<char *>(flags) + pl.partials_offset);
+            if (cudaMemsetAsync(counts, 0, static_cast<size_t>(pl.flag_words) * sizeof(unsigned), stream) !=
+                cudaSuccess) {
+                (void)cudaGetLastError();
+                return SGEMM_ERR_LAUNCH;
+            }
+            cfg.gridDim = dim3(static_cast<unsigned>(pl.dp_tiles));
+            if (cudaLaunchKernelEx(&cfg, kDp[v], p, maps) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return SGEMM_ERR_LAUNCH;
+            }
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr.val.programmaticStreamSerializationAllowed = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            if (cudaLaunchKernelEx(&cfg, kTail, p, maps, static_cast<int>(pl.dp_tiles), pl.tail_parts, counts,
+                                   slots) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return SGEMM_ERR_LAUNCH;
+            }
+            return SGEMM_OK;
+        }
+        pl = plan_schedule(T, KT, G, info.sms, false);  // workspace too small for the split tail
+    }
     cudaError_t err = cudaErrorUnknown;
     bool done = false;
     if (flags != nullptr && pl.kind != 0 && flag_bytes >= pl.bytes) {
@@ -829,12 +945,39 @@ extern "C" size_t sgemm_f32_workspace_size(int M, int N, int K) {
     if (cudaGetDevice(&dev) == cudaSuccess && setup_device(dev, &info) == SGEMM_OK) {
         int per_sm = 0;
         for (int v = 0; v < kVariants; ++v) per_sm = info.sk_per_sm[v] > per_sm ? info.sk_per_sm[v] : per_sm;
-        const Plan pl = plan_schedule(T, (K + BK - 1) / BK, static_cast<long long>(per_sm) * info.sms, info.sms);
-        if (pl.bytes > bytes) bytes = pl.bytes;
+        for (const bool tail : {true, false}) {
+            const Plan pl = plan_schedule(T, (K + BK - 1) / BK, static_cast<long long>(per_sm) * info.sms, info.sms, tail);
+            if (pl.bytes > bytes) bytes = pl.bytes;
+        }
     } else {
         (void)cudaGetLastError();
     }
     return (bytes + 255) / 256 * 256;
+}
+
+extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int lda, const float *B, int ldb,
+                                     const float *C, int ldc, int *kind, long long *words) {
+    if (kind == nullptr || words == nullptr) return SGEMM_ERR_NULL_PTR;
+    *kind = 0;
+    *words = 0;
+    const int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    int dev = 0;
+    DeviceInfo info;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_DEVICE;
+    }
+    const int sd = setup_device(dev, &info);
+    if (sd != SGEMM_OK) return sd;
+    Maps maps;
+    const int v = choose_variant(M, N, K, A, lda, B, ldb, maps);
+    const long long T = tile_count(M, N);
+    const Plan pl = plan_schedule(T, (K + BK - 1) / BK, static_cast<long long>(info.sk_per_sm[v]) * info.sms,
+                                  info.sms, v == kTmaVariant);
+    *kind = pl.kind;
+    *words = pl.flag_words;
+    return SGEMM_OK;
 }
 
 extern "C" int sgemm_f32_ws(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C,

@@ -81,25 +81,31 @@ int sgemm_f32(int M, int N, int K,
  *   workspace_bytes : its size; sgemm_f32_workspace_size(M, N, K) is enough.
  *
  * When the workspace is large enough, the call balances the work over the
- * CTAs the GPU holds at once (2 per SM) with a persistent "stream-K"
- * schedule: every CTA gets the same number of 16-deep K slices, and a 128 x
- * 128 output tile cut between CTAs is summed in a fixed order, so results are
- * deterministic.  Two cases use it:
- *   - more tiles than resident CTAs, not a whole number of waves: the last
- *     wave and a bit are split, with partial sums handed over through C (the
- *     workspace holds one flag per tile plus an error word);
- *   - fewer tiles than resident CTAs: every tile is split into several K
- *     parts (at least 8 K slices per CTA), with partial sums handed over
- *     through 64 KiB slots in the workspace (one flag and one slot per CTA).
- * Otherwise, or with a smaller workspace, it runs exactly as sgemm_f32.
+ * CTAs the GPU holds at once (G = 2 per SM).  Every output tile (128 x 128)
+ * cut into K parts is summed in a fixed order, so results are deterministic.
+ * The schedules (sgemm_f32_ws_schedule reports which one a call uses):
+ *   1  more tiles than G, not a whole number of waves, rows not 16-byte
+ *      aligned: a persistent grid splits the last wave and a bit, with partial
+ *      sums handed over through C (the workspace holds one flag per tile plus
+ *      an error word);
+ *   2  fewer tiles than G: a persistent grid splits every tile into several K
+ *      parts (at least 8 K slices per CTA), with partial sums handed over
+ *      through 64 KiB slots in the workspace (one flag and one slot per CTA,
+ *      plus an error word);
+ *   3  more tiles than G, not a whole number of waves, rows 16-byte aligned:
+ *      one CTA per tile for the whole waves, and the R = T mod G leftover
+ *      tiles cut into S K parts each (S = 4 to 8) in a second grid that starts
+ *      as SMs free up; the part that finishes a tile last adds all parts
+ *      (one count per leftover tile, then S * R slots of 64 KiB).
+ *   0  otherwise, or with a smaller workspace: exactly as sgemm_f32.
  * sgemm_f32_workspace_size reports the bytes for the current device.  The
- * call zero-fills the flag words it uses at the start of the workspace on
- * `stream` before the kernel, so the workspace needs no preparation and its
+ * call zero-fills the words it uses at the start of the workspace on
+ * `stream` before the kernels, so the workspace needs no preparation and its
  * contents are not preserved; calls that share one workspace must not overlap
- * in time.  After the call completes, the 32-bit word following the flags
- * (word ceil(M/128) * ceil(N/128) in the first case, word G in the second,
- * G = number of CTAs) is nonzero only if a CTA gave up waiting for a partner
- * (about a second; the result is then wrong, nothing hangs).
+ * in time.  After a successful call those words are zero again.  In
+ * schedules 1 and 2 the last of them is an error word, nonzero only if a CTA
+ * gave up waiting for a partner (about a second; the result is then wrong,
+ * nothing hangs); in schedule 3 no CTA waits for another.
  * Other argument checks and errors are those of sgemm_f32, plus
  * SGEMM_ERR_ALIAS for a workspace overlapping A, B or C and
  * SGEMM_ERR_INVALID_ARG for a misaligned workspace.
@@ -110,6 +116,18 @@ int sgemm_f32_ws(int M, int N, int K,
                  float *C, int ldc,
                  void *workspace, size_t workspace_bytes,
                  cudaStream_t stream);
+
+/* The schedule sgemm_f32_ws would use for these arguments on the current
+ * device with a large enough workspace (host-only; launches nothing):
+ * *kind (0 to 3, as listed above) and *words, the 32-bit words at the start
+ * of the workspace that the call zero-fills and leaves zero on success (flags
+ * and error word, or tile counts).  Returns the argument-check status of
+ * sgemm_f32_ws, or SGEMM_ERR_DEVICE without a usable device. */
+int sgemm_f32_ws_schedule(int M, int N, int K,
+                          const float *A, int lda,
+                          const float *B, int ldb,
+                          const float *C, int ldc,
+                          int *kind, long long *words);
 
 /* Workspace bytes sgemm_f32_ws can use for this shape on the current device
  * (0 for an empty or invalid shape).  Reads device attributes only; with no

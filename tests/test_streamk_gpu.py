@@ -1,8 +1,9 @@
-"""sgemm_f32_ws (stream-K schedule) vs the FP64 oracle and vs sgemm_f32 (needs a GB300).
+"""sgemm_f32_ws (balanced schedules) vs the FP64 oracle and vs sgemm_f32 (needs a GB300).
 
 Shapes have more 128 x 128 output tiles than the GPU holds CTAs at once (2 per
-SM) and a count that does not divide evenly, so tiles are cut between two
-CTAs and summed through the workspace fix-up.
+SM) and a count that does not divide evenly, so tiles are cut into K parts:
+between two CTAs through C (schedule 1, rows not 16-byte aligned) or into 4 to
+8 parts of a split tail (schedule 3, aligned rows).
 """
 import numpy as np
 import pytest
@@ -37,13 +38,17 @@ def _run_ws(M, N, K, A, lda, B, ldb, ldc, a_off=0, b_off=0, c_off=0, ws_fill=0):
     tC = torch.full((c_elems + c_off + 4,), float("nan"), device="cuda")
     nbytes = sg.workspace_size(M, N, K)
     ws = torch.full((nbytes // 4,), ws_fill, dtype=torch.int32, device="cuda")
-    st = sg.sgemm_f32_ws(M, N, K, pA, lda, pB, ldb, tC.data_ptr() + 4 * c_off, ldc, ws.data_ptr(), nbytes,
+    pC = tC.data_ptr() + 4 * c_off
+    sst, kind, words = sg.ws_schedule(M, N, K, pA, lda, pB, ldb, pC, ldc)
+    assert sst == 0 and 0 < words <= nbytes // 4
+    st = sg.sgemm_f32_ws(M, N, K, pA, lda, pB, ldb, pC, ldc, ws.data_ptr(), nbytes,
                          torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     raw = tC.cpu().numpy()[c_off:c_off + c_elems]
     C = np.stack([raw[i * ldc:i * ldc + N] for i in range(M)])
-    # the call zero-fills and uses the first tiles + 1 words (flags, error word)
-    return st, C, ws.cpu().numpy()[:_tiles(M, N) + 1]
+    # the call zero-fills the first `words` words (flags and error word, or
+    # tile counts) and leaves them zero
+    return st, C, ws.cpu().numpy()[:words], kind
 
 
 @pytest.mark.parametrize("M,N,K,kind", [(2500, 2100, 333, "uniform"), (2432, 2560, 300, "normal"),
@@ -52,9 +57,10 @@ def test_streamk_full_check(oracle_lib, M, N, K, kind):
     assert _tiles(M, N) > 2 * torch.cuda.get_device_properties(0).multi_processor_count
     A = synth.matrix(M, K, 17, 0, kind)
     B = synth.matrix(K, N, 17, 1, kind)
-    st, C, ws = _run_ws(M, N, K, A, K, B, N, N, ws_fill=7)
+    st, C, ws, kind = _run_ws(M, N, K, A, K, B, N, N, ws_fill=7)
     assert st == 0
-    assert not ws.any(), "flags and error word must be zero after a successful call"
+    assert kind == (3 if K % 4 == 0 and N % 4 == 0 else 1)
+    assert not ws.any(), "flags and error word (or tile counts) must be zero after a successful call"
     Cr, Sr = oracle_lib.gemm(A, B)
     tol.assert_close(C, Cr, Sr, K, f"stream-K {M}x{N}x{K}")
 
@@ -64,8 +70,8 @@ def test_streamk_misaligned_strides_and_offsets(oracle_lib):
     lda, ldb, ldc = 259, 2335, 2337
     A = synth.matrix(M, K, 23, 0, ld=lda, pad_value=np.nan)
     B = synth.matrix(K, N, 23, 1, ld=ldb, pad_value=np.nan)
-    st, C, ws = _run_ws(M, N, K, A, lda, B, ldb, ldc, a_off=1, b_off=3, c_off=2)
-    assert st == 0 and not ws.any()
+    st, C, ws, kind = _run_ws(M, N, K, A, lda, B, ldb, ldc, a_off=1, b_off=3, c_off=2)
+    assert st == 0 and kind == 1 and not ws.any()
     Cr, Sr = oracle_lib.gemm(A, B, M=M, N=N, K=K, lda=lda, ldb=ldb)
     tol.assert_close(C, Cr, Sr, K, "stream-K misaligned")
 
@@ -74,8 +80,8 @@ def test_streamk_integer_inputs_exact_and_equal_to_data_parallel(oracle_lib):
     M, N, K = 2500, 2100, 1000
     A = synth.matrix(M, K, 29, 0, "int5")
     B = synth.matrix(K, N, 29, 1, "int5")
-    st, C, _ = _run_ws(M, N, K, A, K, B, N, N)
-    assert st == 0
+    st, C, _, kind = _run_ws(M, N, K, A, K, B, N, N)
+    assert st == 0 and kind == 3
     Cr, _ = oracle_lib.gemm(A, B)
     np.testing.assert_array_equal(C.astype(np.float64), Cr)
     from tests._gpu import run
@@ -98,20 +104,44 @@ def test_streamk_deterministic_4096():
 
 
 def test_words_past_the_used_ones_are_untouched():
-    M, N, K = 2500, 2100, 40
+    """Schedule 1 (rows not 16-byte aligned) uses only its flag words."""
+    M, N, K = 2500, 2100, 41
     A = synth.matrix(M, K, 37, 0)
     B = synth.matrix(K, N, 37, 1)
     from tests._gpu import dev_buffer
     tA, pA = dev_buffer(A)
     tB, pB = dev_buffer(B)
     C = torch.empty(M, N, device="cuda")
+    sst, kind, used = sg.ws_schedule(M, N, K, pA, K, pB, N, C.data_ptr(), N)
+    assert sst == 0 and kind == 1 and used == _tiles(M, N) + 1
     nbytes = sg.workspace_size(M, N, K)
     ws = torch.full((nbytes // 4 + 8,), 7, dtype=torch.int32, device="cuda")
     st = sg.sgemm_f32_ws(M, N, K, pA, K, pB, N, C.data_ptr(), N, ws.data_ptr(), nbytes,
                          torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
-    used = _tiles(M, N) + 1
     assert st == 0 and not ws[:used].any() and torch.all(ws[used:] == 7)
+
+
+@pytest.mark.parametrize("extra_rows,extra_cols,K", [(0, 23, 512), (5, 0, 1024)])
+def test_split_tail_parts(oracle_lib, extra_rows, extra_cols, K):
+    """Schedule 3 with more leftover tiles than SMs (fewer than 8 parts each)
+    and with a handful of leftover tiles (4 parts): full check against the
+    oracle, deterministic, tile counts left zero."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # one whole wave of 2 * sms tiles plus the leftover: rows of 128 x (cols) tiles
+    cols = 20 + extra_cols
+    rows = (2 * sms + (sms + 4 if extra_cols else 5)) // cols + 1 + extra_rows
+    M, N = 128 * rows - 37, 128 * cols
+    T = _tiles(M, N)
+    assert T > 2 * sms and T % (2 * sms) != 0
+    A = synth.matrix(M, K, 53, 0, "normal")
+    B = synth.matrix(K, N, 53, 1, "normal")
+    st, C, ws, kind = _run_ws(M, N, K, A, K, B, N, N, ws_fill=9)
+    assert st == 0 and kind == 3 and not ws.any()
+    Cr, Sr = oracle_lib.gemm(A, B)
+    tol.assert_close(C, Cr, Sr, K, f"split tail {M}x{N}x{K}")
+    st2, C2, _, _ = _run_ws(M, N, K, A, K, B, N, N)
+    assert st2 == 0 and np.array_equal(C, C2)
 
 
 def test_small_workspace_falls_back_to_one_cta_per_tile(oracle_lib):
