@@ -122,16 +122,17 @@ def test_words_past_the_used_ones_are_untouched():
     assert st == 0 and not ws[:used].any() and torch.all(ws[used:] == 7)
 
 
-@pytest.mark.parametrize("extra_rows,extra_cols,K", [(0, 23, 512), (5, 0, 1024)])
-def test_split_tail_parts(oracle_lib, extra_rows, extra_cols, K):
+@pytest.mark.parametrize("extra_rows,extra_cols,K,n_cut", [(0, 23, 512, 0), (5, 0, 1024, 0), (5, 0, 1024, 12)])
+def test_split_tail_parts(oracle_lib, extra_rows, extra_cols, K, n_cut):
     """Schedule 3 with more leftover tiles than SMs (fewer than 8 parts each)
-    and with a handful of leftover tiles (4 parts): full check against the
-    oracle, deterministic, tile counts left zero."""
+    and with a handful of leftover tiles (4 parts), ragged last tile row and
+    column: full check against the oracle, deterministic, tile counts left
+    zero."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     # one whole wave of 2 * sms tiles plus the leftover: rows of 128 x (cols) tiles
     cols = 20 + extra_cols
     rows = (2 * sms + (sms + 4 if extra_cols else 5)) // cols + 1 + extra_rows
-    M, N = 128 * rows - 37, 128 * cols
+    M, N = 128 * rows - 37, 128 * cols - n_cut  # ragged last tile row; n_cut keeps rows 16-byte aligned
     T = _tiles(M, N)
     assert T > 2 * sms and T % (2 * sms) != 0
     A = synth.matrix(M, K, 53, 0, "normal")
