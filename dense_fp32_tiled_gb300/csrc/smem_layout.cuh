@@ -38,7 +38,7 @@ constexpr int BM = 128;          // CTA tile rows (M)
 constexpr int BN = 128;          // CTA tile cols (N)
 constexpr int BK = 16;           // K depth of one pipeline stage
 constexpr int NT = 256;          // threads per CTA (8 warps)
-constexpr int STAGES = 4;        // copy ring depth (tiles in flight: STAGES - 1)
+constexpr int STAGES = 3;        // copy ring depth (tiles in flight: STAGES - 1)
 constexpr int TM = 8;            // per-thread register tile rows
 constexpr int TN = 8;            // per-thread register tile cols
 constexpr int WARPS_M = 4;       // warp grid over the CTA tile
