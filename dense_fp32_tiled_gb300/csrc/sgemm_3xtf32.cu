@@ -52,6 +52,9 @@ __global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ A,
                                                     float *__restrict__ a_lo, float *__restrict__ bt_hi,
                                                     float *__restrict__ bt_lo, int a_blocks, int b_tiles_k) {
     __shared__ float tile[ST * ST_STRIDE];
+    // the MMA grid queued behind this one may start its set-up now; it waits
+    // for this grid to complete before its first copy of split data
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int tx = threadIdx.x, ty = threadIdx.y;
     if (static_cast<int>(blockIdx.x) < a_blocks) {
         // 8 rows of A per block, the whole padded K range
@@ -367,6 +370,9 @@ sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, 
 
     if (warp == COPY_WARP) {
         if (lane == 0) {
+            // the split operands come from the grid this one may overlap: wait for it (a no-op
+            // when launched without a programmatic dependency)
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
             const uint32_t full0 = peer_addr(smem_u32(&full_bar[0]), 0);  // CTA 0 counts both CTAs' bytes
             uint32_t it = 0;                                               // K tiles issued so far
             SegIter seg(pair, pl);
@@ -707,6 +713,10 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, co
     const int b_tiles_k = (Kp + ST - 1) / ST, b_tiles_n = (N + ST - 1) / ST;
     const long long split_blocks = static_cast<long long>(a_blocks) + static_cast<long long>(b_tiles_k) * b_tiles_n;
     if (split_blocks > INT_MAX) return SGEMM_ERR_INVALID_DIM;
+    if (cudaMemsetAsync(counts, 0, static_cast<size_t>(2 * T) * sizeof(unsigned), stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
     split_kernel<<<static_cast<unsigned>(split_blocks), dim3(32, 8), 0, stream>>>(
         A, lda, B, ldb, M, N, K, Kp, a_hi, a_lo, bt_hi, bt_lo, a_blocks, b_tiles_k);
     if (cudaPeekAtLastError() != cudaSuccess) {
@@ -746,14 +756,22 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, co
         pl.Psk = static_cast<int>(psk);
         pl.U = static_cast<int>(sk_units);
     }
-    if (cudaMemsetAsync(counts, 0, static_cast<size_t>(2 * T) * sizeof(unsigned), stream) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return SGEMM_ERR_LAUNCH;
-    }
     const int vc = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0) ? 4 : 1;
-    sgemm_3xtf32_kernel<<<static_cast<unsigned>(2 * pl.P), TC_THREADS, MMA_SMEM, stream>>>(
-        maps, C, ldc, M, N, pl, counts, partials, vc, timeout);
-    if (cudaPeekAtLastError() != cudaSuccess) {
+    // programmatic dependent launch: the MMA grid's CTAs may start (barriers,
+    // tensor-memory allocation) as the split grid drains
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pl.P));
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = MMA_SMEM;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel, maps, C, ldc, M, N, pl, counts, partials, vc, timeout) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
     }
