@@ -730,7 +730,11 @@ struct Plan {
     int tail_parts;            // S (kind 3)
     long long tail_tiles;      // R (kind 3)
 };
-constexpr long long kMinItersPerCta = 8;  // K tiles per CTA below which splitting stops paying
+// K tiles per CTA below which splitting stops paying.  Measured on GB300
+// (stream-K kernel, fewer tiles than resident CTAs): 4 beats 8 at 256^3
+// (22.5 -> 18.5 us) and 512^3 (24.6 -> 22.5 us); 2 is slower at 512^3
+// (32.5 us), where the owner's serial fix-up of more parts dominates.
+constexpr long long kMinItersPerCta = 4;
 
 // Chooses the schedule for T output tiles of KT K tiles each, with G CTAs
 // resident at once on `sms` multiprocessors.

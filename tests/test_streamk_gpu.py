@@ -160,14 +160,16 @@ def test_small_workspace_falls_back_to_one_cta_per_tile(oracle_lib):
     tol.assert_close(C.cpu().numpy(), Cr, Sr, K, "fallback")
 
 
-def _plan_words(M, N, K):
-    """Flag words (with the error word) the multi-part schedule uses for a
-    shape with fewer tiles than resident CTAs, or None if it is not used."""
-    T = _tiles(M, N)
-    G = 2 * torch.cuda.get_device_properties(0).multi_processor_count
-    KT = (K + 15) // 16
-    g = min(G, T * KT // 8)
-    return g + 1 if T <= G and g > 1.1 * T else None
+def _plan_words(M, N, K, pA, lda, pB, ldb, pC, ldc):
+    """Flag words (with the error word) of the multi-part schedule (kind 2,
+    fewer tiles than resident CTAs) the library plans for these operands, or
+    None if it plans another schedule."""
+    sst, kind, words = sg.ws_schedule(M, N, K, pA, lda, pB, ldb, pC, ldc)
+    assert sst == 0
+    if kind != 2:
+        return None
+    assert words > _tiles(M, N) + 1, "more parts than tiles"
+    return words
 
 
 @pytest.mark.parametrize("M,N,K,lds,kind", [
@@ -178,8 +180,6 @@ def _plan_words(M, N, K):
 ])
 def test_multipart_split_full_check(oracle_lib, M, N, K, lds, kind):
     lda, ldb, ldc = lds or (K, N, N)
-    words = _plan_words(M, N, K)
-    assert words is not None, "shape must use the multi-part schedule"
     A = synth.matrix(M, K, 43, 0, kind, ld=lda)
     B = synth.matrix(K, N, 43, 1, kind, ld=ldb)
     from tests._gpu import dev_buffer
@@ -187,6 +187,8 @@ def test_multipart_split_full_check(oracle_lib, M, N, K, lds, kind):
     tB, pB = dev_buffer(B)
     c_elems = (M - 1) * ldc + N
     tC = torch.full((c_elems + 4,), float("nan"), device="cuda")
+    words = _plan_words(M, N, K, pA, lda, pB, ldb, tC.data_ptr(), ldc)
+    assert words is not None, "shape must use the multi-part schedule"
     nbytes = sg.workspace_size(M, N, K)
     assert nbytes >= words * 4 + (words - 1) * 128 * 128 * 4
     ws = torch.full((nbytes // 4,), 5, dtype=torch.int32, device="cuda")
@@ -203,10 +205,11 @@ def test_multipart_split_full_check(oracle_lib, M, N, K, lds, kind):
 
 def test_multipart_integer_exact_and_deterministic(oracle_lib):
     M, N, K = 1024, 768, 2048
-    assert _plan_words(M, N, K) is not None
     A = synth.matrix(M, K, 47, 0, "int5")
     B = synth.matrix(K, N, 47, 1, "int5")
     tA, tB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    probe = torch.empty(M, N, device="cuda")
+    assert _plan_words(M, N, K, tA.data_ptr(), K, tB.data_ptr(), N, probe.data_ptr(), N) is not None
     C1 = sg.sgemm(tA, tB)
     C2 = sg.sgemm(tA, tB)
     torch.cuda.synchronize()
