@@ -1,13 +1,20 @@
 // sgemm_host.cu -- the FP32 product for operands that live in host memory.
 //
 // The product itself is sgemm_f32_ws (the tiled CUDA-core kernel).  This
-// file adds the transfers around it.  B is copied to the device first, since
-// every row of C needs all of B.  A is then copied in row panels on a copy
+// file adds the transfers around it.  A is copied in row panels on a copy
 // stream, and the product of each panel starts, on the caller's stream, as
-// soon as that panel has landed.  Each finished panel of C is copied back on
-// a second copy stream while the next panel computes.  Host memory should be
-// pinned (page-locked) for the copies to run asynchronously at full speed;
-// pageable memory works, but the CUDA runtime then stages it.
+// soon as that panel and B have landed.  Each finished panel of C is copied
+// back on a second copy stream while the next panel computes.
+//
+// Every row of C needs all of B, so B's copy would otherwise stall the first
+// product.  When there are several panels and N >= 512, the first panel's
+// product is cut into two column halves instead: the copy order is A's first
+// panel, B's left columns, B's right columns, then A's other panels, and the
+// left half computes while B's right columns are still in flight.
+//
+// Host memory should be pinned (page-locked) for the copies to run
+// asynchronously at full speed; pageable memory works, but the CUDA runtime
+// then stages it.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -32,6 +39,10 @@ void panels_of(int M, int &P, int &rows) {
     P = (M + rows - 1) / rows;
 }
 
+// Columns of the first panel's left half (a multiple of the 128-column tile),
+// or N when the first panel is not split.
+int first_split(int P, int N) { return P >= 2 && N >= 512 ? (N / 2) / 128 * 128 : N; }
+
 struct HostLayout {
     size_t b, a, c, ws, ws_bytes, bytes;
 };
@@ -43,10 +54,17 @@ HostLayout host_layout(int M, int N, int K) {
     l.a = round256(static_cast<size_t>(K) * N * 4);
     l.c = l.a + round256(static_cast<size_t>(M) * K * 4);
     l.ws = l.c + round256(static_cast<size_t>(M) * N * 4);
+    // the products run one after another on one stream, so they share one
+    // workspace sized for the largest need among the shapes they take
+    const int first = rows < M ? rows : M;
     const int last = M - (P - 1) * rows;  // the last panel's rows (its schedule may differ)
-    const size_t w_full = sgemm_f32_workspace_size(rows < M ? rows : M, N, K);
-    const size_t w_last = sgemm_f32_workspace_size(last, N, K);
-    l.ws_bytes = round256(w_full > w_last ? w_full : w_last);
+    const int n1 = first_split(P, N);
+    const size_t need[4] = {sgemm_f32_workspace_size(first, N, K), sgemm_f32_workspace_size(last, N, K),
+                            sgemm_f32_workspace_size(first, n1, K),
+                            n1 < N ? sgemm_f32_workspace_size(first, N - n1, K) : 0};
+    size_t w = 0;
+    for (size_t x : need) w = x > w ? x : w;
+    l.ws_bytes = round256(w);
     l.bytes = l.ws + l.ws_bytes;
     return l;
 }
@@ -120,10 +138,12 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     void *dW = ws + l.ws;
     int P = 0, rows = 0;
     panels_of(M, P, rows);
+    const int n1 = first_split(P, N);
 
-    // events: start, B landed, A panel p landed, C panel p computed, all copied back
-    cudaEvent_t ev[3 + 2 * kMaxPanels] = {};
-    const int n_ev = 3 + 2 * P;
+    // events: start, B's left columns landed, all of B landed, all copied
+    // back, A panel p landed, C panel p computed
+    cudaEvent_t ev[4 + 2 * kMaxPanels] = {};
+    const int n_ev = 4 + 2 * P;
     for (int i = 0; i < n_ev; ++i) {
         if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -131,36 +151,56 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
             return SGEMM_ERR_DEVICE;
         }
     }
-    cudaEvent_t &e_start = ev[0], &e_b = ev[1], &e_done = ev[2];
-    cudaEvent_t *e_a = ev + 3, *e_c = ev + 3 + P;
+    cudaEvent_t &e_start = ev[0], &e_bl = ev[1], &e_b = ev[2], &e_done = ev[3];
+    cudaEvent_t *e_a = ev + 4, *e_c = ev + 4 + P;
 
     auto fail = [&](int code) {
         (void)cudaGetLastError();
         for (int i = 0; i < n_ev; ++i) (void)cudaEventDestroy(ev[i]);
         return code;
     };
+    // columns [c0, c0 + nc) of B, all K rows
+    auto copy_b = [&](int c0, int nc) {
+        return K == 0 || cudaMemcpy2DAsync(dB + c0, static_cast<size_t>(N) * 4, B + c0, static_cast<size_t>(ldb) * 4,
+                                           static_cast<size_t>(nc) * 4, K, cudaMemcpyHostToDevice, h2d) == cudaSuccess;
+    };
+    auto copy_a = [&](int p) {
+        const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
+        return (K == 0 || cudaMemcpy2DAsync(dA + static_cast<size_t>(r0) * K, static_cast<size_t>(K) * 4,
+                                            A + static_cast<size_t>(r0) * lda, static_cast<size_t>(lda) * 4,
+                                            static_cast<size_t>(K) * 4, nr, cudaMemcpyHostToDevice,
+                                            h2d) == cudaSuccess) &&
+               cudaEventRecord(e_a[p], h2d) == cudaSuccess;
+    };
+    // columns [c0, c0 + nc) of panel p's product
+    auto product = [&](int p, int c0, int nc) {
+        const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
+        return sgemm_f32_ws(nr, nc, K, dA + static_cast<size_t>(r0) * K, K > 0 ? K : 1, dB + c0, N,
+                            dC + static_cast<size_t>(r0) * N + c0, N, dW, l.ws_bytes, stream);
+    };
     // the workspace may still be in use by work queued earlier on `stream`
     if (cudaEventRecord(e_start, stream) != cudaSuccess || cudaStreamWaitEvent(h2d, e_start, 0) != cudaSuccess ||
         cudaStreamWaitEvent(d2h, e_start, 0) != cudaSuccess)
         return fail(SGEMM_ERR_LAUNCH);
-    if (K > 0 && cudaMemcpy2DAsync(dB, static_cast<size_t>(N) * 4, B, static_cast<size_t>(ldb) * 4,
-                                   static_cast<size_t>(N) * 4, K, cudaMemcpyHostToDevice, h2d) != cudaSuccess)
+    // copy order: A panel 0, B's left columns, the rest of B, A panels 1..
+    if (!copy_a(0) || !copy_b(0, n1) || cudaEventRecord(e_bl, h2d) != cudaSuccess || (n1 < N && !copy_b(n1, N - n1)) ||
+        cudaEventRecord(e_b, h2d) != cudaSuccess)
         return fail(SGEMM_ERR_LAUNCH);
-    if (cudaEventRecord(e_b, h2d) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
-    for (int p = 0; p < P; ++p) {
-        const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
-        if (K > 0 && cudaMemcpy2DAsync(dA + static_cast<size_t>(r0) * K, static_cast<size_t>(K) * 4,
-                                       A + static_cast<size_t>(r0) * lda, static_cast<size_t>(lda) * 4,
-                                       static_cast<size_t>(K) * 4, nr, cudaMemcpyHostToDevice, h2d) != cudaSuccess)
-            return fail(SGEMM_ERR_LAUNCH);
-        if (cudaEventRecord(e_a[p], h2d) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
-    }
-    if (cudaStreamWaitEvent(stream, e_b, 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
+    for (int p = 1; p < P; ++p)
+        if (!copy_a(p)) return fail(SGEMM_ERR_LAUNCH);
     for (int p = 0; p < P; ++p) {
         const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
         if (cudaStreamWaitEvent(stream, e_a[p], 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
-        st = sgemm_f32_ws(nr, N, K, dA + static_cast<size_t>(r0) * K, K > 0 ? K : 1, dB, N,
-                          dC + static_cast<size_t>(r0) * N, N, dW, l.ws_bytes, stream);
+        if (p == 0 && n1 < N) {  // left half while B's right columns land
+            if (cudaStreamWaitEvent(stream, e_bl, 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
+            st = product(0, 0, n1);
+            if (st != SGEMM_OK) return fail(st);
+            if (cudaStreamWaitEvent(stream, e_b, 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
+            st = product(0, n1, N - n1);
+        } else {
+            if (p == 0 && cudaStreamWaitEvent(stream, e_b, 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
+            st = product(p, 0, N);
+        }
         if (st != SGEMM_OK) return fail(st);
         if (cudaEventRecord(e_c[p], stream) != cudaSuccess || cudaStreamWaitEvent(d2h, e_c[p], 0) != cudaSuccess)
             return fail(SGEMM_ERR_LAUNCH);

@@ -137,12 +137,14 @@ size_t sgemm_f32_workspace_size(int M, int N, int K);
 /*
  * sgemm_f32_host -- the same product for operands in HOST memory: copies A
  * and B to the device, multiplies with sgemm_f32_ws, and copies C back.
- * B goes first; A goes in row panels of about 1024 rows (at most 4), and each
- * panel's product starts as soon as that panel has landed.  Each finished panel
- * of C is copied back while the next one computes.  The copies run on two
- * internal non-blocking streams (created once per device), the products on
- * `stream`.  The pages have no counterpart: this entry point is the path's
- * public interface for host-resident data.
+ * A goes in row panels of about 1024 rows (at most 4), B after the first
+ * panel, and each panel's product starts as soon as that panel and B have
+ * landed; with several panels and N >= 512 the first panel's product runs as
+ * two column halves, the left one while B's right columns are still copying.
+ * Each finished panel of C is copied back while the next one computes.  The
+ * copies run on two internal non-blocking streams (created once per device),
+ * the products on `stream`.  The pages have no counterpart: this entry point
+ * is the path's public interface for host-resident data.
  *   A, B, C, M, N, K, lda, ldb, ldc : as for sgemm_f32, but HOST pointers.
  *                     Page-locked memory gives asynchronous copies at full
  *                     speed; pageable memory works, staged by the runtime.

@@ -34,10 +34,14 @@ def test_pageable_strided_ragged(oracle_lib):
     assert torch.all(out[:, :4] == -5.0) and torch.all(out[:, 1034:] == -5.0)
 
 
-@pytest.mark.parametrize("M,N,K", [(4100, 300, 200), (2048, 512, 1024), (129, 7, 3)])
+@pytest.mark.parametrize("M,N,K", [(4100, 300, 200), (2048, 512, 1024), (129, 7, 3), (2500, 1030, 333),
+                                   (3000, 700, 64)])
 def test_pinned_integer_exact(oracle_lib, M, N, K):
     """Pinned buffers across one to four row panels; integer inputs make every
-    partial sum exact, so C must equal the oracle bit for bit."""
+    partial sum exact, so C must equal the oracle bit for bit.  With several
+    panels and N >= 512 the first panel is computed in two column halves
+    (2048x512: 256 + 256; 2500x1030: 512 + 518, rows not 16-byte aligned;
+    3000x700: 256 + 444)."""
     A = torch.from_numpy(synth.matrix(M, K, 93, 0, "int5")).pin_memory()
     B = torch.from_numpy(synth.matrix(K, N, 93, 1, "int5")).pin_memory()
     C = sg.sgemm_host(A, B)
@@ -70,6 +74,10 @@ def test_empty_and_k_zero():
     A = torch.empty(5, 0)
     B = torch.empty(0, 6)
     sg.sgemm_host(A, B, out=C)
+    assert torch.all(C == 0.0)
+    # several panels, first one split in column halves, nothing to copy in
+    C = torch.full((2100, 600), 7.0).pin_memory()
+    sg.sgemm_host(torch.empty(2100, 0), torch.empty(0, 600), out=C)
     assert torch.all(C == 0.0)
     assert sg.sgemm_f32_host(0, 6, 3, 0, 3, 0, 6, 0, 6, 0, 0, 0) == 0
 
