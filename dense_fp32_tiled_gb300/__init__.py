@@ -5,15 +5,18 @@
 ``sgemm_f32(...)`` is the raw C call on device addresses.  ``sgemm_host(A, B)``
 takes CPU tensors (``sgemm_f32_host``: copies overlapped with the product).  ``transpose(x)`` /
 ``transpose_f32(...)`` run the FP32 transpose, the pages' second workload.
+``copy_timeouts()``, ``tc_timeouts()`` and ``wait_selftest(case)`` expose the
+bounded waits' failure reporting.
 """
-from ._binding import (SGEMM_OK, SgemmError, declared_functions, host_workspace_size, load_library, sgemm,
-                       sgemm_f32, sgemm_f32_3xtf32, sgemm_f32_host, sgemm_host, sgemm_f32_static_scratch, sgemm_f32_ws, sgemm_tc, smem_request,
-                       smem_shape, status_string, tc_timeouts, tc_workspace_size, transpose, transpose_f32,
-                       transpose_smem_request, transpose_status_string, workspace_size, ws_schedule)
+from ._binding import (SGEMM_OK, WAIT_SELFTESTS, SgemmError, copy_timeouts, declared_functions, host_workspace_size,
+                       load_library, sgemm, sgemm_f32, sgemm_f32_3xtf32, sgemm_f32_host, sgemm_host,
+                       sgemm_f32_static_scratch, sgemm_f32_ws, sgemm_tc, smem_request, smem_shape, status_string,
+                       tc_timeouts, tc_workspace_size, transpose, transpose_f32, transpose_smem_request,
+                       transpose_status_string, wait_selftest, workspace_size, ws_schedule)
 
-__all__ = ["SGEMM_OK", "SgemmError", "declared_functions", "host_workspace_size", "load_library", "sgemm",
-           "sgemm_f32", "sgemm_f32_3xtf32", "sgemm_f32_host", "sgemm_host",
+__all__ = ["SGEMM_OK", "WAIT_SELFTESTS", "SgemmError", "copy_timeouts", "declared_functions", "host_workspace_size",
+           "load_library", "sgemm", "sgemm_f32", "sgemm_f32_3xtf32", "sgemm_f32_host", "sgemm_host",
            "sgemm_tc", "tc_timeouts", "tc_workspace_size",
            "sgemm_f32_static_scratch", "sgemm_f32_ws", "smem_request", "smem_shape", "status_string",
-           "transpose", "transpose_f32", "transpose_smem_request", "transpose_status_string", "workspace_size",
-           "ws_schedule"]
+           "transpose", "transpose_f32", "transpose_smem_request", "transpose_status_string", "wait_selftest",
+           "workspace_size", "ws_schedule"]

@@ -48,6 +48,11 @@ def load_library():
     lib.sgemm_f32_3xtf32_workspace_size.restype = ctypes.c_size_t
     lib.sgemm_f32_3xtf32_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.sgemm_f32_3xtf32_timeouts.restype = i32
+    lib.sgemm_f32_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.sgemm_f32_timeouts.restype = i32
+    for name in ("sgemm_f32_wait_selftest", "sgemm_f32_3xtf32_wait_selftest"):
+        getattr(lib, name).argtypes = [i32, ctypes.c_uint, ctypes.POINTER(ctypes.c_uint)]
+        getattr(lib, name).restype = i32
     lib.sgemm_f32_host.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p, ctypes.c_size_t, p]
     lib.sgemm_f32_host.restype = i32
     lib.sgemm_f32_host_workspace_size.argtypes = [i32, i32, i32]
@@ -190,6 +195,31 @@ def tc_timeouts() -> int:
     if st != SGEMM_OK:
         raise SgemmError(st, "sgemm_f32_3xtf32_timeouts")
     return n.value
+
+
+def copy_timeouts() -> int:
+    """Flag of sgemm_f32_timeouts: 1 if a CUDA-core kernel gave up a copy wait."""
+    n = ctypes.c_uint()
+    st = load_library().sgemm_f32_timeouts(ctypes.byref(n))
+    if st != SGEMM_OK:
+        raise SgemmError(st, "sgemm_f32_timeouts")
+    return n.value
+
+
+WAIT_SELFTESTS = {"copy_never": ("sgemm_f32_wait_selftest", 0), "flag_never": ("sgemm_f32_wait_selftest", 1),
+                  "copy_done": ("sgemm_f32_wait_selftest", 2), "flag_done": ("sgemm_f32_wait_selftest", 3),
+                  "tc_never": ("sgemm_f32_3xtf32_wait_selftest", 0), "tc_done": ("sgemm_f32_3xtf32_wait_selftest", 1)}
+
+
+def wait_selftest(case: str, polls: int = 1000) -> bool:
+    """Runs one bounded-wait self-test (WAIT_SELFTESTS); True if the wait gave up."""
+    fn, which = WAIT_SELFTESTS[case]
+    n = ctypes.c_uint(7)
+    st = getattr(load_library(), fn)(which, int(polls), ctypes.byref(n))
+    if st != SGEMM_OK:
+        raise SgemmError(st, fn)
+    assert n.value in (0, 1)
+    return n.value == 1
 
 
 _tc_workspaces = {}

@@ -179,11 +179,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-// Bounded wait: gives up after kWaitPolls polls and records the timeout.
-__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, unsigned *timeout_flag) {
+// Bounded wait: gives up after `limit` polls and records the timeout.
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, unsigned *timeout_flag,
+                                          uint32_t limit = kWaitPolls) {
     uint32_t polls = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if (++polls > kWaitPolls) {
+        if (++polls > limit) {
             *timeout_flag = 1u;
             break;
         }
@@ -646,6 +647,25 @@ WsLayout ws_layout(int M, int N, int K, int pairs) {
 // device-side timeout word of the last call, per library instance
 __device__ unsigned g_tc_timeout;
 
+// Largest poll limit sgemm_f32_3xtf32_wait_selftest accepts.
+constexpr unsigned kSelftestMaxPolls = 1u << 16;
+
+// The pipeline's bounded mbarrier wait on a phase nothing completes (which =
+// 0: no arrival) or one already complete (1: after an arrival), with a short
+// poll limit; status[0] = 1 if the wait gave up.  One CTA of 32 threads.
+__global__ void tc_wait_selftest_kernel(int which, unsigned limit, unsigned *status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        const uint32_t b = smem_u32(&bar);
+        mbar_init(b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        if (which == 1) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(b) : "memory");
+        unsigned gave_up = 0u;
+        mbar_wait(b, 0, &gave_up, limit);
+        status[0] = gave_up;
+    }
+}
+
 }  // namespace
 
 extern "C" size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K) {
@@ -785,4 +805,33 @@ extern "C" int sgemm_f32_3xtf32_timeouts(unsigned *count) {
         return SGEMM_ERR_DEVICE;
     }
     return SGEMM_OK;
+}
+
+extern "C" int sgemm_f32_3xtf32_wait_selftest(int which, unsigned polls, unsigned *timed_out) {
+    if (timed_out == nullptr) return SGEMM_ERR_NULL_PTR;
+    if (which < 0 || which > 1 || polls == 0 || polls > kSelftestMaxPolls) return SGEMM_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_DEVICE;
+    }
+    const int st = setup(dev);
+    if (st != SGEMM_OK) return st;
+    unsigned *d = nullptr;
+    if (cudaMalloc(&d, sizeof(unsigned)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_DEVICE;
+    }
+    int rc = SGEMM_OK;
+    if (cudaMemset(d, 0, sizeof(unsigned)) != cudaSuccess) {
+        rc = SGEMM_ERR_LAUNCH;
+    } else {
+        tc_wait_selftest_kernel<<<1, 32>>>(which, polls, d);
+        if (cudaGetLastError() != cudaSuccess ||
+            cudaMemcpy(timed_out, d, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
+            rc = SGEMM_ERR_LAUNCH;
+    }
+    (void)cudaGetLastError();
+    (void)cudaFree(d);
+    return rc;
 }

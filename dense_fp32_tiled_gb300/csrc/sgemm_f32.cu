@@ -80,6 +80,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
+// Polls one mbarrier phase at most `limit` times; false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t polls = 0; !mbar_try_wait(bar, parity);)
+        if (++polls > limit) return false;
+    return true;
+}
 // 2-D tiled bulk copy global -> shared; elements outside the tensor read 0.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
     asm volatile(
@@ -92,6 +98,8 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 // Polls of one mbarrier phase before a wait is abandoned (each try_wait
 // itself blocks for a while): far beyond any copy's latency.
 constexpr uint32_t kWaitLimit = 1u << 22;
+// Largest poll limit sgemm_f32_wait_selftest accepts (keeps the test short).
+constexpr unsigned kSelftestMaxPolls = 1u << 16;
 // Set to 1 by a CTA whose copy wait ran out (the result is then wrong; the
 // kernel still finishes).  Stays set until the process exits.
 __device__ unsigned g_copy_timeout;
@@ -218,14 +226,7 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
     auto wait_tile = [&](int kt, auto pending) {
         if constexpr (TMA) {
             const uint32_t u = u0 + kt;
-            const uint32_t bar = bars + 8 * (u % STAGES);
-            uint32_t polls = 0;
-            while (!mbar_try_wait(bar, (u / STAGES) & 1u)) {
-                if (++polls > kWaitLimit) {
-                    g_copy_timeout = 1u;
-                    break;
-                }
-            }
+            if (!mbar_wait_bounded(bars + 8 * (u % STAGES), (u / STAGES) & 1u, kWaitLimit)) g_copy_timeout = 1u;
         } else {
             cp_async_wait<decltype(pending)::value>();
         }
@@ -402,12 +403,12 @@ __device__ __forceinline__ void add_partial(const float *slot, Acc &acc) {
     }
 }
 // Thread 0 waits for a flag raised by another CTA; a wait longer than
-// kSpinLimit polls sets bit 1 of *error and gives up (wrong result, no hang).
-__device__ __forceinline__ void wait_flag(const unsigned *flag, unsigned *error) {
+// `limit` polls sets bit 0 of *error and gives up (wrong result, no hang).
+__device__ __forceinline__ void wait_flag(const unsigned *flag, unsigned *error, unsigned limit = kSpinLimit) {
     if (threadIdx.x == 0) {
         unsigned spins = 0;
         while (ld_acquire(flag) == 0u) {
-            if (++spins > kSpinLimit) {
+            if (++spins > limit) {
                 atomicOr(error, 1u);
                 break;
             }
@@ -441,8 +442,8 @@ __device__ __forceinline__ void raise_flag(unsigned *flag) {
 //     slots of the following CTAs in CTA order.
 // Every hand-over comes first in its CTA's range, so no wait can form a
 // cycle, and the order of the additions is fixed: results are deterministic.
-// A wait longer than kSpinLimit polls records error bit 1 in the word after
-// the flags and stores without that part: a wrong result, never a hang.
+// A wait longer than kSpinLimit polls sets bit 0 of the word after the flags
+// and stores without that part: a wrong result, never a hang.
 template <int VA, int VB, bool TMA>
 __global__ void __launch_bounds__(NT, 2)
 sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles, unsigned *flags,
@@ -555,6 +556,30 @@ sgemm_f32_tail_kernel(const Problem p, const __grid_constant__ Maps maps, const 
         acc_zero(acc);
         for (int k = 0; k < parts; ++k) add_partial(slots + static_cast<size_t>(tile * parts + k) * (BM * BN), acc);
         store_tile<false>(p, tm * BM, tn * BN, acc);
+    }
+}
+
+// Runs one of the bounded waits above on a target that nothing completes
+// (which = 0: a copy-ring mbarrier phase with no arrival and no copy; 1: a
+// partner flag nobody raises) or on one that is already complete (2: the
+// phase after an arrival; 3: a raised flag), with a short poll limit.
+// status[0] = 1 if the wait gave up.  status[1] is the flag, status[2] the
+// error word (both zeroed by the host).  One CTA of 32 threads.
+__global__ void wait_selftest_kernel(int which, unsigned limit, unsigned *status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (which == 0 || which == 2) {
+        if (threadIdx.x == 0) {
+            const uint32_t b = smem_u32(&bar);
+            mbar_init(b, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+            if (which == 2) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(b) : "memory");
+            status[0] = mbar_wait_bounded(b, 0, limit) ? 0u : 1u;
+        }
+    } else {
+        if (which == 3 && threadIdx.x == 0) st_release(status + 1, 1u);
+        __syncthreads();
+        wait_flag(status + 1, status + 2, limit);
+        if (threadIdx.x == 0) status[0] = ld_acquire(status + 2) != 0u ? 1u : 0u;
     }
 }
 
@@ -1077,4 +1102,43 @@ extern "C" int sgemm_f32_smem_request(int kind, int warp, int step, int stage, i
     }
     if (width_bytes) *width_bytes = width;
     return SGEMM_OK;
+}
+
+extern "C" int sgemm_f32_timeouts(unsigned *count) {
+    if (count == nullptr) return SGEMM_ERR_NULL_PTR;
+    if (cudaMemcpyFromSymbol(count, g_copy_timeout, sizeof(unsigned)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_DEVICE;
+    }
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_f32_wait_selftest(int which, unsigned polls, unsigned *timed_out) {
+    if (timed_out == nullptr) return SGEMM_ERR_NULL_PTR;
+    if (which < 0 || which > 3 || polls == 0 || polls > kSelftestMaxPolls) return SGEMM_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_DEVICE;
+    }
+    DeviceInfo info;
+    const int st = setup_device(dev, &info);
+    if (st != SGEMM_OK) return st;
+    unsigned *d = nullptr;
+    if (cudaMalloc(&d, 3 * sizeof(unsigned)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_DEVICE;
+    }
+    int rc = SGEMM_OK;
+    if (cudaMemset(d, 0, 3 * sizeof(unsigned)) != cudaSuccess) {
+        rc = SGEMM_ERR_LAUNCH;
+    } else {
+        wait_selftest_kernel<<<1, 32>>>(which, polls, d);
+        if (cudaGetLastError() != cudaSuccess || cudaMemcpy(timed_out, d, sizeof(unsigned), cudaMemcpyDeviceToHost) !=
+                                                     cudaSuccess)
+            rc = SGEMM_ERR_LAUNCH;
+    }
+    (void)cudaGetLastError();
+    (void)cudaFree(d);
+    return rc;
 }

@@ -89,7 +89,7 @@ int sgemm_f32(int M, int N, int K,
  *      sums handed over through C (the workspace holds one flag per tile plus
  *      an error word);
  *   2  fewer tiles than G: a persistent grid splits every tile into several K
- *      parts (at least 8 K slices per CTA), with partial sums handed over
+ *      parts (at least 4 K slices per CTA), with partial sums handed over
  *      through 64 KiB slots in the workspace (one flag and one slot per CTA,
  *      plus an error word);
  *   3  more tiles than G, not a whole number of waves, rows 16-byte aligned:
@@ -229,7 +229,7 @@ int sgemm_f32_static_scratch(int M, int N, int K,
  * misaligned or too small workspace and SGEMM_ERR_DEVICE when no tensor map
  * can be encoded.  K == 0 writes C = 0 as sgemm_f32 does.  Every wait inside
  * the kernel is bounded: a wait that runs out (about a second) leaves C wrong
- * and increments the counter sgemm_f32_3xtf32_timeouts reports; nothing hangs.
+ * and sets the flag sgemm_f32_3xtf32_timeouts reports; nothing hangs.
  */
 int sgemm_f32_3xtf32(int M, int N, int K,
                      const float *A, int lda,
@@ -244,6 +244,29 @@ size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K);
 /* Copies into *count whether any tensor-core kernel on the current device gave
  * up a wait since the library was loaded (0 = never).  Synchronous. */
 int sgemm_f32_3xtf32_timeouts(unsigned *count);
+
+/* Copies into *count whether any CUDA-core kernel on the current device gave
+ * up waiting for a tensor copy of its ring since the library was loaded
+ * (0 = never; the product of that call is then wrong, nothing hangs).  The
+ * wait allows about a second.  Synchronous. */
+int sgemm_f32_timeouts(unsigned *count);
+
+/* Failure-detection self-tests (the pages have no counterpart).  Each runs, in
+ * a one-CTA kernel, one of the library's bounded waits with a limit of
+ * `polls` polls (1 .. 65536) and stores into *timed_out 1 if the wait gave up,
+ * else 0.  The target is either one that nothing ever completes (the wait must
+ * give up and return; the kernel exits normally and the context stays usable)
+ * or one already complete (the wait must not give up):
+ *   sgemm_f32_wait_selftest, which = 0: a copy-ring mbarrier phase with no
+ *     arrival and no copy; 1: a stream-K partner flag nobody raises;
+ *     2: the phase after an arrival; 3: a raised flag.
+ *   sgemm_f32_3xtf32_wait_selftest, which = 0: a tensor-core pipeline
+ *     mbarrier phase with no arrival; 1: the phase after an arrival.
+ * They leave the flags of sgemm_f32_timeouts and sgemm_f32_3xtf32_timeouts
+ * alone.  Synchronous (they allocate and free 12 bytes of device memory).
+ * SGEMM_ERR_INVALID_ARG for another `which` or a limit out of range. */
+int sgemm_f32_wait_selftest(int which, unsigned polls, unsigned *timed_out);
+int sgemm_f32_3xtf32_wait_selftest(int which, unsigned polls, unsigned *timed_out);
 
 /* Static English description of a status code (never NULL). */
 const char *sgemm_f32_status_string(int status);
