@@ -57,11 +57,13 @@ def load_library():
     lib.sgemm_f32_host.restype = i32
     lib.sgemm_f32_host_workspace_size.argtypes = [i32, i32, i32]
     lib.sgemm_f32_host_workspace_size.restype = ctypes.c_size_t
-    lib.sgemm_f32_ws_schedule.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, ctypes.POINTER(ctypes.c_int),
-                                          ctypes.POINTER(ctypes.c_longlong)]
+    lib.sgemm_f32_ws_schedule.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, ctypes.c_size_t,
+                                          ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_longlong)]
     lib.sgemm_f32_ws_schedule.restype = i32
     lib.sgemm_f32_workspace_size.argtypes = [i32, i32, i32]
     lib.sgemm_f32_workspace_size.restype = ctypes.c_size_t
+    lib.sgemm_f32_workspace_size_for.argtypes = [i32, i32, i32, p, i32, p, i32]
+    lib.sgemm_f32_workspace_size_for.restype = ctypes.c_size_t
     lib.sgemm_f32_status_string.argtypes = [i32]
     lib.sgemm_f32_status_string.restype = ctypes.c_char_p
     ip = ctypes.POINTER(ctypes.c_int)
@@ -251,19 +253,30 @@ def sgemm_tc(A, B, out=None, stream=None):
     return out
 
 
-def ws_schedule(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int):
-    """(status, kind, words): the schedule sgemm_f32_ws uses for these arguments
-    and the leading workspace words it zero-fills and leaves zero (host-only)."""
+def ws_schedule(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                workspace_bytes: int = None):
+    """(status, kind, words): what sgemm_f32_ws runs for these arguments with a
+    workspace of `workspace_bytes` (default: workspace_size_for these
+    operands): kind = schedule (bits 0-1) + 4 if A is repacked + 8 if B is;
+    words = the leading workspace words it zero-fills and leaves zero."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace_size_for(M, N, K, A, lda, B, ldb)
     kind, words = ctypes.c_int(), ctypes.c_longlong()
     st = load_library().sgemm_f32_ws_schedule(int(M), int(N), int(K), ctypes.c_void_p(int(A) or None), int(lda),
                                               ctypes.c_void_p(int(B) or None), int(ldb),
-                                              ctypes.c_void_p(int(C) or None), int(ldc), ctypes.byref(kind),
-                                              ctypes.byref(words))
+                                              ctypes.c_void_p(int(C) or None), int(ldc), int(workspace_bytes),
+                                              ctypes.byref(kind), ctypes.byref(words))
     return st, kind.value, words.value
 
 
 def workspace_size(M: int, N: int, K: int) -> int:
     return int(load_library().sgemm_f32_workspace_size(int(M), int(N), int(K)))
+
+
+def workspace_size_for(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int) -> int:
+    """Workspace bytes for these operands, room to repack unaligned rows included."""
+    return int(load_library().sgemm_f32_workspace_size_for(int(M), int(N), int(K), ctypes.c_void_p(int(A) or None),
+                                                           int(lda), ctypes.c_void_p(int(B) or None), int(ldb)))
 
 
 def smem_shape(kind: int):
@@ -332,10 +345,12 @@ def sgemm(A, B, out=None, stream=None, balanced=True):
     s = (stream or torch.cuda.current_stream(A.device)).cuda_stream
     with torch.cuda.device(A.device):
         if balanced:
-            nbytes = workspace_size(M, N, K)
+            # exactly the size asked for (not the cached buffer's), so the
+            # schedule, and with it the summation order, depends only on the call
+            nbytes = workspace_size_for(M, N, K, a, lda, b, ldb)
             ws = _workspace(A.device, nbytes) if nbytes else None
             st = sgemm_f32_ws(M, N, K, a, lda, b, ldb, c, ldc, ws.data_ptr() if ws is not None else 0,
-                              ws.numel() if ws is not None else 0, s)
+                              nbytes if ws is not None else 0, s)
         else:
             st = sgemm_f32(M, N, K, a, lda, b, ldb, c, ldc, s)
     if st != SGEMM_OK:

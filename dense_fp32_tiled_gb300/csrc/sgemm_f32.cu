@@ -559,6 +559,31 @@ sgemm_f32_tail_kernel(const Problem p, const __grid_constant__ Maps maps, const 
     }
 }
 
+// Copies a rows x cols row-major matrix whose rows are not 16-byte aligned
+// (leading dimension ld_src, any 4-byte alignment) into dst, whose leading
+// dimension ld_dst is cols rounded up to 4 and whose base is 16-byte aligned,
+// so that the tensor-copy kernels can read it.  Vector q of a row holds
+// columns 4q .. 4q+3 (zeros past cols); consecutive threads take consecutive
+// vectors of a row, so the scalar loads of a warp cover 512 contiguous bytes
+// and each 16-byte store is aligned.  Grid-stride over rows x ld_dst / 4.
+__global__ void __launch_bounds__(256) repack_rows_kernel(const float *__restrict__ src, long long ld_src, int rows,
+                                                          int cols, float *__restrict__ dst, long long ld_dst) {
+    const long long per_row = ld_dst / 4;
+    const long long total = static_cast<long long>(rows) * per_row;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long r = i / per_row;
+        const int c = static_cast<int>(i - r * per_row) * 4;
+        const float *s = src + r * ld_src + c;
+        float4 v;
+        v.x = c < cols ? __ldg(s) : 0.0f;
+        v.y = c + 1 < cols ? __ldg(s + 1) : 0.0f;
+        v.z = c + 2 < cols ? __ldg(s + 2) : 0.0f;
+        v.w = c + 3 < cols ? __ldg(s + 3) : 0.0f;
+        *reinterpret_cast<float4 *>(dst + r * ld_dst + c) = v;
+    }
+}
+
 // Runs one of the bounded waits above on a target that nothing completes
 // (which = 0: a copy-ring mbarrier phase with no arrival and no copy; 1: a
 // partner flag nobody raises) or on one that is already complete (2: the
@@ -826,6 +851,61 @@ int choose_variant(int M, int N, int K, const float *A, int lda, const float *B,
     return v;
 }
 
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Products below this many FLOPs get no repack room from
+// sgemm_f32_workspace_size_for (see there).
+constexpr double kRepackMinFlops = 4e9;
+
+// Repacking of operands whose rows are not 16-byte aligned (workspace
+// entry point only).  When the workspace has room, such an operand is first
+// copied into 16-byte aligned rows in the workspace, after the schedule's
+// own words and slots, and the product runs on the tensor-copy kernels and
+// their schedules; else on the cp.async kernels with narrower copies.
+struct Repack {
+    bool a, b;            // A / B repacked
+    int lda2, ldb2;       // their new leading dimensions (K, N rounded up to 4)
+    size_t a_off, b_off;  // byte offsets of the copies in the workspace
+    size_t plan_bytes;    // the schedule's region at the start of the workspace
+    size_t bytes;         // total workspace bytes this needs
+};
+Repack plan_repack(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const DeviceInfo &info,
+                   size_t avail) {
+    Repack r = {false, false, 0, 0, 0, 0, 0, 0};
+    if (K <= 0 || encode_fn() == nullptr) return r;
+    const bool ra = vector_class(A, lda) != 4, rb = vector_class(B, ldb) != 4;
+    if (!ra && !rb) return r;
+    const long long T = tile_count(M, N), KT = (K + BK - 1) / BK;
+    const Plan pl = plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[kTmaVariant]) * info.sms, info.sms, true);
+    r.lda2 = (K + 3) / 4 * 4;
+    r.ldb2 = (N + 3) / 4 * 4;
+    r.plan_bytes = round256(pl.bytes);
+    size_t off = r.plan_bytes;
+    if (ra) {
+        r.a_off = off;
+        off += round256(static_cast<size_t>(M) * r.lda2 * sizeof(float));
+    }
+    if (rb) {
+        r.b_off = off;
+        off += round256(static_cast<size_t>(K) * r.ldb2 * sizeof(float));
+    }
+    r.bytes = off;
+    if (off <= avail) {
+        r.a = ra;
+        r.b = rb;
+    }
+    return r;
+}
+
+// The schedule run() uses: plan_schedule, then the fallbacks run() takes when
+// the workspace region (avail bytes) is too small for it.
+Plan effective_plan(long long T, long long KT, long long G, long long sms, bool tma, size_t avail) {
+    Plan pl = plan_schedule(T, KT, G, sms, tma);
+    if (pl.kind == 3 && avail < pl.bytes) pl = plan_schedule(T, KT, G, sms, false);
+    if (pl.kind != 0 && avail < pl.bytes) pl = Plan{0, T, 0, 0, 0, 0, 0, 0};
+    return pl;
+}
+
 // Runs one product whose arguments passed check_args (M, N > 0).  Uses a
 // stream-K schedule when the workspace `flags` (flag_bytes long) is large
 // enough for the plan chosen for this shape; else one CTA per tile.
@@ -839,6 +919,29 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     DeviceInfo info;
     const int st = setup_device(dev, &info);
     if (st != SGEMM_OK) return st;
+
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, flags != nullptr ? flag_bytes : 0);
+    if (rp.a || rp.b) {
+        char *ws = reinterpret_cast<char *>(flags);
+        const unsigned blocks = static_cast<unsigned>(info.sms) * 8;
+        if (rp.a) {
+            float *a2 = reinterpret_cast<float *>(ws + rp.a_off);
+            repack_rows_kernel<<<blocks, 256, 0, stream>>>(A, lda, M, K, a2, rp.lda2);
+            A = a2;
+            lda = rp.lda2;
+        }
+        if (rp.b) {
+            float *b2 = reinterpret_cast<float *>(ws + rp.b_off);
+            repack_rows_kernel<<<blocks, 256, 0, stream>>>(B, ldb, K, N, b2, rp.ldb2);
+            B = b2;
+            ldb = rp.ldb2;
+        }
+        if (cudaPeekAtLastError() != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_LAUNCH;
+        }
+        flag_bytes = rp.plan_bytes;  // the schedule keeps to the region before the copies
+    }
 
     Maps maps;
     const int v = choose_variant(M, N, K, A, lda, B, ldb, maps);
@@ -984,8 +1087,26 @@ extern "C" size_t sgemm_f32_workspace_size(int M, int N, int K) {
     return (bytes + 255) / 256 * 256;
 }
 
+extern "C" size_t sgemm_f32_workspace_size_for(int M, int N, int K, const float *A, int lda, const float *B,
+                                               int ldb) {
+    const size_t base = sgemm_f32_workspace_size(M, N, K);
+    // Smaller products run faster on the narrow copies than with a repack
+    // first (measured on GB300: 512^3 29.7 vs 35.9 us, 1000x1030x777 57.4 vs
+    // 60.0 us; from about 2 GFLOP on the repack wins, 1536^3 153.6 vs 137.5,
+    // 3000^3 1189 vs 920 us), so no room is asked for them.
+    if (base == 0 || K == 0 || 2.0 * M * N * K < kRepackMinFlops) return base;
+    int dev = 0;
+    DeviceInfo info;
+    if (cudaGetDevice(&dev) != cudaSuccess || setup_device(dev, &info) != SGEMM_OK) {
+        (void)cudaGetLastError();
+        return base;
+    }
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, SIZE_MAX);
+    return rp.bytes > base ? round256(rp.bytes) : base;
+}
+
 extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int lda, const float *B, int ldb,
-                                     const float *C, int ldc, int *kind, long long *words) {
+                                     const float *C, int ldc, size_t workspace_bytes, int *kind, long long *words) {
     if (kind == nullptr || words == nullptr) return SGEMM_ERR_NULL_PTR;
     *kind = 0;
     *words = 0;
@@ -999,12 +1120,17 @@ extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int ld
     }
     const int sd = setup_device(dev, &info);
     if (sd != SGEMM_OK) return sd;
-    Maps maps;
-    const int v = choose_variant(M, N, K, A, lda, B, ldb, maps);
-    const long long T = tile_count(M, N);
-    const Plan pl = plan_schedule(T, (K + BK - 1) / BK, static_cast<long long>(info.sk_per_sm[v]) * info.sms,
-                                  info.sms, v == kTmaVariant);
-    *kind = pl.kind;
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, workspace_bytes);
+    int v = kTmaVariant;  // the repacked operands have 16-byte aligned rows
+    if (!rp.a && !rp.b) {
+        Maps maps;
+        v = choose_variant(M, N, K, A, lda, B, ldb, maps);
+    }
+    const size_t avail = (rp.a || rp.b) ? rp.plan_bytes : workspace_bytes;
+    const Plan pl = effective_plan(tile_count(M, N), (K + BK - 1) / BK,
+                                   static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, v == kTmaVariant,
+                                   avail);
+    *kind = pl.kind | (rp.a ? 4 : 0) | (rp.b ? 8 : 0);
     *words = pl.flag_words;
     return SGEMM_OK;
 }

@@ -78,7 +78,11 @@ int sgemm_f32(int M, int N, int K,
  *
  *   workspace       : DEVICE pointer, 16-byte aligned, or NULL (then
  *                     workspace_bytes must be 0); must not overlap A, B or C.
- *   workspace_bytes : its size; sgemm_f32_workspace_size(M, N, K) is enough.
+ *   workspace_bytes : its size.  sgemm_f32_workspace_size(M, N, K) is enough
+ *                     for every schedule below;
+ *                     sgemm_f32_workspace_size_for(M, N, K, A, lda, B, ldb)
+ *                     also makes room to repack operands whose rows are not
+ *                     16-byte aligned (below).
  *
  * When the workspace is large enough, the call balances the work over the
  * CTAs the GPU holds at once (G = 2 per SM).  Every output tile (128 x 128)
@@ -106,6 +110,13 @@ int sgemm_f32(int M, int N, int K,
  * schedules 1 and 2 the last of them is an error word, nonzero only if a CTA
  * gave up waiting for a partner (about a second; the result is then wrong,
  * nothing hangs); in schedule 3 no CTA waits for another.
+ * Repacking: when A's or B's rows are not 16-byte aligned (pointer or
+ * leading dimension) and K > 0, and the workspace has room for the schedule
+ * plus a copy of that operand with 16-byte aligned rows (leading dimension
+ * rounded up to 4), the call first copies it there (one kernel per operand,
+ * HBM-bound) and runs the 16-byte-aligned kernels and schedules on the copy;
+ * without the room it runs the narrower-copy kernels on the operand itself.
+ * The copies follow the schedule's words in the workspace.
  * Other argument checks and errors are those of sgemm_f32, plus
  * SGEMM_ERR_ALIAS for a workspace overlapping A, B or C and
  * SGEMM_ERR_INVALID_ARG for a misaligned workspace.
@@ -117,22 +128,34 @@ int sgemm_f32_ws(int M, int N, int K,
                  void *workspace, size_t workspace_bytes,
                  cudaStream_t stream);
 
-/* The schedule sgemm_f32_ws would use for these arguments on the current
- * device with a large enough workspace (host-only; launches nothing):
- * *kind (0 to 3, as listed above) and *words, the 32-bit words at the start
- * of the workspace that the call zero-fills and leaves zero on success (flags
+/* What sgemm_f32_ws would run for these arguments on the current device
+ * with a workspace of workspace_bytes bytes (host-only; launches nothing):
+ * *kind = the schedule (0 to 3, as listed above) in bits 0-1, plus 4 if A is
+ * repacked and 8 if B is repacked; *words = the 32-bit words at the start of
+ * the workspace that the call zero-fills and leaves zero on success (flags
  * and error word, or tile counts).  Returns the argument-check status of
  * sgemm_f32_ws, or SGEMM_ERR_DEVICE without a usable device. */
 int sgemm_f32_ws_schedule(int M, int N, int K,
                           const float *A, int lda,
                           const float *B, int ldb,
                           const float *C, int ldc,
+                          size_t workspace_bytes,
                           int *kind, long long *words);
 
 /* Workspace bytes sgemm_f32_ws can use for this shape on the current device
- * (0 for an empty or invalid shape).  Reads device attributes only; with no
- * usable device it returns the size of the flags-only schedule. */
+ * (0 for an empty or invalid shape), not counting operand repacking.  Reads
+ * device attributes only; with no usable device it returns the size of the
+ * flags-only schedule. */
 size_t sgemm_f32_workspace_size(int M, int N, int K);
+
+/* Workspace bytes for these operands: sgemm_f32_workspace_size(M, N, K), or
+ * more when A's or B's rows are not 16-byte aligned and the product has at
+ * least 4 GFLOP (2*M*N*K), enough to repack them (see sgemm_f32_ws); smaller
+ * products measured faster without the copy.  The pointers are only
+ * inspected for alignment. */
+size_t sgemm_f32_workspace_size_for(int M, int N, int K,
+                                    const float *A, int lda,
+                                    const float *B, int ldb);
 
 /*
  * sgemm_f32_host -- the same product for operands in HOST memory: copies A

@@ -149,4 +149,4 @@ def test_schedule_query_checks_arguments_on_host(lib):
     assert sg.ws_schedule(-1, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4) == (-1, 0, 0)
     assert sg.ws_schedule(4, 4, 8, FAKE, 7, FAKE * 2, 4, FAKE * 3, 4) == (-2, 0, 0)
     assert sg.ws_schedule(0, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4) == (0, 0, 0)
-    assert lib.sgemm_f32_ws_schedule(4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, None, None) == -3
+    assert lib.sgemm_f32_ws_schedule(4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, None, None) == -3

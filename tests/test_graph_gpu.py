@@ -72,9 +72,9 @@ def test_balanced_schedules_in_a_graph(oracle_lib, M, N, K, kind):
     tA = torch.empty(M, K, device="cuda")
     tB = torch.empty(K, N, device="cuda")
     tC = torch.empty(M, N, device="cuda")
-    sst, got, _ = sg.ws_schedule(M, N, K, tA.data_ptr(), K, tB.data_ptr(), N, tC.data_ptr(), N)
-    assert sst == 0 and got == kind
     nbytes = sg.workspace_size(M, N, K)
+    sst, got, _ = sg.ws_schedule(M, N, K, tA.data_ptr(), K, tB.data_ptr(), N, tC.data_ptr(), N, nbytes)
+    assert sst == 0 and got == kind
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
 
     def call(s):

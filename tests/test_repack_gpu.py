@@ -1,0 +1,133 @@
+"""Operands whose rows are not 16-byte aligned, repacked into the workspace
+(sgemm_f32_ws with sgemm_f32_workspace_size_for bytes) vs the FP64 oracle
+(needs a GB300).
+
+The repack copies A and/or B into rows of K (N) rounded up to 4 floats, then
+the 16-byte-aligned kernels and schedules run on the copies.  Checked: the
+reported plan (schedule bits and repack bits), the result against the oracle
+(exactly, for integer inputs), that the schedule's leading words are zero
+again afterwards, that nothing past the requested size is written, and that
+the smaller workspace of sgemm_f32_workspace_size keeps the unrepacked path.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import dense_fp32_tiled_gb300 as sg
+from dense_fp32_tiled_gb300 import synth
+from tests import _tolerance as tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_fp32_tiled_gb300 import build
+    build.build()
+    sg.load_library()
+
+
+def _r256(b):
+    return (b + 255) // 256 * 256
+
+
+def _room(M, N, K):
+    """Workspace bytes with room to repack both operands, whatever the size of
+    the product (sgemm_f32_ws repacks whenever the workspace has room)."""
+    return sg.workspace_size(M, N, K) + _r256(M * ((K + 3) // 4 * 4) * 4) + _r256(K * ((N + 3) // 4 * 4) * 4)
+
+
+def _run(M, N, K, A, lda, B, ldb, ldc, a_off=0, b_off=0, nbytes=None, guard=64):
+    from tests._gpu import dev_buffer
+    tA, pA = dev_buffer(A, a_off)
+    tB, pB = dev_buffer(B, b_off)
+    c_elems = (M - 1) * ldc + N
+    tC = torch.full((c_elems + 4,), float("nan"), device="cuda")
+    if nbytes is None:
+        nbytes = _room(M, N, K)
+    ws = torch.full((nbytes // 4 + guard,), 9, dtype=torch.int32, device="cuda")
+    sst, kind, words = sg.ws_schedule(M, N, K, pA, lda, pB, ldb, tC.data_ptr(), ldc, nbytes)
+    assert sst == 0
+    st = sg.sgemm_f32_ws(M, N, K, pA, lda, pB, ldb, tC.data_ptr(), ldc, ws.data_ptr(), nbytes,
+                         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == 0
+    raw = tC.cpu().numpy()[:c_elems]
+    C = np.stack([raw[i * ldc:i * ldc + N] for i in range(M)])
+    w = ws.cpu().numpy()
+    assert not w[:words].any(), "schedule words must be zero after the call"
+    assert np.all(w[nbytes // 4:] == 9), "nothing past the requested workspace is written"
+    return C, kind
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,a_off,b_off,bits", [
+    (1000, 1030, 777, 777, 1030, 1030, 0, 0, 4 | 8),   # the ragged workload: both repacked
+    (2500, 2100, 333, 333, 2100, 2100, 0, 0, 4),       # A only (K odd), 380 tiles: split tail after
+    (2500, 2100, 336, 336, 2102, 2100, 0, 0, 8),       # B only (ldb not a multiple of 4)
+    (1100, 900, 512, 512, 900, 901, 1, 0, 4),          # A base off by 4 bytes, C misaligned too
+    (300, 5, 7, 7, 5, 5, 0, 0, 4 | 8),                 # tiny: N < 4, K < 16
+    (129, 1030, 2049, 2049, 1030, 1030, 0, 0, 4 | 8),  # deep odd K
+])
+def test_repacked_operands_match_the_oracle(oracle_lib, M, N, K, lda, ldb, ldc, a_off, b_off, bits):
+    A = synth.matrix(M, K, 351, 0, ld=lda, pad_value=np.nan)
+    B = synth.matrix(K, N, 351, 1, ld=ldb, pad_value=np.nan)
+    C, kind = _run(M, N, K, A, lda, B, ldb, ldc, a_off, b_off)
+    assert kind & 12 == bits
+    Cr, Sr = oracle_lib.gemm(A, B, M=M, N=N, K=K, lda=lda, ldb=ldb)
+    tol.assert_close(C, Cr, Sr, K, f"repacked {M}x{N}x{K}")
+
+
+def test_repacked_integer_exact_and_same_as_aligned_copy(oracle_lib):
+    """Integer inputs: exact.  And the repacked run equals the same product on
+    operands the caller laid out with aligned rows (same kernels, same
+    schedule, so bit for bit)."""
+    M, N, K = 2432, 2560, 301
+    A = synth.matrix(M, K, 353, 0, "int5")
+    B = synth.matrix(K, N, 353, 1, "int5")
+    C, kind = _run(M, N, K, A, K, B, N, N)
+    assert kind == 3 | 4  # split tail, A repacked
+    Cr, _ = oracle_lib.gemm(A, B)
+    np.testing.assert_array_equal(C.astype(np.float64), Cr)
+    K4 = (K + 3) // 4 * 4
+    A4 = np.zeros((M, K4), np.float32)
+    A4[:, :K] = A
+    Ca, kind_a = _run(M, N, K, A4, K4, B, N, N)
+    assert kind_a == 3
+    np.testing.assert_array_equal(C, Ca)
+
+
+def test_smaller_workspace_keeps_the_unrepacked_path(oracle_lib):
+    M, N, K = 1000, 1030, 777
+    A = synth.matrix(M, K, 355, 0)
+    B = synth.matrix(K, N, 355, 1)
+    C, kind = _run(M, N, K, A, K, B, N, N, nbytes=sg.workspace_size(M, N, K))
+    assert kind & 12 == 0
+    Cr, Sr = oracle_lib.gemm(A, B)
+    tol.assert_close(C, Cr, Sr, K, "unrepacked")
+
+
+def test_size_query_asks_for_repack_room_only_for_large_products():
+    from tests._gpu import dev_buffer
+    for (M, N, K), large in (((1000, 1030, 777), False), ((2048, 2048, 2049), True), ((1536, 1536, 1537), True)):
+        tA, pA = dev_buffer(np.zeros(4, np.float32))
+        base = sg.workspace_size(M, N, K)
+        got = sg.workspace_size_for(M, N, K, pA, K, pA, N)
+        assert (got > base) == large, (M, N, K)
+        assert sg.workspace_size_for(M, N, K, pA, (K + 3) // 4 * 4, pA, (N + 3) // 4 * 4) == base
+
+
+def test_torch_wrapper_uses_the_repack(oracle_lib):
+    M, N, K = 2100, 2060, 513  # 4.4 GFLOP: the size query asks for repack room
+    base = torch.from_numpy(synth.matrix(M, K + 3, 357, 0)).cuda()
+    A = base[:, 1:K + 1]  # row stride K + 3, base off by 4 bytes
+    B = torch.from_numpy(synth.matrix(K, N, 357, 1)).cuda()
+    C = torch.empty(M, N, device="cuda")
+    _, kind, _ = sg.ws_schedule(M, N, K, A.data_ptr(), K + 3, B.data_ptr(), N, C.data_ptr(), N)
+    assert kind & 4
+    sg.sgemm(A, B, out=C)
+    torch.cuda.synchronize()
+    Cr, Sr = oracle_lib.gemm(A.cpu().numpy(), B.cpu().numpy())
+    tol.assert_close(C.cpu().numpy(), Cr, Sr, K, "wrapper")

@@ -39,7 +39,7 @@ def _run_ws(M, N, K, A, lda, B, ldb, ldc, a_off=0, b_off=0, c_off=0, ws_fill=0):
     nbytes = sg.workspace_size(M, N, K)
     ws = torch.full((nbytes // 4,), ws_fill, dtype=torch.int32, device="cuda")
     pC = tC.data_ptr() + 4 * c_off
-    sst, kind, words = sg.ws_schedule(M, N, K, pA, lda, pB, ldb, pC, ldc)
+    sst, kind, words = sg.ws_schedule(M, N, K, pA, lda, pB, ldb, pC, ldc, nbytes)
     assert sst == 0 and 0 < words <= nbytes // 4
     st = sg.sgemm_f32_ws(M, N, K, pA, lda, pB, ldb, pC, ldc, ws.data_ptr(), nbytes,
                          torch.cuda.current_stream().cuda_stream)
@@ -112,9 +112,9 @@ def test_words_past_the_used_ones_are_untouched():
     tA, pA = dev_buffer(A)
     tB, pB = dev_buffer(B)
     C = torch.empty(M, N, device="cuda")
-    sst, kind, used = sg.ws_schedule(M, N, K, pA, K, pB, N, C.data_ptr(), N)
+    nbytes = sg.workspace_size(M, N, K)  # no room to repack A
+    sst, kind, used = sg.ws_schedule(M, N, K, pA, K, pB, N, C.data_ptr(), N, nbytes)
     assert sst == 0 and kind == 1 and used == _tiles(M, N) + 1
-    nbytes = sg.workspace_size(M, N, K)
     ws = torch.full((nbytes // 4 + 8,), 7, dtype=torch.int32, device="cuda")
     st = sg.sgemm_f32_ws(M, N, K, pA, K, pB, N, C.data_ptr(), N, ws.data_ptr(), nbytes,
                          torch.cuda.current_stream().cuda_stream)
@@ -164,7 +164,7 @@ def _plan_words(M, N, K, pA, lda, pB, ldb, pC, ldc):
     """Flag words (with the error word) of the multi-part schedule (kind 2,
     fewer tiles than resident CTAs) the library plans for these operands, or
     None if it plans another schedule."""
-    sst, kind, words = sg.ws_schedule(M, N, K, pA, lda, pB, ldb, pC, ldc)
+    sst, kind, words = sg.ws_schedule(M, N, K, pA, lda, pB, ldb, pC, ldc, sg.workspace_size(M, N, K))
     assert sst == 0
     if kind != 2:
         return None
