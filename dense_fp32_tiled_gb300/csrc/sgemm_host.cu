@@ -12,11 +12,15 @@
 // panel, B's left columns, B's right columns, then A's other panels, and the
 // left half computes while B's right columns are still in flight.
 //
+// The device copies of A, B and C have 16-byte aligned rows (leading
+// dimensions rounded up to 4 floats), whatever the host leading dimensions.
+//
 // Host memory should be pinned (page-locked) for the copies to run
 // asynchronously at full speed; pageable memory works, but the CUDA runtime
 // then stages it.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 #include <mutex>
 
@@ -29,6 +33,9 @@ constexpr int kMaxPanels = 4;
 constexpr int kPanelRows = 1024;  // rows per panel when M allows several (a multiple of the 128-row tile)
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+// Device copies keep rows 16-byte aligned (leading dimension rounded up to
+// 4 floats), so the products always run on the tensor-copy kernels.
+long long pad4(long long n) { return (n + 3) / 4 * 4; }
 
 // Row panels: P panels of `rows` rows (the last may be shorter).
 void panels_of(int M, int &P, int &rows) {
@@ -51,9 +58,9 @@ HostLayout host_layout(int M, int N, int K) {
     panels_of(M, P, rows);
     HostLayout l;
     l.b = 0;
-    l.a = round256(static_cast<size_t>(K) * N * 4);
-    l.c = l.a + round256(static_cast<size_t>(M) * K * 4);
-    l.ws = l.c + round256(static_cast<size_t>(M) * N * 4);
+    l.a = round256(static_cast<size_t>(K) * pad4(N) * 4);
+    l.c = l.a + round256(static_cast<size_t>(M) * pad4(K) * 4);
+    l.ws = l.c + round256(static_cast<size_t>(M) * pad4(N) * 4);
     // the products run one after another on one stream, so they share one
     // workspace sized for the largest need among the shapes they take
     const int first = rows < M ? rows : M;
@@ -112,6 +119,7 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
     if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_LD;
     if (M == 0 || N == 0) return SGEMM_OK;
+    if (K > INT_MAX - 3 || N > INT_MAX - 3) return SGEMM_ERR_INVALID_DIM;  // padded leading dimensions
     if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr)) || workspace == nullptr) return SGEMM_ERR_NULL_PTR;
     const uintptr_t host_bits =
         reinterpret_cast<uintptr_t>(C) | (K > 0 ? reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) : 0);
@@ -139,6 +147,7 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     int P = 0, rows = 0;
     panels_of(M, P, rows);
     const int n1 = first_split(P, N);
+    const int K4 = static_cast<int>(pad4(K)), N4 = static_cast<int>(pad4(N));  // fit: checked above
 
     // events: start, B's left columns landed, all of B landed, all copied
     // back, A panel p landed, C panel p computed
@@ -161,12 +170,12 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     };
     // columns [c0, c0 + nc) of B, all K rows
     auto copy_b = [&](int c0, int nc) {
-        return K == 0 || cudaMemcpy2DAsync(dB + c0, static_cast<size_t>(N) * 4, B + c0, static_cast<size_t>(ldb) * 4,
+        return K == 0 || cudaMemcpy2DAsync(dB + c0, static_cast<size_t>(N4) * 4, B + c0, static_cast<size_t>(ldb) * 4,
                                            static_cast<size_t>(nc) * 4, K, cudaMemcpyHostToDevice, h2d) == cudaSuccess;
     };
     auto copy_a = [&](int p) {
         const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
-        return (K == 0 || cudaMemcpy2DAsync(dA + static_cast<size_t>(r0) * K, static_cast<size_t>(K) * 4,
+        return (K == 0 || cudaMemcpy2DAsync(dA + static_cast<size_t>(r0) * K4, static_cast<size_t>(K4) * 4,
                                             A + static_cast<size_t>(r0) * lda, static_cast<size_t>(lda) * 4,
                                             static_cast<size_t>(K) * 4, nr, cudaMemcpyHostToDevice,
                                             h2d) == cudaSuccess) &&
@@ -175,8 +184,8 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     // columns [c0, c0 + nc) of panel p's product
     auto product = [&](int p, int c0, int nc) {
         const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
-        return sgemm_f32_ws(nr, nc, K, dA + static_cast<size_t>(r0) * K, K > 0 ? K : 1, dB + c0, N,
-                            dC + static_cast<size_t>(r0) * N + c0, N, dW, l.ws_bytes, stream);
+        return sgemm_f32_ws(nr, nc, K, dA + static_cast<size_t>(r0) * K4, K4 > 0 ? K4 : 1, dB + c0, N4,
+                            dC + static_cast<size_t>(r0) * N4 + c0, N4, dW, l.ws_bytes, stream);
     };
     // the workspace may still be in use by work queued earlier on `stream`
     if (cudaEventRecord(e_start, stream) != cudaSuccess || cudaStreamWaitEvent(h2d, e_start, 0) != cudaSuccess ||
@@ -205,7 +214,7 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
         if (cudaEventRecord(e_c[p], stream) != cudaSuccess || cudaStreamWaitEvent(d2h, e_c[p], 0) != cudaSuccess)
             return fail(SGEMM_ERR_LAUNCH);
         if (cudaMemcpy2DAsync(C + static_cast<size_t>(r0) * ldc, static_cast<size_t>(ldc) * 4,
-                              dC + static_cast<size_t>(r0) * N, static_cast<size_t>(N) * 4,
+                              dC + static_cast<size_t>(r0) * N4, static_cast<size_t>(N4) * 4,
                               static_cast<size_t>(N) * 4, nr, cudaMemcpyDeviceToHost, d2h) != cudaSuccess)
             return fail(SGEMM_ERR_LAUNCH);
     }

@@ -173,7 +173,8 @@ size_t sgemm_f32_workspace_size_for(int M, int N, int K,
  *                     speed; pageable memory works, staged by the runtime.
  *   workspace       : DEVICE pointer, 256-byte aligned, at least
  *                     sgemm_f32_host_workspace_size(M,N,K) bytes.  It holds
- *                     dense device copies of B, A and C and the product's
+ *                     device copies of B, A and C, their rows padded to a
+ *                     multiple of 4 floats (16-byte aligned), and the product's
  *                     own workspace.  Its contents are not preserved, and calls
  *                     sharing a workspace are ordered by `stream`.
  *   stream          : work queued on `stream` before the call completes
