@@ -80,11 +80,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-// Polls one mbarrier phase at most `limit` times; false if it gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t polls = 0; !mbar_try_wait(bar, parity);)
-        if (++polls > limit) return false;
-    return true;
+// Polls one mbarrier phase at most `limit` times; a wait that runs out sets
+// *timeout_flag to 1 and returns.
+__device__ __forceinline__ void mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit,
+                                                  unsigned *timeout_flag) {
+    uint32_t polls = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if (++polls > limit) {
+            *timeout_flag = 1u;
+            break;
+        }
+    }
 }
 // 2-D tiled bulk copy global -> shared; elements outside the tensor read 0.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
@@ -226,7 +232,7 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
     auto wait_tile = [&](int kt, auto pending) {
         if constexpr (TMA) {
             const uint32_t u = u0 + kt;
-            if (!mbar_wait_bounded(bars + 8 * (u % STAGES), (u / STAGES) & 1u, kWaitLimit)) g_copy_timeout = 1u;
+            mbar_wait_bounded(bars + 8 * (u % STAGES), (u / STAGES) & 1u, kWaitLimit, &g_copy_timeout);
         } else {
             cp_async_wait<decltype(pending)::value>();
         }
@@ -598,7 +604,7 @@ __global__ void wait_selftest_kernel(int which, unsigned limit, unsigned *status
             mbar_init(b, 1);
             asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
             if (which == 2) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(b) : "memory");
-            status[0] = mbar_wait_bounded(b, 0, limit) ? 0u : 1u;
+            mbar_wait_bounded(b, 0, limit, status);  // status[0] was zeroed by the host
         }
     } else {
         if (which == 3 && threadIdx.x == 0) st_release(status + 1, 1u);
