@@ -178,9 +178,10 @@ def sgemm_host(A, B, out=None, device=None, stream=None):
     c, ldc = _host_matrix_args(out, M, N, "out")
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
-        ws = _workspace(dev, host_workspace_size(M, N, K))
         st_obj = stream or torch.cuda.current_stream(dev)
-        st = sgemm_f32_host(M, N, K, a, lda, b, ldb, c, ldc, ws.data_ptr(), ws.numel(), st_obj.cuda_stream)
+        nbytes = host_workspace_size(M, N, K)
+        ws = _workspace("host", dev, st_obj, nbytes)
+        st = sgemm_f32_host(M, N, K, a, lda, b, ldb, c, ldc, ws.data_ptr(), nbytes, st_obj.cuda_stream)
         if st != SGEMM_OK:
             raise SgemmError(st, "sgemm_f32_host")
         st_obj.synchronize()
@@ -224,12 +225,9 @@ def wait_selftest(case: str, polls: int = 1000) -> bool:
     return n.value == 1
 
 
-_tc_workspaces = {}
-
-
 def sgemm_tc(A, B, out=None, stream=None):
     """C = A @ B through the tensor-core 3xTF32 variant (same FP32 tolerance,
-    not bit-identical to sgemm); the workspace is a cached torch buffer."""
+    not bit-identical to sgemm); the workspace is cached per device and stream."""
     import torch
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError(f"shape mismatch: {tuple(A.shape)} @ {tuple(B.shape)}")
@@ -241,13 +239,11 @@ def sgemm_tc(A, B, out=None, stream=None):
     b, ldb = _matrix_args(B, K, N, "B")
     c, ldc = _matrix_args(out, M, N, "out")
     nbytes = tc_workspace_size(M, N, K)
-    ws = _tc_workspaces.get(A.device)
-    if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=A.device)
-        _tc_workspaces[A.device] = ws
-    s = (stream or torch.cuda.current_stream(A.device)).cuda_stream
+    st_obj = stream or torch.cuda.current_stream(A.device)
     with torch.cuda.device(A.device):
-        st = sgemm_f32_3xtf32(M, N, K, a, lda, b, ldb, c, ldc, ws.data_ptr(), ws.numel(), s)
+        ws = _workspace("tc", A.device, st_obj, nbytes)
+        st = sgemm_f32_3xtf32(M, N, K, a, lda, b, ldb, c, ldc, ws.data_ptr(), max(nbytes, 256),
+                              st_obj.cuda_stream)
     if st != SGEMM_OK:
         raise SgemmError(st, "sgemm_f32_3xtf32")
     return out
@@ -312,13 +308,19 @@ def _matrix_args(t, rows: int, cols: int, name: str):
 _workspaces = {}
 
 
-def _workspace(device, nbytes: int):
-    """A per-device scratch buffer for sgemm_f32_ws, grown on demand (torch memory)."""
+def _workspace(kind: str, device, stream, nbytes: int):
+    """Scratch for one entry point on one stream of one device (torch memory,
+    grown on demand).  Calls on one stream are ordered, so they can share it;
+    calls on different streams get different buffers.  record_stream keeps
+    torch from handing the memory out again while work queued on `stream`
+    may still use it."""
     import torch
-    buf = _workspaces.get(device)
+    key = (kind, torch.device(device), stream.cuda_stream)
+    buf = _workspaces.get(key)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.zeros(max(nbytes, 1 << 12), dtype=torch.uint8, device=device)
-        _workspaces[device] = buf
+        buf = torch.empty(max(nbytes, 1 << 12), dtype=torch.uint8, device=device)
+        _workspaces[key] = buf
+    buf.record_stream(stream)
     return buf
 
 
@@ -328,9 +330,9 @@ def sgemm(A, B, out=None, stream=None, balanced=True):
     ``out`` (M x N, row-major) is written when given, else allocated.  Runs on
     ``stream`` (a torch.cuda.Stream) or the current stream; asynchronous.
     With ``balanced`` (default) the call goes through sgemm_f32_ws with a
-    per-device workspace, which enables the stream-K schedule; otherwise
-    through sgemm_f32.  Calls that share the cached workspace must run in
-    stream order (the default when one stream is used).
+    workspace cached per device and stream, which enables the balanced
+    schedules and the repacking of unaligned rows; otherwise through
+    sgemm_f32.
     """
     import torch
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
@@ -342,13 +344,14 @@ def sgemm(A, B, out=None, stream=None, balanced=True):
     a, lda = _matrix_args(A, M, K, "A")
     b, ldb = _matrix_args(B, K, N, "B")
     c, ldc = _matrix_args(out, M, N, "out")
-    s = (stream or torch.cuda.current_stream(A.device)).cuda_stream
+    st_obj = stream or torch.cuda.current_stream(A.device)
+    s = st_obj.cuda_stream
     with torch.cuda.device(A.device):
         if balanced:
             # exactly the size asked for (not the cached buffer's), so the
             # schedule, and with it the summation order, depends only on the call
             nbytes = workspace_size_for(M, N, K, a, lda, b, ldb)
-            ws = _workspace(A.device, nbytes) if nbytes else None
+            ws = _workspace("ws", A.device, st_obj, nbytes) if nbytes else None
             st = sgemm_f32_ws(M, N, K, a, lda, b, ldb, c, ldc, ws.data_ptr() if ws is not None else 0,
                               nbytes if ws is not None else 0, s)
         else:

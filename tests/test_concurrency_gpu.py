@@ -90,3 +90,28 @@ def test_concurrent_callers_match_serial_calls():
             assert torch.equal(C, Cs)
             assert torch.equal(Ct, Cts)
     assert sg.copy_timeouts() == 0 and sg.tc_timeouts() == 0
+
+
+def test_torch_wrappers_on_two_streams_do_not_share_a_workspace():
+    """sgemm / sgemm_tc cache their workspaces per device and stream, so
+    products queued on two streams at once cannot overwrite each other's
+    partial sums."""
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    jobs = _jobs(470)
+    want = []
+    for M, N, K, A, lda, B in jobs:
+        Av = A.view(-1)[: (M - 1) * lda + K].as_strided((M, K), (lda, 1))
+        want.append((sg.sgemm(Av, B), sg.sgemm_tc(Av, B)))
+    torch.cuda.synchronize()
+    for rep in range(3):
+        got = []
+        for i, (M, N, K, A, lda, B) in enumerate(jobs):
+            Av = A.view(-1)[: (M - 1) * lda + K].as_strided((M, K), (lda, 1))
+            s = s1 if (i + rep) % 2 == 0 else s2
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                got.append((sg.sgemm(Av, B, stream=s), sg.sgemm_tc(Av, B, stream=s)))
+        torch.cuda.synchronize()
+        for (C, Ct), (Cw, Ctw) in zip(got, want):
+            assert torch.equal(C, Cw)
+            assert torch.equal(Ct, Ctw)
