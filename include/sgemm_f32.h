@@ -17,8 +17,11 @@
  * unspecified, so results agree with an exact dot product to FP32 rounding,
  * not bit for bit with another order.
  *
- * All functions are thread-safe.  None allocates device memory.  The first call
- * on a device sets up that device's kernel attributes (once, under a lock).
+ * All functions are thread-safe (calls of sgemm_f32_static_scratch that
+ * overlap on the GPU share its scratch: see there).  No product entry point
+ * allocates device memory; only the two wait self-tests allocate (and free)
+ * a few bytes.  The first call on a device sets up that device's kernel
+ * attributes (once, under a lock).
  */
 #ifndef SGEMM_F32_H
 #define SGEMM_F32_H
