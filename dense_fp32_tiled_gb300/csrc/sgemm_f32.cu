@@ -33,6 +33,7 @@
 
 #include "sgemm_f32.h"
 #include "smem_layout.cuh"
+#include "transpose_f32.h"
 
 namespace {
 
@@ -163,11 +164,22 @@ __device__ __forceinline__ void acc_zero(Acc &acc) {
 //   4. 16 k steps of fragment reads and packed FMAs on tile kt.
 // On return every copy has landed; the caller must __syncthreads() before
 // starting another range (other threads may still read shared memory).
-template <int VA, int VB, bool TMA>
+//
+// AT: p.A holds A already transposed (At = A^T, K x M, row stride p.lda), so
+// each stage's A half receives the k-major tile directly from a tensor copy
+// and nothing is transposed in shared memory.  The ring is then STAGES_AT
+// deep and iteration kt waits for tile kt itself:
+//   1. wait until tile kt has landed, then barrier (every thread has
+//      finished tile kt-1, whose stage is free);
+//   2. issue the copies of tile kt+STAGES_AT-1 into that stage;
+//   3. 16 k steps on tile kt.
+template <int VA, int VB, bool TMA, bool AT>
 __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, const int m0, const int n0,
                                             const int kt0, const int kt1, uint32_t &pipe, float *smem,
                                             const uint32_t bars, Acc &acc) {
     static_assert(!TMA || (VA == 4 && VB == 4), "tensor copies need 16-byte aligned rows");
+    static_assert(!AT || TMA, "the k-major A tile arrives by tensor copy");
+    constexpr uint32_t RING = AT ? STAGES_AT : STAGES;
     const int tid = threadIdx.x;
     const int K = p.K, M = p.M, N = p.N;
     const uint32_t sbase = smem_u32(smem);
@@ -193,13 +205,14 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
     const float *b_colp = p.B + (b_valid > 0 ? b_col : 0);
 
     auto issue_tile = [&](int kt) {
-        const uint32_t stage = (u0 + kt) % STAGES;
+        const uint32_t stage = (u0 + kt) % RING;
         const int kb = kt * BK;
         if constexpr (TMA) {
             if (tid == 0) {
                 const uint32_t bar = bars + 8 * stage;
                 mbar_expect_tx(bar, STAGE_FLOATS * 4);
-                tma_load_2d(sbase + ar_word(stage, 0, 0) * 4, &maps.a, kb, m0, bar);
+                if constexpr (AT) tma_load_2d(sbase + at_word(stage, 0, 0) * 4, &maps.a, m0, kb, bar);
+                else tma_load_2d(sbase + ar_word(stage, 0, 0) * 4, &maps.a, kb, m0, bar);
                 tma_load_2d(sbase + bs_word(stage, 0, 0) * 4, &maps.b, n0, kb, bar);
             }
         } else {
@@ -232,7 +245,7 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
     auto wait_tile = [&](int kt, auto pending) {
         if constexpr (TMA) {
             const uint32_t u = u0 + kt;
-            mbar_wait_bounded(bars + 8 * (u % STAGES), (u / STAGES) & 1u, kWaitLimit, &g_copy_timeout);
+            mbar_wait_bounded(bars + 8 * (u % RING), (u / RING) & 1u, kWaitLimit, &g_copy_timeout);
         } else {
             cp_async_wait<decltype(pending)::value>();
         }
@@ -258,6 +271,37 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
 
     const int ra = frag_row0(tid);
     const int cb = frag_col0(tid);
+
+    if constexpr (AT) {
+        // prologue: tiles kt0 .. kt0+STAGES_AT-2 in flight
+#pragma unroll
+        for (int s = 0; s < STAGES_AT - 1; ++s)
+            if (kt0 + s < kt1) issue_tile(kt0 + s);
+        for (int kt = kt0; kt < kt1; ++kt) {
+            wait_tile(kt, Pending1{});
+            __syncthreads();
+            if (kt + STAGES_AT - 1 < kt1) issue_tile(kt + STAGES_AT - 1);
+            const uint32_t stage = (u0 + kt) % RING;
+#pragma unroll
+            for (int k = 0; k < BK; ++k) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(smem + at_word(stage, k, ra));
+                const float4 a1 = *reinterpret_cast<const float4 *>(smem + at_word(stage, k, ra + 16));
+                const float4 b0 = *reinterpret_cast<const float4 *>(smem + bs_word(stage, k, cb));
+                const float4 b1 = *reinterpret_cast<const float4 *>(smem + bs_word(stage, k, cb + 32));
+                const float a[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float2 bp[TN / 2] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                           make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+#pragma unroll
+                for (int j = 0; j < TN / 2; ++j) {
+#pragma unroll
+                    for (int r = 0; r < TM; ++r)
+                        acc.c[r][j] = __ffma2_rn(make_float2(a[r], a[r]), bp[j], acc.c[r][j]);
+                }
+            }
+        }
+        pipe += static_cast<uint32_t>(kt1 > kt0 ? kt1 - kt0 : 0);
+        return;
+    }
 
     // prologue: tiles kt0 .. kt0+STAGES-2 in flight, tile kt0 transposed
 #pragma unroll
@@ -308,11 +352,12 @@ __device__ __forceinline__ float *aligned_smem(float *raw) {
     const uint32_t s = smem_u32(raw);
     return raw + ((SMEM_ALIGN - (s & (SMEM_ALIGN - 1))) & (SMEM_ALIGN - 1)) / 4;
 }
+constexpr int kMaxRing = STAGES_AT > STAGES ? STAGES_AT : STAGES;
 template <bool TMA>
 __device__ __forceinline__ void init_bars(uint32_t bars) {
     if (TMA) {
         if (threadIdx.x == 0) {
-            for (int s = 0; s < STAGES; ++s) mbar_init(bars + 8 * s, 1);
+            for (int s = 0; s < kMaxRing; ++s) mbar_init(bars + 8 * s, 1);
             asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         }
         __syncthreads();
@@ -360,10 +405,10 @@ __device__ __forceinline__ void store_tile(const Problem &p, const int m0, const
 }
 
 // Data-parallel schedule: one CTA per C tile, the whole K range.
-template <int VA, int VB, bool TMA>
+template <int VA, int VB, bool TMA, bool AT>
 __global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p, const __grid_constant__ Maps maps) {
     extern __shared__ float smem_raw[];
-    __shared__ __align__(8) uint64_t bar_mem[STAGES];
+    __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
     // a split-tail grid queued behind this one may start as SMs free up: it
     // writes other tiles and reads nothing this grid writes
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -375,7 +420,7 @@ __global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p,
     Acc acc;
     acc_zero(acc);
     uint32_t pipe = 0;
-    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
+    mma_k_range<VA, VB, TMA, AT>(p, maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
     store_tile<false>(p, tm * BM, tn * BN, acc);
 }
 
@@ -450,12 +495,12 @@ __device__ __forceinline__ void raise_flag(unsigned *flag) {
 // cycle, and the order of the additions is fixed: results are deterministic.
 // A wait longer than kSpinLimit polls sets bit 0 of the word after the flags
 // and stores without that part: a wrong result, never a hang.
-template <int VA, int VB, bool TMA>
+template <int VA, int VB, bool TMA, bool AT>
 __global__ void __launch_bounds__(NT, 2)
 sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles, unsigned *flags,
                          float *partials) {
     extern __shared__ float smem_raw[];
-    __shared__ __align__(8) uint64_t bar_mem[STAGES];
+    __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
     float *smem = aligned_smem(smem_raw);
     const uint32_t bars = smem_u32(bar_mem);
     init_bars<TMA>(bars);
@@ -490,7 +535,7 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
         tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
         Acc acc;
         acc_zero(acc);
-        mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
+        mma_k_range<VA, VB, TMA, AT>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
         if (k0 == 0 && k1 == KT) {
             store_tile<false>(p, tm * BM, tn * BN, acc);
         } else if (k0 > 0) {  // hand the partial sums for k >= k0 over to the owner
@@ -528,12 +573,12 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
 // counts itself in counts[c / S]; the part that arrives last adds all S
 // slots in part order and stores the tile: deterministic, and no CTA waits
 // for another.
-template <int VA, int VB, bool TMA>
+template <int VA, int VB, bool TMA, bool AT>
 __global__ void __launch_bounds__(NT, 2)
 sgemm_f32_tail_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles, const int parts,
                       unsigned *counts, float *slots) {
     extern __shared__ float smem_raw[];
-    __shared__ __align__(8) uint64_t bar_mem[STAGES];
+    __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
     __shared__ int last;
     float *smem = aligned_smem(smem_raw);
     const uint32_t bars = smem_u32(bar_mem);
@@ -547,7 +592,7 @@ sgemm_f32_tail_kernel(const Problem p, const __grid_constant__ Maps maps, const 
     Acc acc;
     acc_zero(acc);
     uint32_t pipe = 0;
-    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
+    mma_k_range<VA, VB, TMA, AT>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
     store_partial(slots + static_cast<size_t>(c) * (BM * BN), acc);
     __threadfence();
     __syncthreads();
@@ -619,21 +664,27 @@ __global__ void wait_selftest_kernel(int which, unsigned limit, unsigned *status
 // ---------------------------------------------------------------------------
 
 constexpr int kMaxDevices = 64;
-constexpr int kVariants = 7;  // (VA, VB) in {4, 1} x {4, 2, 1} with cp.async, and (4, 4) with TMA
+// (VA, VB) in {4, 1} x {4, 2, 1} with cp.async; (4, 4) with TMA; and (4, 4)
+// with TMA on the k-major copy of A (AT)
+constexpr int kVariants = 8;
 constexpr int kTmaVariant = 6;
+constexpr int kAtVariant = 7;
 using DpKernel = void (*)(Problem, Maps);
 using SkKernel = void (*)(Problem, Maps, int, unsigned *, float *);
 const DpKernel kDp[kVariants] = {
-    sgemm_f32_tiled_kernel<4, 4, false>, sgemm_f32_tiled_kernel<4, 2, false>, sgemm_f32_tiled_kernel<4, 1, false>,
-    sgemm_f32_tiled_kernel<1, 4, false>, sgemm_f32_tiled_kernel<1, 2, false>, sgemm_f32_tiled_kernel<1, 1, false>,
-    sgemm_f32_tiled_kernel<4, 4, true>};
+    sgemm_f32_tiled_kernel<4, 4, false, false>, sgemm_f32_tiled_kernel<4, 2, false, false>,
+    sgemm_f32_tiled_kernel<4, 1, false, false>, sgemm_f32_tiled_kernel<1, 4, false, false>,
+    sgemm_f32_tiled_kernel<1, 2, false, false>, sgemm_f32_tiled_kernel<1, 1, false, false>,
+    sgemm_f32_tiled_kernel<4, 4, true, false>,  sgemm_f32_tiled_kernel<4, 4, true, true>};
 const SkKernel kSk[kVariants] = {
-    sgemm_f32_streamk_kernel<4, 4, false>, sgemm_f32_streamk_kernel<4, 2, false>,
-    sgemm_f32_streamk_kernel<4, 1, false>, sgemm_f32_streamk_kernel<1, 4, false>,
-    sgemm_f32_streamk_kernel<1, 2, false>, sgemm_f32_streamk_kernel<1, 1, false>,
-    sgemm_f32_streamk_kernel<4, 4, true>};
+    sgemm_f32_streamk_kernel<4, 4, false, false>, sgemm_f32_streamk_kernel<4, 2, false, false>,
+    sgemm_f32_streamk_kernel<4, 1, false, false>, sgemm_f32_streamk_kernel<1, 4, false, false>,
+    sgemm_f32_streamk_kernel<1, 2, false, false>, sgemm_f32_streamk_kernel<1, 1, false, false>,
+    sgemm_f32_streamk_kernel<4, 4, true, false>,  sgemm_f32_streamk_kernel<4, 4, true, true>};
 using TailKernel = void (*)(Problem, Maps, int, int, unsigned *, float *);
-const TailKernel kTail = sgemm_f32_tail_kernel<4, 4, true>;  // tensor-copy variant only
+// tensor-copy variants only: [0] A row-major, [1] A k-major
+const TailKernel kTail[2] = {sgemm_f32_tail_kernel<4, 4, true, false>, sgemm_f32_tail_kernel<4, 4, true, true>};
+bool is_tma(int v) { return v == kTmaVariant || v == kAtVariant; }
 
 // cuTensorMapEncodeTiled, fetched from the driver at run time (no link
 // against libcuda).  Null when unavailable: the cp.async kernels are used.
@@ -659,19 +710,23 @@ EncodeTiledFn encode_fn() {
 
 // Describes A (K x M elements, rows lda apart; box 16 x 128, 64-byte
 // swizzle) and B (N x K, rows ldb apart; box 128 x 16, no swizzle) for the
-// tensor copies.  Needs 16-byte aligned bases and row strides.
-bool encode_maps(Maps &maps, int M, int N, int K, const float *A, int lda, const float *B, int ldb) {
+// tensor copies.  With a_kmajor, A is the k-major copy At (M x K elements in
+// the map's order, rows lda apart: box 128 x 16, no swizzle, the As
+// layout).  Needs 16-byte aligned bases and row strides.
+bool encode_maps(Maps &maps, int M, int N, int K, const float *A, int lda, const float *B, int ldb,
+                 bool a_kmajor = false) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
-    const cuuint64_t a_dim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t a_dim[2] = {static_cast<cuuint64_t>(a_kmajor ? M : K), static_cast<cuuint64_t>(a_kmajor ? K : M)};
     const cuuint64_t a_stride[1] = {static_cast<cuuint64_t>(lda) * 4};
-    const cuuint32_t a_box[2] = {BK, BM};
+    const cuuint32_t a_box[2] = {a_kmajor ? BM : BK, a_kmajor ? BK : BM};
     const cuuint64_t b_dim[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
     const cuuint64_t b_stride[1] = {static_cast<cuuint64_t>(ldb) * 4};
     const cuuint32_t b_box[2] = {BN, BK};
     const cuuint32_t ones[2] = {1, 1};
     return enc(&maps.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(A), a_dim, a_stride, a_box, ones,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, a_kmajor ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
            enc(&maps.b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(B), b_dim, b_stride, b_box, ones,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -714,11 +769,12 @@ int setup_device(int dev, DeviceInfo *out) {
                         cudaSuccess)
                     st = SGEMM_ERR_DEVICE;
             }
-            if (st == SGEMM_OK &&
-                (cudaFuncSetAttribute(kTail, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
-                 cudaFuncSetAttribute(kTail, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                      cudaSharedmemCarveoutMaxShared) != cudaSuccess))
-                st = SGEMM_ERR_DEVICE;
+            for (const TailKernel f : kTail)
+                if (st == SGEMM_OK &&
+                    (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
+                     cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                          cudaSharedmemCarveoutMaxShared) != cudaSuccess))
+                    st = SGEMM_ERR_DEVICE;
         }
         if (st != SGEMM_OK) (void)cudaGetLastError();  // do not leave our failure sticky for the caller
         d.state = st == SGEMM_OK ? 1 : st;
@@ -863,29 +919,76 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 // sgemm_f32_workspace_size_for (see there).
 constexpr double kRepackMinFlops = 4e9;
 
-// Repacking of operands whose rows are not 16-byte aligned (workspace
-// entry point only).  When the workspace has room, such an operand is first
-// copied into 16-byte aligned rows in the workspace, after the schedule's
-// own words and slots, and the product runs on the tensor-copy kernels and
-// their schedules; else on the cp.async kernels with narrower copies.
+// Whether transposing a 16-byte aligned A into its k-major copy first pays.
+// Measured on GB300 (same results bit for bit): the k-major kernels take
+// about 2.5 % less time than the row-major ones (4096^3 1986 -> 1934 us,
+// 8192^3 15643 -> 15300 us, 3072^3 900 -> 873 us, 2048^3 277 -> 270 us,
+// 16384x256x4096 539 -> 528 us), and the transpose moves 8 M K bytes at
+// about 5.5 TB/s plus a launch (4096^3 26.8 us, 16384 x 4096 84.3 us).  So
+// the copy pays once N is large: it is taken when the expected saving, 2.5 %
+// of 2MNK at 70 TFLOP/s, exceeds 1.2 x the transpose's time (4096^3: 49 vs
+// 34 us, whole product 69.2 -> 70.1 TFLOP/s; 8192^3 70.3 -> 71.5; it is not
+// taken at 16384x256x4096, 2048^3 or 2500x2100x4096, where it measured
+// 12 %, 1.6 % and 0.3 % slower).  An A whose rows are not 16-byte aligned is
+// copied anyway, and then always into the k-major copy.
+bool kmajor_pays(int M, int N, int K) {
+    const double saving = 0.025 * 2.0 * M * N * K / 70e12;
+    const double copy = 8.0 * M * K / 5.5e12 + 4e-6;
+    return saving > 1.2 * copy;
+}
+
+// Copies of the operands in the workspace (workspace entry point only),
+// placed after the schedule's own words and slots.
+//   * k-major A: when the workspace has room for it, A is first transposed
+//     into At = A^T (K rows of M floats, row stride M rounded up to 4) by
+//     the transpose kernel, whatever A's alignment, and the product runs on
+//     the k-major tensor-copy kernels (kAtVariant), which load the fragment
+//     layout directly and store nothing to shared memory in their K loop.
+//   * Otherwise an operand whose rows are not 16-byte aligned is copied into
+//     16-byte aligned rows when there is room, and the product runs on the
+//     tensor-copy kernels and their schedules; else on the cp.async kernels
+//     with narrower copies.
+//   B is repacked in both cases when its rows are not 16-byte aligned.
 struct Repack {
     bool a, b;            // A / B repacked
-    int lda2, ldb2;       // their new leading dimensions (K, N rounded up to 4)
+    bool at;              // A transposed into the k-major copy (instead of repacked)
+    int lda2, ldb2;       // the repacked leading dimensions (K, N rounded up to 4)
+    int ldat;             // the k-major copy's row stride (M rounded up to 4)
     size_t a_off, b_off;  // byte offsets of the copies in the workspace
+    size_t at_off;
     size_t plan_bytes;    // the schedule's region at the start of the workspace
     size_t bytes;         // total workspace bytes this needs
 };
 Repack plan_repack(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const DeviceInfo &info,
-                   size_t avail) {
-    Repack r = {false, false, 0, 0, 0, 0, 0, 0};
+                   size_t avail, bool at_pays) {
+    Repack r = {false, false, false, 0, 0, 0, 0, 0, 0, 0, 0};
     if (K <= 0 || encode_fn() == nullptr) return r;
     const bool ra = vector_class(A, lda) != 4, rb = vector_class(B, ldb) != 4;
-    if (!ra && !rb) return r;
+    const bool want_at = at_pays || ra;
+    if (!ra && !rb && !want_at) return r;
     const long long T = tile_count(M, N), KT = (K + BK - 1) / BK;
-    const Plan pl = plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[kTmaVariant]) * info.sms, info.sms, true);
+    const int v = want_at ? kAtVariant : kTmaVariant;
+    const Plan pl = plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, true);
     r.lda2 = (K + 3) / 4 * 4;
     r.ldb2 = (N + 3) / 4 * 4;
+    r.ldat = (M + 3) / 4 * 4;
     r.plan_bytes = round256(pl.bytes);
+    if (want_at) {
+        size_t off = r.plan_bytes;
+        r.at_off = off;
+        off += round256(static_cast<size_t>(K) * r.ldat * sizeof(float));
+        if (rb) {
+            r.b_off = off;
+            off += round256(static_cast<size_t>(K) * r.ldb2 * sizeof(float));
+        }
+        r.bytes = off;
+        if (off <= avail) {
+            r.at = true;
+            r.b = rb;
+            return r;
+        }
+        if (!ra && !rb) return r;  // no room: nothing else to copy
+    }
     size_t off = r.plan_bytes;
     if (ra) {
         r.a_off = off;
@@ -895,7 +998,7 @@ Repack plan_repack(int M, int N, int K, const float *A, int lda, const float *B,
         r.b_off = off;
         off += round256(static_cast<size_t>(K) * r.ldb2 * sizeof(float));
     }
-    r.bytes = off;
+    if (!want_at) r.bytes = off;
     if (off <= avail) {
         r.a = ra;
         r.b = rb;
@@ -926,8 +1029,35 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     const int st = setup_device(dev, &info);
     if (st != SGEMM_OK) return st;
 
-    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, flags != nullptr ? flag_bytes : 0);
-    if (rp.a || rp.b) {
+    const Repack rp =
+        plan_repack(M, N, K, A, lda, B, ldb, info, flags != nullptr ? flag_bytes : 0, kmajor_pays(M, N, K));
+    Maps maps;
+    if (rp.at) {
+        // every copy's address is known before anything is launched: encode
+        // the tensor maps of the copies first, so a failure launches nothing
+        char *ws = reinterpret_cast<char *>(flags);
+        float *at = reinterpret_cast<float *>(ws + rp.at_off);
+        float *b2 = rp.b ? reinterpret_cast<float *>(ws + rp.b_off) : nullptr;
+        memset(&maps, 0, sizeof maps);
+        if (!encode_maps(maps, M, N, K, at, rp.ldat, rp.b ? b2 : B, rp.b ? rp.ldb2 : ldb, true))
+            return SGEMM_ERR_DEVICE;
+        if (transpose_f32(M, K, A, lda, at, rp.ldat, stream) != TRANSPOSE_OK) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_LAUNCH;
+        }
+        A = at;
+        lda = rp.ldat;
+        if (rp.b) {
+            repack_rows_kernel<<<static_cast<unsigned>(info.sms) * 8, 256, 0, stream>>>(B, ldb, K, N, b2, rp.ldb2);
+            if (cudaPeekAtLastError() != cudaSuccess) {
+                (void)cudaGetLastError();
+                return SGEMM_ERR_LAUNCH;
+            }
+            B = b2;
+            ldb = rp.ldb2;
+        }
+        flag_bytes = rp.plan_bytes;  // the schedule keeps to the region before the copies
+    } else if (rp.a || rp.b) {
         char *ws = reinterpret_cast<char *>(flags);
         const unsigned blocks = static_cast<unsigned>(info.sms) * 8;
         if (rp.a) {
@@ -949,8 +1079,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
         flag_bytes = rp.plan_bytes;  // the schedule keeps to the region before the copies
     }
 
-    Maps maps;
-    const int v = choose_variant(M, N, K, A, lda, B, ldb, maps);
+    const int v = rp.at ? kAtVariant : choose_variant(M, N, K, A, lda, B, ldb, maps);
     Problem p;
     p.M = M; p.N = N; p.K = K; p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
     p.tiles_m = (M + BM - 1) / BM;
@@ -959,7 +1088,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     const long long T = static_cast<long long>(p.tiles_m) * p.tiles_n;
     const long long G = static_cast<long long>(info.sk_per_sm[v]) * info.sms;
     const long long KT = (K + BK - 1) / BK;
-    Plan pl = plan_schedule(T, KT, G, info.sms, v == kTmaVariant);
+    Plan pl = plan_schedule(T, KT, G, info.sms, is_tma(v));
 
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT);
@@ -985,7 +1114,8 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
             cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
-            if (cudaLaunchKernelEx(&cfg, kTail, p, maps, static_cast<int>(pl.dp_tiles), pl.tail_parts, counts,
+            if (cudaLaunchKernelEx(&cfg, kTail[v == kAtVariant ? 1 : 0], p, maps, static_cast<int>(pl.dp_tiles),
+                                   pl.tail_parts, counts,
                                    slots) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return SGEMM_ERR_LAUNCH;
@@ -1107,7 +1237,7 @@ extern "C" size_t sgemm_f32_workspace_size_for(int M, int N, int K, const float 
         (void)cudaGetLastError();
         return base;
     }
-    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, SIZE_MAX);
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, SIZE_MAX, kmajor_pays(M, N, K));
     return rp.bytes > base ? round256(rp.bytes) : base;
 }
 
@@ -1126,17 +1256,16 @@ extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int ld
     }
     const int sd = setup_device(dev, &info);
     if (sd != SGEMM_OK) return sd;
-    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, workspace_bytes);
-    int v = kTmaVariant;  // the repacked operands have 16-byte aligned rows
-    if (!rp.a && !rp.b) {
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, workspace_bytes, kmajor_pays(M, N, K));
+    int v = rp.at ? kAtVariant : kTmaVariant;  // the copies have 16-byte aligned rows
+    if (!rp.a && !rp.b && !rp.at) {
         Maps maps;
         v = choose_variant(M, N, K, A, lda, B, ldb, maps);
     }
-    const size_t avail = (rp.a || rp.b) ? rp.plan_bytes : workspace_bytes;
+    const size_t avail = (rp.a || rp.b || rp.at) ? rp.plan_bytes : workspace_bytes;
     const Plan pl = effective_plan(tile_count(M, N), (K + BK - 1) / BK,
-                                   static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, v == kTmaVariant,
-                                   avail);
-    *kind = pl.kind | (rp.a ? 4 : 0) | (rp.b ? 8 : 0);
+                                   static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, is_tma(v), avail);
+    *kind = pl.kind | (rp.a ? 4 : 0) | (rp.b ? 8 : 0) | (rp.at ? 16 : 0);
     *words = pl.flag_words;
     return SGEMM_OK;
 }
@@ -1194,7 +1323,9 @@ extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n
         case 0: steps = A_COPIES16; break;
         case 1: steps = b_copies<4>(); break;
         case 2:
-        case 3: steps = 2 * BK; break;
+        case 3:
+        case 9:
+        case 10: steps = 2 * BK; break;
         case 4: steps = b_copies<2>(); break;
         case 5: steps = b_copies<1>(); break;
         case 6: steps = A_COPIES4; break;
@@ -1204,7 +1335,7 @@ extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n
     }
     if (n_warps) *n_warps = NT / 32;
     if (n_steps) *n_steps = steps;
-    if (n_stages) *n_stages = (kind == 2 || kind == 8) ? 2 : STAGES;
+    if (n_stages) *n_stages = (kind == 2 || kind == 8) ? 2 : (kind == 9 || kind == 10) ? STAGES_AT : STAGES;
     return SGEMM_OK;
 }
 
@@ -1228,7 +1359,9 @@ extern "C" int sgemm_f32_smem_request(int kind, int warp, int step, int stage, i
             case 7: a_xpose_coord(tid, step, k, x); word = ar_word(stage, x, k); width = 16; break;
             case 8: a_xpose_coord(tid, step >> 2, k, x); word = as_word(stage, k + (step & 3), x); width = 4; break;
             case 2: word = as_word(stage, step >> 1, frag_row0(tid) + 16 * (step & 1)); width = 16; break;
-            case 3: word = bs_word(stage, step >> 1, frag_col0(tid) + 32 * (step & 1)); width = 16; break;
+            case 3:
+            case 10: word = bs_word(stage, step >> 1, frag_col0(tid) + 32 * (step & 1)); width = 16; break;
+            case 9: word = at_word(stage, step >> 1, frag_row0(tid) + 16 * (step & 1)); width = 16; break;
         }
         byte_offset[lane] = static_cast<int64_t>(word) * 4;
     }

@@ -84,8 +84,8 @@ int sgemm_f32(int M, int N, int K,
  *   workspace_bytes : its size.  sgemm_f32_workspace_size(M, N, K) is enough
  *                     for every schedule below;
  *                     sgemm_f32_workspace_size_for(M, N, K, A, lda, B, ldb)
- *                     also makes room to repack operands whose rows are not
- *                     16-byte aligned (below).
+ *                     also makes room for the operand copies below where
+ *                     they pay.
  *
  * When the workspace is large enough, the call balances the work over the
  * CTAs the GPU holds at once (G = 2 per SM).  Every output tile (128 x 128)
@@ -113,13 +113,24 @@ int sgemm_f32(int M, int N, int K,
  * schedules 1 and 2 the last of them is an error word, nonzero only if a CTA
  * gave up waiting for a partner (about a second; the result is then wrong,
  * nothing hangs); in schedule 3 no CTA waits for another.
- * Repacking: when A's or B's rows are not 16-byte aligned (pointer or
- * leading dimension) and K > 0, and the workspace has room for the schedule
- * plus a copy of that operand with 16-byte aligned rows (leading dimension
- * rounded up to 4), the call first copies it there (one kernel per operand,
- * HBM-bound) and runs the 16-byte-aligned kernels and schedules on the copy;
- * without the room it runs the narrower-copy kernels on the operand itself.
- * The copies follow the schedule's words in the workspace.
+ * Operand copies (K > 0; each one kernel, HBM-bound; placed after the
+ * schedule's words in the workspace):
+ *   k-major A: when the k-major copy pays (large N, see
+ *      sgemm_f32_workspace_size_for) or A's rows are not 16-byte aligned
+ *      (pointer or lda), and the workspace has room for the schedule plus
+ *      At = A^T (K rows of M floats, row stride M rounded up to 4) plus the
+ *      repacked B below if B needs it, the call first transposes A into At
+ *      (the transpose_f32 kernel) and runs kernels that load k-major A tiles
+ *      straight into the layout the FMA loop reads: no transpose in shared
+ *      memory and no shared store in the K loop.  The summation order is
+ *      unchanged, so the result equals the call without the copy bit for bit.
+ *   repacked rows: otherwise, when A's or B's rows are not 16-byte aligned
+ *      and the workspace has room for the schedule plus a copy of that
+ *      operand with 16-byte aligned rows (leading dimension rounded up to 4),
+ *      the call first copies it there and runs the 16-byte-aligned kernels and
+ *      schedules on the copy.
+ *   Without the room it runs the narrower-copy kernels on the operands
+ *   themselves.
  * Other argument checks and errors are those of sgemm_f32, plus
  * SGEMM_ERR_ALIAS for a workspace overlapping A, B or C and
  * SGEMM_ERR_INVALID_ARG for a misaligned workspace.
@@ -134,7 +145,8 @@ int sgemm_f32_ws(int M, int N, int K,
 /* What sgemm_f32_ws would run for these arguments on the current device
  * with a workspace of workspace_bytes bytes (host-only; launches nothing):
  * *kind = the schedule (0 to 3, as listed above) in bits 0-1, plus 4 if A is
- * repacked and 8 if B is repacked; *words = the 32-bit words at the start of
+ * repacked, 8 if B is repacked and 16 if A is transposed into its k-major
+ * copy; *words = the 32-bit words at the start of
  * the workspace that the call zero-fills and leaves zero on success (flags
  * and error word, or tile counts).  Returns the argument-check status of
  * sgemm_f32_ws, or SGEMM_ERR_DEVICE without a usable device. */
@@ -152,10 +164,16 @@ int sgemm_f32_ws_schedule(int M, int N, int K,
 size_t sgemm_f32_workspace_size(int M, int N, int K);
 
 /* Workspace bytes for these operands: sgemm_f32_workspace_size(M, N, K), or
- * more when A's or B's rows are not 16-byte aligned and the product has at
- * least 4 GFLOP (2*M*N*K), enough to repack them (see sgemm_f32_ws); smaller
- * products measured faster without the copy.  The pointers are only
- * inspected for alignment. */
+ * more, enough for the operand copies of sgemm_f32_ws, in two cases:
+ *   - A's or B's rows are not 16-byte aligned and the product has at least
+ *     4 GFLOP (2*M*N*K): room for the k-major copy of an unaligned A and the
+ *     repacked copy of an unaligned B (smaller products measured faster
+ *     without the copies);
+ *   - the k-major copy of A pays: its expected saving, 2.5 % of the product's
+ *     time at 70 TFLOP/s, exceeds 1.2 times the transpose's (8*M*K bytes at
+ *     5.5 TB/s plus 4 us).  This holds for large N (4096^3: 69.2 -> 70.1
+ *     TFLOP/s measured on GB300), not for 16384 x 256 x 4096 or 2048^3.
+ * The pointers are only inspected for alignment. */
 size_t sgemm_f32_workspace_size_for(int M, int N, int K,
                                     const float *A, int lda,
                                     const float *B, int ldb);
@@ -310,14 +328,16 @@ const char *sgemm_f32_status_string(int status);
  *          1 = B tile copy (16-byte copies), 4 = 8-byte, 5 = 4-byte class,
  *          7 = A transpose read (raw tile -> registers, 16-byte),
  *          8 = A transpose store (registers -> k-major tile, 4-byte),
- *          2 = A fragment read (16-byte), 3 = B fragment read (16-byte).
+ *          2 = A fragment read (16-byte), 3 = B fragment read (16-byte);
+ *          with the k-major copy of A (no transpose, a 4-deep ring):
+ *          9 = A fragment read from the ring stage, 10 = B fragment read.
  *   warp : warp index in the CTA, 0 <= warp < *n_warps.
  *   step : which instruction of that warp, 0 <= step < *n_steps (copies,
  *          transpose reads and stores: index within one tile; fragment
  *          reads: 2*k + half, k < BK).
- *   stage: ring stage (copies, transpose reads, B reads) or k-major buffer
- *          (A reads, transpose stores) the access targets, 0 <= stage <
- *          *n_stages.
+ *   stage: ring stage (copies, transpose reads, B reads, kinds 9 and 10)
+ *          or k-major buffer (A reads, transpose stores) the access targets,
+ *          0 <= stage < *n_stages.
  *   byte_offset[32] (out): shared-memory byte offset each lane touches,
  *          relative to the start of the dynamic shared-memory block.
  *   width_bytes (out): bytes each lane moves (4, 8 or 16).

@@ -1,13 +1,15 @@
-"""Operands whose rows are not 16-byte aligned, repacked into the workspace
-(sgemm_f32_ws with sgemm_f32_workspace_size_for bytes) vs the FP64 oracle
-(needs a GB300).
+"""Operands whose rows are not 16-byte aligned, copied into the workspace
+(sgemm_f32_ws with room for the copies) vs the FP64 oracle (needs a GB300).
 
-The repack copies A and/or B into rows of K (N) rounded up to 4 floats, then
-the 16-byte-aligned kernels and schedules run on the copies.  Checked: the
-reported plan (schedule bits and repack bits), the result against the oracle
-(exactly, for integer inputs), that the schedule's leading words are zero
-again afterwards, that nothing past the requested size is written, and that
-the smaller workspace of sgemm_f32_workspace_size keeps the unrepacked path.
+An unaligned A is transposed into its k-major copy (K rows of M rounded up to
+4 floats) when the workspace has room for it, else repacked into rows of K
+rounded up to 4; an unaligned B is repacked into rows of N rounded up to 4.
+The 16-byte-aligned kernels and schedules then run on the copies.  Checked:
+the reported plan (schedule bits and copy bits), the result against the
+oracle (exactly, for integer inputs), that the schedule's leading words are
+zero again afterwards, that nothing past the requested size is written, and
+that the smaller workspace of sgemm_f32_workspace_size keeps the uncopied
+path.
 """
 import numpy as np
 import pytest
@@ -34,10 +36,23 @@ def _r256(b):
     return (b + 255) // 256 * 256
 
 
+def _a_repack(M, K):
+    return _r256(M * ((K + 3) // 4 * 4) * 4)
+
+
+def _a_kmajor(M, K):
+    return _r256(K * ((M + 3) // 4 * 4) * 4)
+
+
+def _b_repack(K, N):
+    return _r256(K * ((N + 3) // 4 * 4) * 4)
+
+
 def _room(M, N, K):
-    """Workspace bytes with room to repack both operands, whatever the size of
-    the product (sgemm_f32_ws repacks whenever the workspace has room)."""
-    return sg.workspace_size(M, N, K) + _r256(M * ((K + 3) // 4 * 4) * 4) + _r256(K * ((N + 3) // 4 * 4) * 4)
+    """Workspace bytes with room for either copy of A and the repacked B,
+    whatever the size of the product (sgemm_f32_ws copies whenever the
+    workspace has room)."""
+    return sg.workspace_size(M, N, K) + max(_a_repack(M, K), _a_kmajor(M, K)) + _b_repack(K, N)
 
 
 def _run(M, N, K, A, lda, B, ldb, ldc, a_off=0, b_off=0, nbytes=None, guard=64):
@@ -64,20 +79,36 @@ def _run(M, N, K, A, lda, B, ldb, ldc, a_off=0, b_off=0, nbytes=None, guard=64):
 
 
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc,a_off,b_off,bits", [
-    (1000, 1030, 777, 777, 1030, 1030, 0, 0, 4 | 8),   # the ragged workload: both repacked
-    (2500, 2100, 333, 333, 2100, 2100, 0, 0, 4),       # A only (K odd), 380 tiles: split tail after
-    (2500, 2100, 336, 336, 2102, 2100, 0, 0, 8),       # B only (ldb not a multiple of 4)
-    (1100, 900, 512, 512, 900, 901, 1, 0, 4),          # A base off by 4 bytes, C misaligned too
-    (300, 5, 7, 7, 5, 5, 0, 0, 4 | 8),                 # tiny: N < 4, K < 16
-    (129, 1030, 2049, 2049, 1030, 1030, 0, 0, 4 | 8),  # deep odd K
+    (1000, 1030, 777, 777, 1030, 1030, 0, 0, 16 | 8),   # the ragged workload: A k-major, B repacked
+    (2500, 2100, 333, 333, 2100, 2100, 0, 0, 16),       # A only (K odd), 380 tiles: split tail after
+    (2500, 2100, 336, 336, 2102, 2100, 0, 0, 8),        # B only (ldb not a multiple of 4)
+    (1100, 900, 512, 512, 900, 901, 1, 0, 16),          # A base off by 4 bytes, C misaligned too
+    (300, 5, 7, 7, 5, 5, 0, 0, 16 | 8),                 # tiny: N < 4, K < 16
+    (129, 1030, 2049, 2049, 1030, 1030, 0, 0, 16 | 8),  # deep odd K
+    (1001, 700, 515, 515, 700, 700, 0, 0, 16),          # M not a multiple of 4: padded k-major rows
 ])
-def test_repacked_operands_match_the_oracle(oracle_lib, M, N, K, lda, ldb, ldc, a_off, b_off, bits):
+def test_copied_operands_match_the_oracle(oracle_lib, M, N, K, lda, ldb, ldc, a_off, b_off, bits):
     A = synth.matrix(M, K, 351, 0, ld=lda, pad_value=np.nan)
     B = synth.matrix(K, N, 351, 1, ld=ldb, pad_value=np.nan)
     C, kind = _run(M, N, K, A, lda, B, ldb, ldc, a_off, b_off)
-    assert kind & 12 == bits
+    assert kind & 28 == bits
     Cr, Sr = oracle_lib.gemm(A, B, M=M, N=N, K=K, lda=lda, ldb=ldb)
-    tol.assert_close(C, Cr, Sr, K, f"repacked {M}x{N}x{K}")
+    tol.assert_close(C, Cr, Sr, K, f"copied {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(129, 1030, 2049), (61, 300, 1025)])
+def test_room_for_the_row_repack_only(oracle_lib, M, N, K):
+    """A workspace with room for the row repack of A but not for its k-major
+    copy takes the row repack.  129 x 2049 repacks into 2052-float rows
+    (1.06 MB), its k-major copy needs 2049 rows of 132 floats (1.08 MB)."""
+    assert _a_kmajor(M, K) > _a_repack(M, K)
+    nbytes = sg.workspace_size(M, N, K) + _a_repack(M, K) + (_b_repack(K, N) if N % 4 else 0)
+    A = synth.matrix(M, K, 352, 0, ld=K, pad_value=np.nan)
+    B = synth.matrix(K, N, 352, 1, ld=N, pad_value=np.nan)
+    C, kind = _run(M, N, K, A, K, B, N, N, nbytes=nbytes)
+    assert kind & 28 == 4 | (8 if N % 4 else 0)
+    Cr, Sr = oracle_lib.gemm(A, B, M=M, N=N, K=K, lda=K, ldb=N)
+    tol.assert_close(C, Cr, Sr, K, f"row-repacked {M}x{N}x{K}")
 
 
 def test_repacked_integer_exact_and_same_as_aligned_copy(oracle_lib):
@@ -88,7 +119,7 @@ def test_repacked_integer_exact_and_same_as_aligned_copy(oracle_lib):
     A = synth.matrix(M, K, 353, 0, "int5")
     B = synth.matrix(K, N, 353, 1, "int5")
     C, kind = _run(M, N, K, A, K, B, N, N)
-    assert kind == 3 | 4  # split tail, A repacked
+    assert kind == 3 | 16  # split tail, A in its k-major copy
     Cr, _ = oracle_lib.gemm(A, B)
     np.testing.assert_array_equal(C.astype(np.float64), Cr)
     K4 = (K + 3) // 4 * 4
@@ -104,7 +135,7 @@ def test_smaller_workspace_keeps_the_unrepacked_path(oracle_lib):
     A = synth.matrix(M, K, 355, 0)
     B = synth.matrix(K, N, 355, 1)
     C, kind = _run(M, N, K, A, K, B, N, N, nbytes=sg.workspace_size(M, N, K))
-    assert kind & 12 == 0
+    assert kind & 28 == 0
     Cr, Sr = oracle_lib.gemm(A, B)
     tol.assert_close(C, Cr, Sr, K, "unrepacked")
 
@@ -126,7 +157,7 @@ def test_torch_wrapper_uses_the_repack(oracle_lib):
     B = torch.from_numpy(synth.matrix(K, N, 357, 1)).cuda()
     C = torch.empty(M, N, device="cuda")
     _, kind, _ = sg.ws_schedule(M, N, K, A.data_ptr(), K + 3, B.data_ptr(), N, C.data_ptr(), N)
-    assert kind & 4
+    assert kind & 16
     sg.sgemm(A, B, out=C)
     torch.cuda.synchronize()
     Cr, Sr = oracle_lib.gemm(A.cpu().numpy(), B.cpu().numpy())
