@@ -506,7 +506,7 @@ def main():
         dist.destroy_process_group()
 
 
-SIMT_SOURCES = ("sgemm_f32.cu", "smem_layout.cuh")
+SIMT_SOURCES = ("sgemm_f32.cu", "smem_layout.cuh", "transpose_f32.cu")  # the headline step runs all three
 TC_SOURCES = ("sgemm_3xtf32.cu",)
 TRANSPOSE_SOURCES = ("transpose_f32.cu",)
 
