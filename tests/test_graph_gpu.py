@@ -83,6 +83,25 @@ def test_balanced_schedules_in_a_graph(oracle_lib, M, N, K, kind):
     _replay_matches_direct(oracle_lib, M, N, K, call, tA, tB, tC, 301)
 
 
+def test_kmajor_copy_in_a_graph(oracle_lib):
+    """A whose rows are not 16-byte aligned (lda = K + 1) with room for its
+    k-major copy: the transpose kernel, then the k-major kernels."""
+    M, N, K = 1000, 1032, 777
+    lda = K + 1
+    tA = torch.empty(M, lda, device="cuda")[:, :K]
+    tB = torch.empty(K, N, device="cuda")
+    tC = torch.empty(M, N, device="cuda")
+    nbytes = sg.workspace_size(M, N, K) + (K * ((M + 3) // 4 * 4) * 4 + 255) // 256 * 256
+    sst, got, _ = sg.ws_schedule(M, N, K, tA.data_ptr(), lda, tB.data_ptr(), N, tC.data_ptr(), N, nbytes)
+    assert sst == 0 and got & 16
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+    def call(s):
+        return sg.sgemm_f32_ws(M, N, K, tA.data_ptr(), lda, tB.data_ptr(), N, tC.data_ptr(), N, ws.data_ptr(),
+                               nbytes, s)
+    _replay_matches_direct(oracle_lib, M, N, K, call, tA, tB, tC, 321)
+
+
 def test_allocation_free_entry_in_a_graph(oracle_lib):
     M, N, K = 300, 262, 190
     tA = torch.empty(M, K, device="cuda")

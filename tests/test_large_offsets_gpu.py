@@ -7,7 +7,7 @@ address computation on the path (copies, tensor maps, stores, the split
 pass of the 3xTF32 variant) must be 64-bit.  The padding is NaN, so a read of
 it would show in the result.  Rows on both sides of the 2**31 boundary are
 checked against the FP64 oracle; the CUDA-core result must equal the oracle
-exactly for integer inputs.
+exactly for integer inputs, with and without the k-major copy of A.
 """
 import numpy as np
 import pytest
@@ -73,6 +73,31 @@ def test_cuda_core_path_past_2_31(oracle_lib, big):
     _check_rows(oracle_lib, A, B, C, True, "cuda-core")
     assert torch.all(C_buf[M - 1, N:N + 64] == -3.0)  # the padding of the last row is left alone
     del C_buf
+
+
+def test_kmajor_copy_past_2_31(oracle_lib, big):
+    """The same A placed 4 bytes off 16-byte alignment, so that sgemm_f32_ws
+    transposes it into its k-major copy first; its last rows still start past
+    2**31 floats into their buffer."""
+    A, B = big
+    free, _ = torch.cuda.mem_get_info()
+    if free < 8 * M * LDA + (2 << 30):
+        pytest.skip("needs room for a second A buffer and C")
+    A2_buf = torch.full((M, LDA), float("nan"), device="cuda")
+    A2 = A2_buf[:, 1:K + 1]
+    A2.copy_(A)
+    C_buf = torch.full((M, LDC), -3.0, device="cuda")
+    C = C_buf[:, :N]
+    nbytes = sg.workspace_size_for(M, N, K, A2.data_ptr(), LDA, B.data_ptr(), LDB)
+    sst, kind, _ = sg.ws_schedule(M, N, K, A2.data_ptr(), LDA, B.data_ptr(), LDB, C.data_ptr(), LDC, nbytes)
+    assert sst == 0 and kind & 16, kind
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    assert sg.sgemm_f32_ws(M, N, K, A2.data_ptr(), LDA, B.data_ptr(), LDB, C.data_ptr(), LDC, ws.data_ptr(), nbytes,
+                           torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    _check_rows(oracle_lib, A, B, C, True, "k-major copy")
+    assert torch.all(C_buf[M - 1, N:N + 64] == -3.0)
+    del A2_buf, C_buf, ws
 
 
 def test_tensor_core_path_past_2_31(oracle_lib, big):
