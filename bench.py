@@ -438,8 +438,10 @@ def main():
                             else None),
                 "peak_basis": f"{sms} SMs x 128 FP32 FMA/clk x 2 FLOP x {sm_max:.0f} MHz (max SM clock)"}
     if sched_kind & 3 == 3:
-        roofline["kernels"] = ("sgemm_f32_tiled_kernel (whole waves) + sgemm_f32_tail_kernel (leftover tiles in K "
-                               "parts), overlapped; achieved and traffic cover both per step")
+        dp, tail = (("sgemm_f32_kmajor_kernel", "sgemm_f32_kmajor_tail_kernel") if sched_kind & 16 else
+                    ("sgemm_f32_tiled_kernel", "sgemm_f32_tail_kernel"))
+        roofline["kernels"] = (f"{dp} (whole waves) + {tail} (leftover tiles in K parts), overlapped; achieved and "
+                               "traffic cover the whole step")
     if sched_kind & 12:
         roofline["repack"] = ("repack_rows_kernel copies " + " and ".join(
             n for n, bit in (("A", 4), ("B", 8)) if sched_kind & bit) +

@@ -137,6 +137,25 @@ SG_HD int frag_col0(int tid) {
 SG_HD int frag_row(int tid, int i) { return frag_row0(tid) + (i & 3) + 16 * (i >> 2); }
 SG_HD int frag_col(int tid, int j) { return frag_col0(tid) + (j & 3) + 32 * (j >> 2); }
 
+// ---- register-tile maps of the k-major kernels (8 x 16 per thread) -------
+// 128 threads: warp w covers rows 64*(w / 2) and cols 64*(w % 2) of the CTA
+// tile.  Lane l = 16h + 4q + 2e1 + e0 sits at (lr, lc) = (2q + e0, 2h + e1)
+// of an 8 x 4 lane grid (each quad again holds 2 rows x 2 columns of the
+// grid, so each 128-bit fragment read costs the minimum 2 wavefronts).
+// Thread rows: 4*lr + {0..3} and 32 + 4*lr + {0..3}; thread cols:
+// 16g + 4*lc + {0..3} for g = 0..3.  Per k step: 2 A reads and 4 B reads of
+// 128 bits for 64 packed FMAs.
+constexpr int NT16 = 128;        // threads per CTA of the k-major kernels
+constexpr int TN16 = 16;         // their register tile cols (rows: TM = 8)
+SG_HD int lane16_lr(int l) { return 2 * ((l >> 2) & 3) + (l & 1); }
+SG_HD int lane16_lc(int l) { return 2 * (l >> 4) + ((l >> 1) & 1); }
+SG_HD int frag16_row0(int tid) { return 64 * ((tid >> 5) >> 1) + 4 * lane16_lr(tid & 31); }
+SG_HD int frag16_col0(int tid) { return 64 * ((tid >> 5) & 1) + 4 * lane16_lc(tid & 31); }
+// i in [0, 8), j in [0, 16): row / col of register-tile element (i, j).
+SG_HD int frag16_row(int tid, int i) { return frag16_row0(tid) + (i & 3) + 32 * (i >> 2); }
+SG_HD int frag16_col(int tid, int j) { return frag16_col0(tid) + (j & 3) + 16 * (j >> 2); }
+static_assert(NT16 == 4 * 32 && 2 * (8 * 4 * 2) == BM && 2 * (4 * 4 * 4) == BN, "2 x 2 warps of 64 x 64");
+
 // ---- tile rasterisation ------------------------------------------------
 // Linear CTA index -> (tile row, tile col), walking GROUP_M tile rows at a
 // time so CTAs resident together share A row panels and B column panels.

@@ -330,11 +330,14 @@ const char *sgemm_f32_status_string(int status);
  *          8 = A transpose store (registers -> k-major tile, 4-byte),
  *          2 = A fragment read (16-byte), 3 = B fragment read (16-byte);
  *          with the k-major copy of A (no transpose, a 4-deep ring):
- *          9 = A fragment read from the ring stage, 10 = B fragment read.
+ *          9 = A fragment read from the ring stage, 10 = B fragment read
+ *          (8 x 8 register tiles, 8 warps: the stream-K kernel);
+ *          11 = A fragment read, 12 = B fragment read (8 x 16 register
+ *          tiles, 4 warps: the one-CTA-per-tile and split-tail kernels).
  *   warp : warp index in the CTA, 0 <= warp < *n_warps.
  *   step : which instruction of that warp, 0 <= step < *n_steps (copies,
  *          transpose reads and stores: index within one tile; fragment
- *          reads: 2*k + half, k < BK).
+ *          reads: 2*k + half, k < BK; kind 12: 4*k + quarter).
  *   stage: ring stage (copies, transpose reads, B reads, kinds 9 and 10)
  *          or k-major buffer (A reads, transpose stores) the access targets,
  *          0 <= stage < *n_stages.
