@@ -1106,20 +1106,23 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 // sgemm_f32_workspace_size_for (see there).
 constexpr double kRepackMinFlops = 4e9;
 
-// Whether transposing a 16-byte aligned A into its k-major copy first pays.
-// Measured on GB300 (same results bit for bit): the k-major kernels take
-// about 2.5 % less time than the row-major ones (4096^3 1986 -> 1934 us,
-// 8192^3 15643 -> 15300 us, 3072^3 900 -> 873 us, 2048^3 277 -> 270 us,
-// 16384x256x4096 539 -> 528 us), and the transpose moves 8 M K bytes at
-// about 5.5 TB/s plus a launch (4096^3 26.8 us, 16384 x 4096 84.3 us).  So
-// the copy pays once N is large: it is taken when the expected saving, 2.5 %
-// of 2MNK at 70 TFLOP/s, exceeds 1.2 x the transpose's time (4096^3: 49 vs
-// 34 us, whole product 69.2 -> 70.1 TFLOP/s; 8192^3 70.3 -> 71.5; it is not
-// taken at 16384x256x4096, 2048^3 or 2500x2100x4096, where it measured
-// 12 %, 1.6 % and 0.3 % slower).  An A whose rows are not 16-byte aligned is
-// copied anyway, and then always into the k-major copy.
-bool kmajor_pays(int M, int N, int K) {
-    const double saving = 0.025 * 2.0 * M * N * K / 70e12;
+// Whether transposing a 16-byte aligned A into its k-major copy first pays,
+// for a product the k-major variant runs with schedule `kind`.  Measured on
+// GB300, transpose included (us, row-major -> k-major; same results bit for
+// bit): the one-CTA-per-tile and split-tail kernels (8 x 16 tiles) take
+// about 4.8 % less time than the row-major ones (3072^3 901 -> 874, 4096^3
+// 1985 -> 1918, 6144^3 6630 -> 6361, 8192^3 15655 -> 14993, 2500x2100x4096
+// 672 -> 663), the stream-K kernel (8 x 8 tiles, fewer tiles than resident
+// CTAs) about 2.3 % (512x8192x8192 1059 -> 1049, but 2048^3 277 -> 282,
+// 4096x1024x4096 538 -> 553, 16384x256x4096 540 -> 612).  The transpose
+// moves 8 M K bytes at about 5.5 TB/s plus a launch (4096^2 26.8 us,
+// 16384 x 4096 84.3 us).  So the copy is taken when the expected saving, that
+// share of 2MNK at 70 TFLOP/s, exceeds 1.2 x the transpose's time.  An A
+// whose rows are not 16-byte aligned is copied anyway, and then always into
+// the k-major copy.
+bool kmajor_pays(int M, int N, int K, int kind) {
+    const double share = (kind == 0 || kind == 3) ? 0.048 : 0.023;
+    const double saving = share * 2.0 * M * N * K / 70e12;
     const double copy = 8.0 * M * K / 5.5e12 + 4e-6;
     return saving > 1.2 * copy;
 }
@@ -1147,15 +1150,18 @@ struct Repack {
     size_t bytes;         // total workspace bytes this needs
 };
 Repack plan_repack(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const DeviceInfo &info,
-                   size_t avail, bool at_pays) {
+                   size_t avail) {
     Repack r = {false, false, false, 0, 0, 0, 0, 0, 0, 0, 0};
     if (K <= 0 || encode_fn() == nullptr) return r;
     const bool ra = vector_class(A, lda) != 4, rb = vector_class(B, ldb) != 4;
-    const bool want_at = at_pays || ra;
-    if (!ra && !rb && !want_at) return r;
     const long long T = tile_count(M, N), KT = (K + BK - 1) / BK;
-    const int v = want_at ? kAtVariant : kTmaVariant;
-    const Plan pl = plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, true);
+    const Plan pl_at = plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[kAtVariant]) * info.sms, info.sms,
+                                     true);
+    const bool want_at = ra || kmajor_pays(M, N, K, pl_at.kind);
+    if (!ra && !rb && !want_at) return r;
+    const Plan pl = want_at ? pl_at
+                            : plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[kTmaVariant]) * info.sms,
+                                            info.sms, true);
     r.lda2 = (K + 3) / 4 * 4;
     r.ldb2 = (N + 3) / 4 * 4;
     r.ldat = (M + 3) / 4 * 4;
@@ -1216,8 +1222,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     const int st = setup_device(dev, &info);
     if (st != SGEMM_OK) return st;
 
-    const Repack rp =
-        plan_repack(M, N, K, A, lda, B, ldb, info, flags != nullptr ? flag_bytes : 0, kmajor_pays(M, N, K));
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, flags != nullptr ? flag_bytes : 0);
     Maps maps;
     if (rp.at) {
         // every copy's address is known before anything is launched: encode
@@ -1426,7 +1431,7 @@ extern "C" size_t sgemm_f32_workspace_size_for(int M, int N, int K, const float 
         (void)cudaGetLastError();
         return base;
     }
-    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, SIZE_MAX, kmajor_pays(M, N, K));
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, SIZE_MAX);
     return rp.bytes > base ? round256(rp.bytes) : base;
 }
 
@@ -1445,7 +1450,7 @@ extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int ld
     }
     const int sd = setup_device(dev, &info);
     if (sd != SGEMM_OK) return sd;
-    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, workspace_bytes, kmajor_pays(M, N, K));
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, workspace_bytes);
     int v = rp.at ? kAtVariant : kTmaVariant;  // the copies have 16-byte aligned rows
     if (!rp.a && !rp.b && !rp.at) {
         Maps maps;

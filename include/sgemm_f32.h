@@ -169,10 +169,13 @@ size_t sgemm_f32_workspace_size(int M, int N, int K);
  *     4 GFLOP (2*M*N*K): room for the k-major copy of an unaligned A and the
  *     repacked copy of an unaligned B (smaller products measured faster
  *     without the copies);
- *   - the k-major copy of A pays: its expected saving, 2.5 % of the product's
- *     time at 70 TFLOP/s, exceeds 1.2 times the transpose's (8*M*K bytes at
- *     5.5 TB/s plus 4 us).  This holds for large N (4096^3: 69.2 -> 70.1
- *     TFLOP/s measured on GB300), not for 16384 x 256 x 4096 or 2048^3.
+ *   - the k-major copy of A pays: its expected saving exceeds 1.2 times the
+ *     transpose's time (8*M*K bytes at 5.5 TB/s plus 4 us).  The saving is
+ *     taken as 4.8 % of the product's time at 70 TFLOP/s when it has more
+ *     output tiles than the GPU holds at once (the 8 x 16 kernels), 2.3 %
+ *     otherwise (the stream-K kernel).  This holds for large N (4096^3: 69.2
+ *     -> 71.7 TFLOP/s measured on GB300), not for 16384 x 256 x 4096 or
+ *     2048^3.
  * The pointers are only inspected for alignment. */
 size_t sgemm_f32_workspace_size_for(int M, int N, int K,
                                     const float *A, int lda,

@@ -85,7 +85,8 @@ def test_size_query_asks_for_the_copy_only_where_it_pays():
     tA, pA = dev_buffer(np.zeros(4, np.float32))
     for (M, N, K), pays in (((4096, 4096, 4096), True), ((8192, 8192, 8192), True), ((2432, 4096, 4096), True),
                             ((16384, 256, 4096), False), ((2048, 2048, 2048), False),
-                            ((2500, 2100, 4096), False), ((1024, 1024, 1024), False)):
+                            ((2500, 2100, 4096), True), ((3072, 3072, 3072), True), ((4096, 1024, 4096), False),
+                            ((1024, 1024, 1024), False)):
         base = sg.workspace_size(M, N, K)
         got = sg.workspace_size_for(M, N, K, pA, K, pA, N)
         assert (got > base) == pays, (M, N, K)
