@@ -253,8 +253,9 @@ def ws_schedule(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: i
                 workspace_bytes: int = None):
     """(status, kind, words): what sgemm_f32_ws runs for these arguments with a
     workspace of `workspace_bytes` (default: workspace_size_for these
-    operands): kind = schedule (bits 0-1) + 4 if A is repacked + 8 if B is;
-    words = the leading workspace words it zero-fills and leaves zero."""
+    operands): kind = schedule (bits 0-1) + 4 if A is repacked + 8 if B is
+    + 16 if A is transposed into its k-major copy; words = the leading
+    workspace words it zero-fills and leaves zero."""
     if workspace_bytes is None:
         workspace_bytes = workspace_size_for(M, N, K, A, lda, B, ldb)
     kind, words = ctypes.c_int(), ctypes.c_longlong()
@@ -270,7 +271,8 @@ def workspace_size(M: int, N: int, K: int) -> int:
 
 
 def workspace_size_for(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int) -> int:
-    """Workspace bytes for these operands, room to repack unaligned rows included."""
+    """Workspace bytes for these operands, room for the operand copies that pay
+    (the k-major copy of A, repacked unaligned rows) included."""
     return int(load_library().sgemm_f32_workspace_size_for(int(M), int(N), int(K), ctypes.c_void_p(int(A) or None),
                                                            int(lda), ctypes.c_void_p(int(B) or None), int(ldb)))
 
