@@ -164,22 +164,12 @@ __device__ __forceinline__ void acc_zero(Acc &acc) {
 //   4. 16 k steps of fragment reads and packed FMAs on tile kt.
 // On return every copy has landed; the caller must __syncthreads() before
 // starting another range (other threads may still read shared memory).
-//
-// AT: p.A holds A already transposed (At = A^T, K x M, row stride p.lda), so
-// each stage's A half receives the k-major tile directly from a tensor copy
-// and nothing is transposed in shared memory.  The ring is then STAGES_AT
-// deep and iteration kt waits for tile kt itself:
-//   1. wait until tile kt has landed, then barrier (every thread has
-//      finished tile kt-1, whose stage is free);
-//   2. issue the copies of tile kt+STAGES_AT-1 into that stage;
-//   3. 16 k steps on tile kt.
-template <int VA, int VB, bool TMA, bool AT>
+template <int VA, int VB, bool TMA>
 __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, const int m0, const int n0,
                                             const int kt0, const int kt1, uint32_t &pipe, float *smem,
                                             const uint32_t bars, Acc &acc) {
     static_assert(!TMA || (VA == 4 && VB == 4), "tensor copies need 16-byte aligned rows");
-    static_assert(!AT || TMA, "the k-major A tile arrives by tensor copy");
-    constexpr uint32_t RING = AT ? STAGES_AT : STAGES;
+    constexpr uint32_t RING = STAGES;
     const int tid = threadIdx.x;
     const int K = p.K, M = p.M, N = p.N;
     const uint32_t sbase = smem_u32(smem);
@@ -211,8 +201,7 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
             if (tid == 0) {
                 const uint32_t bar = bars + 8 * stage;
                 mbar_expect_tx(bar, STAGE_FLOATS * 4);
-                if constexpr (AT) tma_load_2d(sbase + at_word(stage, 0, 0) * 4, &maps.a, m0, kb, bar);
-                else tma_load_2d(sbase + ar_word(stage, 0, 0) * 4, &maps.a, kb, m0, bar);
+                tma_load_2d(sbase + ar_word(stage, 0, 0) * 4, &maps.a, kb, m0, bar);
                 tma_load_2d(sbase + bs_word(stage, 0, 0) * 4, &maps.b, n0, kb, bar);
             }
         } else {
@@ -271,37 +260,6 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
 
     const int ra = frag_row0(tid);
     const int cb = frag_col0(tid);
-
-    if constexpr (AT) {
-        // prologue: tiles kt0 .. kt0+STAGES_AT-2 in flight
-#pragma unroll
-        for (int s = 0; s < STAGES_AT - 1; ++s)
-            if (kt0 + s < kt1) issue_tile(kt0 + s);
-        for (int kt = kt0; kt < kt1; ++kt) {
-            wait_tile(kt, Pending1{});
-            __syncthreads();
-            if (kt + STAGES_AT - 1 < kt1) issue_tile(kt + STAGES_AT - 1);
-            const uint32_t stage = (u0 + kt) % RING;
-#pragma unroll
-            for (int k = 0; k < BK; ++k) {
-                const float4 a0 = *reinterpret_cast<const float4 *>(smem + at_word(stage, k, ra));
-                const float4 a1 = *reinterpret_cast<const float4 *>(smem + at_word(stage, k, ra + 16));
-                const float4 b0 = *reinterpret_cast<const float4 *>(smem + bs_word(stage, k, cb));
-                const float4 b1 = *reinterpret_cast<const float4 *>(smem + bs_word(stage, k, cb + 32));
-                const float a[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float2 bp[TN / 2] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                                           make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
-#pragma unroll
-                for (int j = 0; j < TN / 2; ++j) {
-#pragma unroll
-                    for (int r = 0; r < TM; ++r)
-                        acc.c[r][j] = __ffma2_rn(make_float2(a[r], a[r]), bp[j], acc.c[r][j]);
-                }
-            }
-        }
-        pipe += static_cast<uint32_t>(kt1 > kt0 ? kt1 - kt0 : 0);
-        return;
-    }
 
     // prologue: tiles kt0 .. kt0+STAGES-2 in flight, tile kt0 transposed
 #pragma unroll
@@ -405,7 +363,7 @@ __device__ __forceinline__ void store_tile(const Problem &p, const int m0, const
 }
 
 // Data-parallel schedule: one CTA per C tile, the whole K range.
-template <int VA, int VB, bool TMA, bool AT>
+template <int VA, int VB, bool TMA>
 __global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p, const __grid_constant__ Maps maps) {
     extern __shared__ float smem_raw[];
     __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
@@ -420,7 +378,7 @@ __global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p,
     Acc acc;
     acc_zero(acc);
     uint32_t pipe = 0;
-    mma_k_range<VA, VB, TMA, AT>(p, maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
+    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
     store_tile<false>(p, tm * BM, tn * BN, acc);
 }
 
@@ -499,7 +457,9 @@ __device__ __forceinline__ void kmajor16_k_range(const Maps &maps, const int m0,
 }
 
 // store_tile for the 8 x 16 register tile: row i of the thread's tile, its
-// 16 columns as 4 groups of 4 (guarded, vectorised by C's class).
+// 16 columns as 4 groups of 4 (guarded, vectorised by C's class).  With
+// ADD_PARTIAL the value already in C is read back from L2 and added first.
+template <bool ADD_PARTIAL>
 __device__ __forceinline__ void store_tile16(const Problem &p, const int m0, const int n0, const Acc16 &acc) {
     const int tid = threadIdx.x;
     const int cb = frag16_col0(tid);
@@ -511,16 +471,25 @@ __device__ __forceinline__ void store_tile16(const Problem &p, const int m0, con
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const int col = n0 + cb + 16 * g;
-            const float v[4] = {acc.c[i][2 * g].x, acc.c[i][2 * g].y, acc.c[i][2 * g + 1].x, acc.c[i][2 * g + 1].y};
+            float v[4] = {acc.c[i][2 * g].x, acc.c[i][2 * g].y, acc.c[i][2 * g + 1].x, acc.c[i][2 * g + 1].y};
             if (col + 3 < p.N && p.vc == 4) {
+                if (ADD_PARTIAL) {
+                    const float4 o = __ldcg(reinterpret_cast<const float4 *>(crow + col));
+                    v[0] += o.x; v[1] += o.y; v[2] += o.z; v[3] += o.w;
+                }
                 *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
             } else if (col + 3 < p.N && p.vc == 2) {
+                if (ADD_PARTIAL) {
+                    const float2 o0 = __ldcg(reinterpret_cast<const float2 *>(crow + col));
+                    const float2 o1 = __ldcg(reinterpret_cast<const float2 *>(crow + col + 2));
+                    v[0] += o0.x; v[1] += o0.y; v[2] += o1.x; v[3] += o1.y;
+                }
                 *reinterpret_cast<float2 *>(crow + col) = make_float2(v[0], v[1]);
                 *reinterpret_cast<float2 *>(crow + col + 2) = make_float2(v[2], v[3]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (col + e < p.N) crow[col + e] = v[e];
+                    if (col + e < p.N) crow[col + e] = ADD_PARTIAL ? v[e] + __ldcg(crow + col + e) : v[e];
             }
         }
     }
@@ -559,7 +528,7 @@ __global__ void __launch_bounds__(NT16, 2) sgemm_f32_kmajor_kernel(const Problem
     acc16_zero(acc);
     uint32_t pipe = 0;
     kmajor16_k_range(maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
-    store_tile16(p, tm * BM, tn * BN, acc);
+    store_tile16<false>(p, tm * BM, tn * BN, acc);
 }
 
 // ---- flags between CTAs (stream-K fix-up) ------------------------------
@@ -633,7 +602,7 @@ __device__ __forceinline__ void raise_flag(unsigned *flag) {
 // cycle, and the order of the additions is fixed: results are deterministic.
 // A wait longer than kSpinLimit polls sets bit 0 of the word after the flags
 // and stores without that part: a wrong result, never a hang.
-template <int VA, int VB, bool TMA, bool AT>
+template <int VA, int VB, bool TMA>
 __global__ void __launch_bounds__(NT, 2)
 sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles, unsigned *flags,
                          float *partials) {
@@ -673,7 +642,7 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
         tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
         Acc acc;
         acc_zero(acc);
-        mma_k_range<VA, VB, TMA, AT>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
+        mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
         if (k0 == 0 && k1 == KT) {
             store_tile<false>(p, tm * BM, tn * BN, acc);
         } else if (k0 > 0) {  // hand the partial sums for k >= k0 over to the owner
@@ -703,6 +672,76 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
     }
 }
 
+// The stream-K schedule of sgemm_f32_streamk_kernel on the k-major copy of
+// A, with the 8 x 16 register tiles of sgemm_f32_kmajor_kernel (the segment
+// walk, the hand-overs and their order are the same).
+__global__ void __launch_bounds__(NT16, 2)
+sgemm_f32_kmajor_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles,
+                                unsigned *flags, float *partials) {
+    extern __shared__ float smem_raw[];
+    __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
+    float *smem = aligned_smem(smem_raw);
+    const uint32_t bars = smem_u32(bar_mem);
+    init_bars<true>(bars);
+    uint32_t pipe = 0;
+    const int KT = (p.K + BK - 1) / BK;
+    const int T = p.tiles_m * p.tiles_n;
+    const int G = gridDim.x;
+    unsigned *error = flags + (partials ? G : T);
+    const long long total_iters = static_cast<long long>(T - dp_tiles) * KT;
+    const long long base = static_cast<long long>(dp_tiles) * KT;
+    const long long it_end = base + total_iters * (blockIdx.x + 1) / G;
+    long long it = base + total_iters * blockIdx.x / G;
+    int dp_lin = blockIdx.x;
+    for (;;) {
+        int lin, k0, k1;
+        if (dp_lin < dp_tiles) {
+            lin = dp_lin;
+            k0 = 0;
+            k1 = KT;
+            dp_lin += G;
+        } else if (it < it_end) {
+            lin = static_cast<int>(it / KT);
+            k0 = static_cast<int>(it % KT);
+            k1 = static_cast<int>(k0 + (it_end - it) < KT ? k0 + (it_end - it) : KT);
+            it += k1 - k0;
+        } else {
+            break;
+        }
+        int tm, tn;
+        tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
+        Acc16 acc;
+        acc16_zero(acc);
+        kmajor16_k_range(maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
+        if (k0 == 0 && k1 == KT) {
+            store_tile16<false>(p, tm * BM, tn * BN, acc);
+        } else if (k0 > 0) {  // hand the partial sums for k >= k0 over to the owner
+            if (partials) {
+                store_partial16(partials + static_cast<size_t>(blockIdx.x) * (BM * BN), acc);
+                raise_flag(flags + blockIdx.x);
+            } else {
+                store_tile16<false>(p, tm * BM, tn * BN, acc);
+                raise_flag(flags + lin);
+            }
+        } else if (partials) {  // owner: add the parts of CTAs blockIdx.x+1 .. c_last
+            const long long last = static_cast<long long>(lin + 1) * KT - 1 - base;
+            const int c_last = static_cast<int>(((last + 1) * G + total_iters - 1) / total_iters - 1);
+            for (int c = blockIdx.x + 1; c <= c_last; ++c) {
+                wait_flag(flags + c, error);
+                add_partial16(partials + static_cast<size_t>(c) * (BM * BN), acc);
+            }
+            store_tile16<false>(p, tm * BM, tn * BN, acc);
+            if (threadIdx.x == 0)
+                for (int c = blockIdx.x + 1; c <= c_last; ++c) flags[c] = 0u;
+        } else {  // owner of a two-part tile
+            wait_flag(flags + lin, error);
+            store_tile16<true>(p, tm * BM, tn * BN, acc);
+            if (threadIdx.x == 0) flags[lin] = 0u;
+        }
+        __syncthreads();  // shared memory free for the next segment
+    }
+}
+
 // Split tail.  The last R = T mod G tiles (G = co-resident CTAs) would leave
 // a partial last wave; instead each is cut into S equal K ranges and the S*R
 // CTAs of this grid, queued behind the one-CTA-per-tile grid of the other
@@ -711,7 +750,7 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
 // counts itself in counts[c / S]; the part that arrives last adds all S
 // slots in part order and stores the tile: deterministic, and no CTA waits
 // for another.
-template <int VA, int VB, bool TMA, bool AT>
+template <int VA, int VB, bool TMA>
 __global__ void __launch_bounds__(NT, 2)
 sgemm_f32_tail_kernel(const Problem p, const __grid_constant__ Maps maps, const int dp_tiles, const int parts,
                       unsigned *counts, float *slots) {
@@ -730,7 +769,7 @@ sgemm_f32_tail_kernel(const Problem p, const __grid_constant__ Maps maps, const 
     Acc acc;
     acc_zero(acc);
     uint32_t pipe = 0;
-    mma_k_range<VA, VB, TMA, AT>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
+    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
     store_partial(slots + static_cast<size_t>(c) * (BM * BN), acc);
     __threadfence();
     __syncthreads();
@@ -783,7 +822,7 @@ sgemm_f32_kmajor_tail_kernel(const Problem p, const __grid_constant__ Maps maps,
         acc16_zero(acc);
         for (int k = 0; k < parts; ++k)
             add_partial16(slots + static_cast<size_t>(tile * parts + k) * (BM * BN), acc);
-        store_tile16(p, tm * BM, tn * BN, acc);
+        store_tile16<false>(p, tm * BM, tn * BN, acc);
     }
 }
 
@@ -841,31 +880,29 @@ __global__ void wait_selftest_kernel(int which, unsigned limit, unsigned *status
 // ---------------------------------------------------------------------------
 
 constexpr int kMaxDevices = 64;
-// (VA, VB) in {4, 1} x {4, 2, 1} with cp.async; (4, 4) with TMA; and (4, 4)
-// with TMA on the k-major copy of A (AT).  The AT variant's one-CTA-per-tile
-// and split-tail kernels are the 8 x 16 ones (NT16 threads); its stream-K
-// kernel keeps the 8 x 8 tiles (NT threads).
+// (VA, VB) in {4, 1} x {4, 2, 1} with cp.async; (4, 4) with TMA; and the
+// kernels on the k-major copy of A (8 x 16 register tiles, NT16 threads).
 constexpr int kVariants = 8;
 constexpr int kTmaVariant = 6;
 constexpr int kAtVariant = 7;
 using DpKernel = void (*)(Problem, Maps);
 using SkKernel = void (*)(Problem, Maps, int, unsigned *, float *);
 const DpKernel kDp[kVariants] = {
-    sgemm_f32_tiled_kernel<4, 4, false, false>, sgemm_f32_tiled_kernel<4, 2, false, false>,
-    sgemm_f32_tiled_kernel<4, 1, false, false>, sgemm_f32_tiled_kernel<1, 4, false, false>,
-    sgemm_f32_tiled_kernel<1, 2, false, false>, sgemm_f32_tiled_kernel<1, 1, false, false>,
-    sgemm_f32_tiled_kernel<4, 4, true, false>,  sgemm_f32_kmajor_kernel};
+    sgemm_f32_tiled_kernel<4, 4, false>, sgemm_f32_tiled_kernel<4, 2, false>,
+    sgemm_f32_tiled_kernel<4, 1, false>, sgemm_f32_tiled_kernel<1, 4, false>,
+    sgemm_f32_tiled_kernel<1, 2, false>, sgemm_f32_tiled_kernel<1, 1, false>,
+    sgemm_f32_tiled_kernel<4, 4, true>,  sgemm_f32_kmajor_kernel};
 const SkKernel kSk[kVariants] = {
-    sgemm_f32_streamk_kernel<4, 4, false, false>, sgemm_f32_streamk_kernel<4, 2, false, false>,
-    sgemm_f32_streamk_kernel<4, 1, false, false>, sgemm_f32_streamk_kernel<1, 4, false, false>,
-    sgemm_f32_streamk_kernel<1, 2, false, false>, sgemm_f32_streamk_kernel<1, 1, false, false>,
-    sgemm_f32_streamk_kernel<4, 4, true, false>,  sgemm_f32_streamk_kernel<4, 4, true, true>};
+    sgemm_f32_streamk_kernel<4, 4, false>, sgemm_f32_streamk_kernel<4, 2, false>,
+    sgemm_f32_streamk_kernel<4, 1, false>, sgemm_f32_streamk_kernel<1, 4, false>,
+    sgemm_f32_streamk_kernel<1, 2, false>, sgemm_f32_streamk_kernel<1, 1, false>,
+    sgemm_f32_streamk_kernel<4, 4, true>,  sgemm_f32_kmajor_streamk_kernel};
 using TailKernel = void (*)(Problem, Maps, int, int, unsigned *, float *);
 // tensor-copy variants only: [0] A row-major, [1] A k-major (8 x 16 tiles)
-const TailKernel kTail[2] = {sgemm_f32_tail_kernel<4, 4, true, false>, sgemm_f32_kmajor_tail_kernel};
+const TailKernel kTail[2] = {sgemm_f32_tail_kernel<4, 4, true>, sgemm_f32_kmajor_tail_kernel};
 bool is_tma(int v) { return v == kTmaVariant || v == kAtVariant; }
-// threads per CTA of variant v's one-CTA-per-tile and split-tail kernels
-unsigned dp_threads(int v) { return v == kAtVariant ? NT16 : NT; }
+// threads per CTA of variant v's kernels
+unsigned threads(int v) { return v == kAtVariant ? NT16 : NT; }
 
 // cuTensorMapEncodeTiled, fetched from the driver at run time (no link
 // against libcuda).  Null when unavailable: the cp.async kernels are used.
@@ -945,9 +982,9 @@ int setup_device(int dev, DeviceInfo *out) {
                         break;
                     }
                 }
-                if (st == SGEMM_OK &&
-                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sk_per_sm[v], kSk[v], NT, SMEM_BYTES) !=
-                        cudaSuccess)
+                if (st == SGEMM_OK && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sk_per_sm[v], kSk[v],
+                                                                                    threads(v), SMEM_BYTES) !=
+                                          cudaSuccess)
                     st = SGEMM_ERR_DEVICE;
             }
             // the k-major variant's waves are those of its 8 x 16 one-CTA-per-tile kernel too
@@ -1106,23 +1143,23 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 // sgemm_f32_workspace_size_for (see there).
 constexpr double kRepackMinFlops = 4e9;
 
-// Whether transposing a 16-byte aligned A into its k-major copy first pays,
-// for a product the k-major variant runs with schedule `kind`.  Measured on
-// GB300, transpose included (us, row-major -> k-major; same results bit for
-// bit): the one-CTA-per-tile and split-tail kernels (8 x 16 tiles) take
-// about 4.8 % less time than the row-major ones (3072^3 901 -> 874, 4096^3
-// 1985 -> 1918, 6144^3 6630 -> 6361, 8192^3 15655 -> 14993, 2500x2100x4096
-// 672 -> 663), the stream-K kernel (8 x 8 tiles, fewer tiles than resident
-// CTAs) about 2.3 % (512x8192x8192 1059 -> 1049, but 2048^3 277 -> 282,
-// 4096x1024x4096 538 -> 553, 16384x256x4096 540 -> 612).  The transpose
-// moves 8 M K bytes at about 5.5 TB/s plus a launch (4096^2 26.8 us,
-// 16384 x 4096 84.3 us).  So the copy is taken when the expected saving, that
-// share of 2MNK at 70 TFLOP/s, exceeds 1.2 x the transpose's time.  An A
-// whose rows are not 16-byte aligned is copied anyway, and then always into
-// the k-major copy.
-bool kmajor_pays(int M, int N, int K, int kind) {
-    const double share = (kind == 0 || kind == 3) ? 0.048 : 0.023;
-    const double saving = share * 2.0 * M * N * K / 70e12;
+// Whether transposing a 16-byte aligned A into its k-major copy first pays.
+// Measured on GB300, transpose included (us, row-major -> k-major; same
+// results bit for bit): the k-major kernels (8 x 16 register tiles) take
+// about 4.5 % less time than the row-major ones, whatever the schedule:
+//   one CTA per tile / split tail: 3072^3 901 -> 874, 4096^3 1985 -> 1918,
+//     6144^3 6630 -> 6361, 8192^3 15655 -> 14993, 2500x2100x4096 672 -> 663;
+//   stream-K (fewer tiles than resident CTAs): 512x8192x8192 1060 -> 1023,
+//     256x16384x4096 539 -> 522, 1024x4096x4096 538 -> 525, 2048x2048x4096
+//     537 -> 529, but 4096x1024x4096 538 -> 541, 1536^3 129 -> 130 and
+//     16384x256x4096 540 -> 598, where the transpose costs more.
+// The transpose moves 8 M K bytes at about 5.5 TB/s plus a launch (4096^2
+// 26.8 us, 16384 x 4096 84.3 us).  So the copy is taken when the expected
+// saving, 4.5 % of 2MNK at 70 TFLOP/s, exceeds 1.2 x the transpose's time.
+// An A whose rows are not 16-byte aligned is copied anyway, and then always
+// into the k-major copy.
+bool kmajor_pays(int M, int N, int K) {
+    const double saving = 0.045 * 2.0 * M * N * K / 70e12;
     const double copy = 8.0 * M * K / 5.5e12 + 4e-6;
     return saving > 1.2 * copy;
 }
@@ -1155,13 +1192,10 @@ Repack plan_repack(int M, int N, int K, const float *A, int lda, const float *B,
     if (K <= 0 || encode_fn() == nullptr) return r;
     const bool ra = vector_class(A, lda) != 4, rb = vector_class(B, ldb) != 4;
     const long long T = tile_count(M, N), KT = (K + BK - 1) / BK;
-    const Plan pl_at = plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[kAtVariant]) * info.sms, info.sms,
-                                     true);
-    const bool want_at = ra || kmajor_pays(M, N, K, pl_at.kind);
+    const bool want_at = ra || kmajor_pays(M, N, K);
     if (!ra && !rb && !want_at) return r;
-    const Plan pl = want_at ? pl_at
-                            : plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[kTmaVariant]) * info.sms,
-                                            info.sms, true);
+    const int v = want_at ? kAtVariant : kTmaVariant;
+    const Plan pl = plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, true);
     r.lda2 = (K + 3) / 4 * 4;
     r.ldb2 = (N + 3) / 4 * 4;
     r.ldat = (M + 3) / 4 * 4;
@@ -1296,7 +1330,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
                 return SGEMM_ERR_LAUNCH;
             }
             cfg.gridDim = dim3(static_cast<unsigned>(pl.dp_tiles));
-            cfg.blockDim = dim3(dp_threads(v));
+            cfg.blockDim = dim3(threads(v));
             if (cudaLaunchKernelEx(&cfg, kDp[v], p, maps) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return SGEMM_ERR_LAUNCH;
@@ -1328,6 +1362,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
             attr.id = cudaLaunchAttributeCooperative;
             attr.val.cooperative = 1;
             cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+            cfg.blockDim = dim3(threads(v));
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
             err = cudaLaunchKernelEx(&cfg, kSk[v], p, maps, static_cast<int>(pl.dp_tiles), flags, partials);
@@ -1346,7 +1381,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     }
     if (!done) {
         cfg.gridDim = dim3(static_cast<unsigned>(T));
-        cfg.blockDim = dim3(dp_threads(v));
+        cfg.blockDim = dim3(threads(v));
         err = cudaLaunchKernelEx(&cfg, kDp[v], p, maps);
         if (err != cudaSuccess) {
             (void)cudaGetLastError();
@@ -1518,8 +1553,6 @@ extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n
         case 1: steps = b_copies<4>(); break;
         case 2:
         case 3:
-        case 9:
-        case 10:
         case 11: steps = 2 * BK; break;
         case 12: steps = 4 * BK; break;
         case 4: steps = b_copies<2>(); break;
@@ -1531,7 +1564,7 @@ extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n
     }
     if (n_warps) *n_warps = (kind == 11 || kind == 12) ? NT16 / 32 : NT / 32;
     if (n_steps) *n_steps = steps;
-    if (n_stages) *n_stages = (kind == 2 || kind == 8) ? 2 : kind >= 9 ? STAGES_AT : STAGES;
+    if (n_stages) *n_stages = (kind == 2 || kind == 8) ? 2 : kind >= 11 ? STAGES_AT : STAGES;
     return SGEMM_OK;
 }
 
@@ -1555,9 +1588,7 @@ extern "C" int sgemm_f32_smem_request(int kind, int warp, int step, int stage, i
             case 7: a_xpose_coord(tid, step, k, x); word = ar_word(stage, x, k); width = 16; break;
             case 8: a_xpose_coord(tid, step >> 2, k, x); word = as_word(stage, k + (step & 3), x); width = 4; break;
             case 2: word = as_word(stage, step >> 1, frag_row0(tid) + 16 * (step & 1)); width = 16; break;
-            case 3:
-            case 10: word = bs_word(stage, step >> 1, frag_col0(tid) + 32 * (step & 1)); width = 16; break;
-            case 9: word = at_word(stage, step >> 1, frag_row0(tid) + 16 * (step & 1)); width = 16; break;
+            case 3: word = bs_word(stage, step >> 1, frag_col0(tid) + 32 * (step & 1)); width = 16; break;
             case 11: word = at_word(stage, step >> 1, frag16_row0(tid) + 32 * (step & 1)); width = 16; break;
             case 12: word = bs_word(stage, step >> 2, frag16_col0(tid) + 16 * (step & 3)); width = 16; break;
         }

@@ -169,12 +169,10 @@ size_t sgemm_f32_workspace_size(int M, int N, int K);
  *     4 GFLOP (2*M*N*K): room for the k-major copy of an unaligned A and the
  *     repacked copy of an unaligned B (smaller products measured faster
  *     without the copies);
- *   - the k-major copy of A pays: its expected saving exceeds 1.2 times the
- *     transpose's time (8*M*K bytes at 5.5 TB/s plus 4 us).  The saving is
- *     taken as 4.8 % of the product's time at 70 TFLOP/s when it has more
- *     output tiles than the GPU holds at once (the 8 x 16 kernels), 2.3 %
- *     otherwise (the stream-K kernel).  This holds for large N (4096^3: 69.2
- *     -> 71.7 TFLOP/s measured on GB300), not for 16384 x 256 x 4096 or
+ *   - the k-major copy of A pays: its expected saving, 4.5 % of the
+ *     product's time at 70 TFLOP/s, exceeds 1.2 times the transpose's time
+ *     (8*M*K bytes at 5.5 TB/s plus 4 us).  This holds for large N (4096^3:
+ *     69.2 -> 71.7 TFLOP/s measured on GB300), not for 16384 x 256 x 4096 or
  *     2048^3.
  * The pointers are only inspected for alignment. */
 size_t sgemm_f32_workspace_size_for(int M, int N, int K,
@@ -332,16 +330,14 @@ const char *sgemm_f32_status_string(int status);
  *          7 = A transpose read (raw tile -> registers, 16-byte),
  *          8 = A transpose store (registers -> k-major tile, 4-byte),
  *          2 = A fragment read (16-byte), 3 = B fragment read (16-byte);
- *          with the k-major copy of A (no transpose, a 4-deep ring):
- *          9 = A fragment read from the ring stage, 10 = B fragment read
- *          (8 x 8 register tiles, 8 warps: the stream-K kernel);
- *          11 = A fragment read, 12 = B fragment read (8 x 16 register
- *          tiles, 4 warps: the one-CTA-per-tile and split-tail kernels).
+ *          with the k-major copy of A (no transpose, a 4-deep ring, 8 x 16
+ *          register tiles, 4 warps): 11 = A fragment read from the ring
+ *          stage, 12 = B fragment read.
  *   warp : warp index in the CTA, 0 <= warp < *n_warps.
  *   step : which instruction of that warp, 0 <= step < *n_steps (copies,
  *          transpose reads and stores: index within one tile; fragment
  *          reads: 2*k + half, k < BK; kind 12: 4*k + quarter).
- *   stage: ring stage (copies, transpose reads, B reads, kinds 9 and 10)
+ *   stage: ring stage (copies, transpose reads, B reads, kinds 11 and 12)
  *          or k-major buffer (A reads, transpose stores) the access targets,
  *          0 <= stage < *n_stages.
  *   byte_offset[32] (out): shared-memory byte offset each lane touches,

@@ -15,9 +15,8 @@ from dense_fp32_tiled_gb300 import build as sg_build
 
 KINDS = {0: "A copy (16 B)", 1: "B copy (16 B)", 2: "A fragment read", 3: "B fragment read",
          4: "B copy (8 B)", 5: "B copy (4 B)", 6: "A copy (4 B)", 7: "A transpose read",
-         8: "A transpose store", 9: "A fragment read (k-major copy of A)",
-         10: "B fragment read (k-major copy of A)", 11: "A fragment read (8 x 16 tiles)",
-         12: "B fragment read (8 x 16 tiles)"}
+         8: "A transpose store", 11: "A fragment read (k-major copy of A, 8 x 16 tiles)",
+         12: "B fragment read (k-major copy of A, 8 x 16 tiles)"}
 
 
 @pytest.fixture(scope="module")
@@ -91,6 +90,8 @@ def test_fragment_reads_stay_inside_their_tile(lib):
 
 
 def test_bad_query_rejected(lib):
+    with pytest.raises(sg.SgemmError):
+        sg.smem_request(9, 0, 0, 0)
     with pytest.raises(sg.SgemmError):
         sg.smem_request(13, 0, 0, 0)
     with pytest.raises(sg.SgemmError):
