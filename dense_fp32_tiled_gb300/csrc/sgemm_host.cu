@@ -62,13 +62,18 @@ HostLayout host_layout(int M, int N, int K) {
     l.c = l.a + round256(static_cast<size_t>(M) * pad4(K) * 4);
     l.ws = l.c + round256(static_cast<size_t>(M) * pad4(N) * 4);
     // the products run one after another on one stream, so they share one
-    // workspace sized for the largest need among the shapes they take
+    // workspace sized for the largest need among the shapes they take: the
+    // schedule's words and, where it pays, the k-major copy of the panel of
+    // A (the device copies have 16-byte aligned rows, which is all the size
+    // query inspects of its pointers, so any 16-byte aligned stand-in will do)
     const int first = rows < M ? rows : M;
     const int last = M - (P - 1) * rows;  // the last panel's rows (its schedule may differ)
     const int n1 = first_split(P, N);
-    const size_t need[4] = {sgemm_f32_workspace_size(first, N, K), sgemm_f32_workspace_size(last, N, K),
-                            sgemm_f32_workspace_size(first, n1, K),
-                            n1 < N ? sgemm_f32_workspace_size(first, N - n1, K) : 0};
+    const float *aligned = reinterpret_cast<const float *>(static_cast<uintptr_t>(256));
+    const int K4 = static_cast<int>(pad4(K > 0 ? K : 1)), N4 = static_cast<int>(pad4(N));
+    auto need_for = [&](int m, int n) { return sgemm_f32_workspace_size_for(m, n, K, aligned, K4, aligned, N4); };
+    const size_t need[4] = {need_for(first, N), need_for(last, N), need_for(first, n1),
+                            n1 < N ? need_for(first, N - n1) : 0};
     size_t w = 0;
     for (size_t x : need) w = x > w ? x : w;
     l.ws_bytes = round256(w);

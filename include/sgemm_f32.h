@@ -196,9 +196,11 @@ size_t sgemm_f32_workspace_size_for(int M, int N, int K,
  *   workspace       : DEVICE pointer, 256-byte aligned, at least
  *                     sgemm_f32_host_workspace_size(M,N,K) bytes.  It holds
  *                     device copies of B, A and C, their rows padded to a
- *                     multiple of 4 floats (16-byte aligned), and the product's
- *                     own workspace.  Its contents are not preserved, and calls
- *                     sharing a workspace are ordered by `stream`.
+ *                     multiple of 4 floats (16-byte aligned), and the products'
+ *                     own workspace (with room for the k-major copy of a panel
+ *                     of A where that pays, see sgemm_f32_workspace_size_for).
+ *                     Its contents are not preserved, and calls sharing a
+ *                     workspace are ordered by `stream`.
  *   stream          : work queued on `stream` before the call completes
  *                     before the workspace is touched; work queued after
  *                     the call sees C complete in host memory.  The host
