@@ -1141,7 +1141,7 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 // Products below this many FLOPs get no repack room from
 // sgemm_f32_workspace_size_for (see there).
-constexpr double kRepackMinFlops = 4e9;
+constexpr double kRepackMinFlops = 2e9;
 
 // Whether transposing a 16-byte aligned A into its k-major copy first pays.
 // Measured on GB300, transpose included (us, row-major -> k-major; same
@@ -1455,10 +1455,12 @@ extern "C" size_t sgemm_f32_workspace_size(int M, int N, int K) {
 extern "C" size_t sgemm_f32_workspace_size_for(int M, int N, int K, const float *A, int lda, const float *B,
                                                int ldb) {
     const size_t base = sgemm_f32_workspace_size(M, N, K);
-    // Smaller products run faster on the narrow copies than with a repack
-    // first (measured on GB300: 512^3 29.7 vs 35.9 us, 1000x1030x777 57.4 vs
-    // 60.0 us; from about 2 GFLOP on the repack wins, 1536^3 153.6 vs 137.5,
-    // 3000^3 1189 vs 920 us), so no room is asked for them.
+    // Smaller products with unaligned rows run faster on the narrow copies
+    // than with the copies first (measured on GB300, narrow -> k-major A and
+    // repacked B: 512^3 with lda = ldb = 513 28.6 -> 37.3 us, 1000x1030x777
+    // 58.6 -> 61.1, 700x900x333 32.7 -> 35.5; from about 2 GFLOP on the copies
+    // win: 1024x1024x1025 61.4 -> 58.6, 1536^3 153.7 -> 131.3, 2048x2048x2049
+    // 362.1 -> 289.3 us), so no room is asked for them.
     if (base == 0 || K == 0 || 2.0 * M * N * K < kRepackMinFlops) return base;
     int dev = 0;
     DeviceInfo info;

@@ -166,7 +166,7 @@ size_t sgemm_f32_workspace_size(int M, int N, int K);
 /* Workspace bytes for these operands: sgemm_f32_workspace_size(M, N, K), or
  * more, enough for the operand copies of sgemm_f32_ws, in two cases:
  *   - A's or B's rows are not 16-byte aligned and the product has at least
- *     4 GFLOP (2*M*N*K): room for the k-major copy of an unaligned A and the
+ *     2 GFLOP (2*M*N*K): room for the k-major copy of an unaligned A and the
  *     repacked copy of an unaligned B (smaller products measured faster
  *     without the copies);
  *   - the k-major copy of A pays: its expected saving, 4.5 % of the
