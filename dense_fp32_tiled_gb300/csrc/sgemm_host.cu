@@ -8,9 +8,10 @@
 //
 // Every row of C needs all of B, so B's copy would otherwise stall the first
 // product.  When there are several panels and N >= 512, the first panel's
-// product is cut into two column halves instead: the copy order is A's first
-// panel, B's left columns, B's right columns, then A's other panels, and the
-// left half computes while B's right columns are still in flight.
+// product is cut into column blocks instead (4 when N >= 1024, else 2): the
+// copy order is A's first panel, B's column blocks one by one, then A's
+// other panels, and each block of the first panel computes while the next
+// block of B is still in flight.
 //
 // The device copies of A, B and C have 16-byte aligned rows (leading
 // dimensions rounded up to 4 floats), whatever the host leading dimensions.
@@ -46,9 +47,15 @@ void panels_of(int M, int &P, int &rows) {
     P = (M + rows - 1) / rows;
 }
 
-// Columns of the first panel's left half (a multiple of the 128-column tile),
-// or N when the first panel is not split.
-int first_split(int P, int N) { return P >= 2 && N >= 512 ? (N / 2) / 128 * 128 : N; }
+// Column blocks of the first panel's product: with several panels, B is
+// copied and the first panel computed in NB blocks of columns (4 when
+// N >= 1024, 2 when N >= 512, else 1), block j covering [col_start(j),
+// col_start(j + 1)) with boundaries on the 128-column tile.
+constexpr int kMaxColBlocks = 4;
+int col_blocks(int P, int N) { return P >= 2 ? (N >= 1024 ? 4 : (N >= 512 ? 2 : 1)) : 1; }
+int col_start(int j, int NB, int N) {
+    return j >= NB ? N : static_cast<int>(static_cast<long long>(N) * j / NB) / 128 * 128;
+}
 
 struct HostLayout {
     size_t b, a, c, ws, ws_bytes, bytes;
@@ -68,14 +75,17 @@ HostLayout host_layout(int M, int N, int K) {
     // query inspects of its pointers, so any 16-byte aligned stand-in will do)
     const int first = rows < M ? rows : M;
     const int last = M - (P - 1) * rows;  // the last panel's rows (its schedule may differ)
-    const int n1 = first_split(P, N);
+    const int NB = col_blocks(P, N);
     const float *aligned = reinterpret_cast<const float *>(static_cast<uintptr_t>(256));
     const int K4 = static_cast<int>(pad4(K > 0 ? K : 1)), N4 = static_cast<int>(pad4(N));
     auto need_for = [&](int m, int n) { return sgemm_f32_workspace_size_for(m, n, K, aligned, K4, aligned, N4); };
-    const size_t need[4] = {need_for(first, N), need_for(last, N), need_for(first, n1),
-                            n1 < N ? need_for(first, N - n1) : 0};
-    size_t w = 0;
-    for (size_t x : need) w = x > w ? x : w;
+    size_t w = need_for(first, N);
+    const size_t w_last = need_for(last, N);
+    w = w_last > w ? w_last : w;
+    for (int j = 0; j < NB; ++j) {
+        const size_t x = need_for(first, col_start(j + 1, NB, N) - col_start(j, NB, N));
+        w = x > w ? x : w;
+    }
     l.ws_bytes = round256(w);
     l.bytes = l.ws + l.ws_bytes;
     return l;
@@ -151,13 +161,13 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     void *dW = ws + l.ws;
     int P = 0, rows = 0;
     panels_of(M, P, rows);
-    const int n1 = first_split(P, N);
+    const int NB = col_blocks(P, N);
     const int K4 = static_cast<int>(pad4(K)), N4 = static_cast<int>(pad4(N));  // fit: checked above
 
-    // events: start, B's left columns landed, all of B landed, all copied
-    // back, A panel p landed, C panel p computed
-    cudaEvent_t ev[4 + 2 * kMaxPanels] = {};
-    const int n_ev = 4 + 2 * P;
+    // events: start, all copied back, B's column block j landed, A panel p
+    // landed, C panel p computed
+    cudaEvent_t ev[2 + kMaxColBlocks + 2 * kMaxPanels] = {};
+    const int n_ev = 2 + NB + 2 * P;
     for (int i = 0; i < n_ev; ++i) {
         if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -165,8 +175,8 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
             return SGEMM_ERR_DEVICE;
         }
     }
-    cudaEvent_t &e_start = ev[0], &e_bl = ev[1], &e_b = ev[2], &e_done = ev[3];
-    cudaEvent_t *e_a = ev + 4, *e_c = ev + 4 + P;
+    cudaEvent_t &e_start = ev[0], &e_done = ev[1];
+    cudaEvent_t *e_b = ev + 2, *e_a = ev + 2 + NB, *e_c = ev + 2 + NB + P;
 
     auto fail = [&](int code) {
         (void)cudaGetLastError();
@@ -196,23 +206,25 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     if (cudaEventRecord(e_start, stream) != cudaSuccess || cudaStreamWaitEvent(h2d, e_start, 0) != cudaSuccess ||
         cudaStreamWaitEvent(d2h, e_start, 0) != cudaSuccess)
         return fail(SGEMM_ERR_LAUNCH);
-    // copy order: A panel 0, B's left columns, the rest of B, A panels 1..
-    if (!copy_a(0) || !copy_b(0, n1) || cudaEventRecord(e_bl, h2d) != cudaSuccess || (n1 < N && !copy_b(n1, N - n1)) ||
-        cudaEventRecord(e_b, h2d) != cudaSuccess)
-        return fail(SGEMM_ERR_LAUNCH);
+    // copy order: A panel 0, B's column blocks, A panels 1..
+    if (!copy_a(0)) return fail(SGEMM_ERR_LAUNCH);
+    for (int j = 0; j < NB; ++j) {
+        const int c0 = col_start(j, NB, N), c1 = col_start(j + 1, NB, N);
+        if (!copy_b(c0, c1 - c0) || cudaEventRecord(e_b[j], h2d) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
+    }
     for (int p = 1; p < P; ++p)
         if (!copy_a(p)) return fail(SGEMM_ERR_LAUNCH);
     for (int p = 0; p < P; ++p) {
         const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
         if (cudaStreamWaitEvent(stream, e_a[p], 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
-        if (p == 0 && n1 < N) {  // left half while B's right columns land
-            if (cudaStreamWaitEvent(stream, e_bl, 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
-            st = product(0, 0, n1);
-            if (st != SGEMM_OK) return fail(st);
-            if (cudaStreamWaitEvent(stream, e_b, 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
-            st = product(0, n1, N - n1);
+        if (p == 0) {  // block by block, each while the next block of B lands
+            for (int j = 0; j < NB; ++j) {
+                const int c0 = col_start(j, NB, N), c1 = col_start(j + 1, NB, N);
+                if (cudaStreamWaitEvent(stream, e_b[j], 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
+                st = product(0, c0, c1 - c0);
+                if (st != SGEMM_OK) return fail(st);
+            }
         } else {
-            if (p == 0 && cudaStreamWaitEvent(stream, e_b, 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
             st = product(p, 0, N);
         }
         if (st != SGEMM_OK) return fail(st);
