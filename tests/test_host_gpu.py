@@ -39,9 +39,9 @@ def test_pageable_strided_ragged(oracle_lib):
 def test_pinned_integer_exact(oracle_lib, M, N, K):
     """Pinned buffers across one to four row panels; integer inputs make every
     partial sum exact, so C must equal the oracle bit for bit.  With several
-    panels and N >= 512 the first panel is computed in two column halves
-    (2048x512: 256 + 256; 2500x1030: 512 + 518, rows not 16-byte aligned;
-    3000x700: 256 + 444)."""
+    panels and N >= 512 the first panel is computed in column blocks of B
+    (2048x512: 256 + 256; 2500x1030: 256 + 256 + 256 + 262, rows not 16-byte
+    aligned; 3000x700: 256 + 444)."""
     A = torch.from_numpy(synth.matrix(M, K, 93, 0, "int5")).pin_memory()
     B = torch.from_numpy(synth.matrix(K, N, 93, 1, "int5")).pin_memory()
     C = sg.sgemm_host(A, B)
