@@ -4,7 +4,8 @@
 // file adds the transfers around it.  A is copied in row panels on a copy
 // stream, and the product of each panel starts, on the caller's stream, as
 // soon as that panel and B have landed.  Each finished panel of C is copied
-// back on a second copy stream while the next panel computes.
+// back on a second copy stream while the next panel computes; the last panel
+// is cut in two so that the final copy back, which nothing hides, is short.
 //
 // Every row of C needs all of B, so B's copy would otherwise stall the first
 // product.  When there are several panels and N >= 512, the first panel's
@@ -38,13 +39,33 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 // 4 floats), so the products always run on the tensor-copy kernels.
 long long pad4(long long n) { return (n + 3) / 4 * 4; }
 
-// Row panels: P panels of `rows` rows (the last may be shorter).
-void panels_of(int M, int &P, int &rows) {
-    P = M / kPanelRows;
+// Row panels: up to kMaxPanels panels of `rows` rows (the last may be
+// shorter); with several panels, a last panel of at least 512 rows is cut in
+// two (on the 128-row tile), so that the copy back of the last panel of C,
+// which nothing hides, is half as long.  Panel p holds rows [start[p],
+// start[p + 1]).
+struct Panels {
+    int P;
+    int start[kMaxPanels + 2];
+    int rows(int p) const { return start[p + 1] - start[p]; }
+};
+Panels panels_of(int M) {
+    int P = M / kPanelRows;
     P = P < 1 ? 1 : (P > kMaxPanels ? kMaxPanels : P);
-    rows = (M + P - 1) / P;
+    int rows = (M + P - 1) / P;
     rows = (rows + 127) / 128 * 128;
     P = (M + rows - 1) / rows;
+    Panels pn;
+    for (int p = 0; p < P; ++p) pn.start[p] = p * rows;
+    pn.start[P] = M;
+    pn.P = P;
+    const int last = M - (P - 1) * rows;
+    if (P >= 2 && last >= 512) {
+        pn.start[P] = (P - 1) * rows + (last / 2 + 127) / 128 * 128;
+        pn.start[P + 1] = M;
+        pn.P = P + 1;
+    }
+    return pn;
 }
 
 // Column blocks of the first panel's product: with several panels, B is
@@ -61,8 +82,7 @@ struct HostLayout {
     size_t b, a, c, ws, ws_bytes, bytes;
 };
 HostLayout host_layout(int M, int N, int K) {
-    int P = 0, rows = 0;
-    panels_of(M, P, rows);
+    const Panels pn = panels_of(M);
     HostLayout l;
     l.b = 0;
     l.a = round256(static_cast<size_t>(K) * pad4(N) * 4);
@@ -73,17 +93,17 @@ HostLayout host_layout(int M, int N, int K) {
     // schedule's words and, where it pays, the k-major copy of the panel of
     // A (the device copies have 16-byte aligned rows, which is all the size
     // query inspects of its pointers, so any 16-byte aligned stand-in will do)
-    const int first = rows < M ? rows : M;
-    const int last = M - (P - 1) * rows;  // the last panel's rows (its schedule may differ)
-    const int NB = col_blocks(P, N);
+    const int NB = col_blocks(pn.P, N);
     const float *aligned = reinterpret_cast<const float *>(static_cast<uintptr_t>(256));
     const int K4 = static_cast<int>(pad4(K > 0 ? K : 1)), N4 = static_cast<int>(pad4(N));
     auto need_for = [&](int m, int n) { return sgemm_f32_workspace_size_for(m, n, K, aligned, K4, aligned, N4); };
-    size_t w = need_for(first, N);
-    const size_t w_last = need_for(last, N);
-    w = w_last > w ? w_last : w;
+    size_t w = 0;
+    for (int p = 0; p < pn.P; ++p) {
+        const size_t x = need_for(pn.rows(p), N);
+        w = x > w ? x : w;
+    }
     for (int j = 0; j < NB; ++j) {
-        const size_t x = need_for(first, col_start(j + 1, NB, N) - col_start(j, NB, N));
+        const size_t x = need_for(pn.rows(0), col_start(j + 1, NB, N) - col_start(j, NB, N));
         w = x > w ? x : w;
     }
     l.ws_bytes = round256(w);
@@ -159,14 +179,14 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     float *dA = reinterpret_cast<float *>(ws + l.a);
     float *dC = reinterpret_cast<float *>(ws + l.c);
     void *dW = ws + l.ws;
-    int P = 0, rows = 0;
-    panels_of(M, P, rows);
+    const Panels pn = panels_of(M);
+    const int P = pn.P;
     const int NB = col_blocks(P, N);
     const int K4 = static_cast<int>(pad4(K)), N4 = static_cast<int>(pad4(N));  // fit: checked above
 
     // events: start, all copied back, B's column block j landed, A panel p
     // landed, C panel p computed
-    cudaEvent_t ev[2 + kMaxColBlocks + 2 * kMaxPanels] = {};
+    cudaEvent_t ev[2 + kMaxColBlocks + 2 * (kMaxPanels + 1)] = {};
     const int n_ev = 2 + NB + 2 * P;
     for (int i = 0; i < n_ev; ++i) {
         if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
@@ -189,7 +209,7 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
                                            static_cast<size_t>(nc) * 4, K, cudaMemcpyHostToDevice, h2d) == cudaSuccess;
     };
     auto copy_a = [&](int p) {
-        const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
+        const int r0 = pn.start[p], nr = pn.rows(p);
         return (K == 0 || cudaMemcpy2DAsync(dA + static_cast<size_t>(r0) * K4, static_cast<size_t>(K4) * 4,
                                             A + static_cast<size_t>(r0) * lda, static_cast<size_t>(lda) * 4,
                                             static_cast<size_t>(K) * 4, nr, cudaMemcpyHostToDevice,
@@ -198,7 +218,7 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     };
     // columns [c0, c0 + nc) of panel p's product
     auto product = [&](int p, int c0, int nc) {
-        const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
+        const int r0 = pn.start[p], nr = pn.rows(p);
         return sgemm_f32_ws(nr, nc, K, dA + static_cast<size_t>(r0) * K4, K4 > 0 ? K4 : 1, dB + c0, N4,
                             dC + static_cast<size_t>(r0) * N4 + c0, N4, dW, l.ws_bytes, stream);
     };
@@ -215,7 +235,7 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     for (int p = 1; p < P; ++p)
         if (!copy_a(p)) return fail(SGEMM_ERR_LAUNCH);
     for (int p = 0; p < P; ++p) {
-        const int r0 = p * rows, nr = (M - r0) < rows ? (M - r0) : rows;
+        const int r0 = pn.start[p], nr = pn.rows(p);
         if (cudaStreamWaitEvent(stream, e_a[p], 0) != cudaSuccess) return fail(SGEMM_ERR_LAUNCH);
         if (p == 0) {  // block by block, each while the next block of B lands
             for (int j = 0; j < NB; ++j) {
