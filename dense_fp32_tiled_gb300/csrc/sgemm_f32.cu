@@ -402,11 +402,14 @@ __device__ __forceinline__ void acc16_zero(Acc16 &acc) {
 }
 
 // Accumulates the product of C tile (m0, n0) over K tiles [kt0, kt1) into
-// acc, with p.A the k-major copy At (K x M, row stride p.lda).  The ring,
-// its mbarriers and the iteration structure are those of the AT branch of
-// mma_k_range (STAGES_AT deep; iteration kt waits for tile kt, barrier,
-// issues tile kt + STAGES_AT - 1, runs 16 k steps); only the thread tile
-// differs.  `pipe` numbers the loads as there.
+// acc, with A given as its k-major copy At (K x M; maps.a describes it).
+// Each stage of a STAGES_AT-deep ring receives a 16 x 128 box of At and a
+// 16 x 128 box of B by tensor copy, completing on the stage's mbarrier.
+// Iteration kt waits for tile kt, then a barrier (every thread has finished
+// tile kt-1, whose stage is free), issues tile kt + STAGES_AT - 1 into that
+// stage and runs 16 k steps.  `pipe` counts the tiles this CTA has loaded
+// before this range (load u goes to stage u % STAGES_AT, whose mbarrier
+// completes phase u / STAGES_AT), as in mma_k_range.
 __device__ __forceinline__ void kmajor16_k_range(const Maps &maps, const int m0, const int n0, const int kt0,
                                                  const int kt1, uint32_t &pipe, float *smem, const uint32_t bars,
                                                  Acc16 &acc) {
