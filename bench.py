@@ -2,9 +2,10 @@
 """Benchmark of the tiled FP32 matrix multiply C = A.B on GB300.
 
 One step = one sgemm_f32_ws call over the workload (the whole path: argument
-checks, the schedule choice, one kernel launch with the copy pipeline, FMA
-main loop, split fix-up where used, and epilogue; the workspace is
-allocated once, outside the timed region).
+checks, the schedule choice, the operand copies that pay -- at 4096^3 the
+transpose of A into its k-major copy --, the product kernels with their copy
+pipelines, FMA main loops, split fix-up where used, and epilogues; the
+workspace is allocated once, outside the timed region).
 Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
@@ -343,7 +344,8 @@ def main():
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
     # the library's balanced entry point, with the workspace it asks for
-    # (for these operands: room to repack rows that are not 16-byte aligned)
+    # (for these operands: room for the copies that pay -- the k-major copy of
+    # A at large N, repacked rows where they are not 16-byte aligned)
     ws_bytes = sg.workspace_size_for(w.M, w.N, w.K, A.data_ptr(), w.lda, B.data_ptr(), w.ldb)
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
