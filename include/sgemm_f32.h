@@ -121,8 +121,9 @@ int sgemm_f32(int M, int N, int K,
  *      At = A^T (K rows of M floats, row stride M rounded up to 4) plus the
  *      repacked B below if B needs it, the call first transposes A into At
  *      (the transpose_f32 kernel) and runs kernels that load k-major A tiles
- *      straight into the layout the FMA loop reads: no transpose in shared
- *      memory and no shared store in the K loop.  The summation order is
+ *      straight into the layout the FMA loop reads (128-thread CTAs, 8 x 16
+ *      register tiles): no transpose in shared memory and no shared store in
+ *      the K loop.  The summation order is
  *      unchanged, so the result equals the call without the copy bit for bit.
  *   repacked rows: otherwise, when A's or B's rows are not 16-byte aligned
  *      and the workspace has room for the schedule plus a copy of that
@@ -158,7 +159,7 @@ int sgemm_f32_ws_schedule(int M, int N, int K,
                           int *kind, long long *words);
 
 /* Workspace bytes sgemm_f32_ws can use for this shape on the current device
- * (0 for an empty or invalid shape), not counting operand repacking.  Reads
+ * (0 for an empty or invalid shape), not counting the operand copies.  Reads
  * device attributes only; with no usable device it returns the size of the
  * flags-only schedule. */
 size_t sgemm_f32_workspace_size(int M, int N, int K);
