@@ -8,7 +8,7 @@ pipelines, FMA main loops, split fix-up where used, and epilogues; the
 workspace is allocated once, outside the timed region).
 Prints ONE JSON line (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME | --shape M,N,K]
                   [--impl ours|reference]
   python bench.py --op transpose [--rows R --cols C] [--layout fast|padded|unpadded|swizzled]
 
@@ -46,6 +46,9 @@ def _args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K: a dense product with uniform[-1,1] inputs from seed 0 instead of a named workload "
+                         "(for profiling other shapes)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -68,8 +71,11 @@ def _measured_peaks():
     return {}
 
 
-def _workload(name):
+def _workload(name, shape=None):
     from dense_fp32_tiled_gb300 import synth
+    if shape:
+        M, N, K = (int(x) for x in shape.split(","))
+        return synth.Workload(f"sgemm_{M}x{N}x{K}_uniform", M, N, K, K, N, N, "uniform", 1.0, 0, (0, 1), "full")
     return synth.WORKLOADS[name or synth.HEADLINE]
 
 
@@ -143,22 +149,21 @@ class ClockSampler:
                 "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
-def _traffic_from_profile(profile: str, stamp: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the kernel as built now (same kernel source stamp); else None."""
-    p = os.path.join(ROOT, "profiles", profile)
+def _traffic(key: str):
+    """DRAM bytes per launch recorded in profiles/dram_traffic.json for one
+    benchmarked kernel, if it was captured on the kernel as built now (same
+    source stamp); else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
-    vals = {}
     with open(p) as f:
-        for line in f:
-            if line.startswith("<!-- bench:"):
-                for kv in line.strip()[len("<!-- bench:"):-3].split():
-                    k, _, v = kv.partition("=")
-                    vals[k] = v
-    if vals.get("source_stamp") == stamp and "dram_bytes_per_launch" in vals:
-        return int(vals["dram_bytes_per_launch"])
-    return None
+        e = json.load(f).get("entries", {}).get(key)
+    if not e:
+        return None
+    from dense_fp32_tiled_gb300 import build as lib_build
+    if lib_build.kernel_stamp(e["sources"]) != e.get("source_stamp"):
+        return None
+    return int(e["dram_bytes_per_launch"])
 
 
 def cpu_baseline(w, seconds: float):
@@ -189,7 +194,7 @@ def run_reference(a):
         return
     import oracle
     from dense_fp32_tiled_gb300 import synth
-    w = _workload(a.workload)
+    w = _workload(a.workload, a.shape)
     oracle.build()
     A = synth.matrix(w.M, w.K, w.seed, w.ids[0], w.kind, w.sigma)
     B = synth.matrix(w.K, w.N, w.seed, w.ids[1], w.kind, w.sigma)
@@ -293,8 +298,7 @@ def run_transpose(a):
     gbs = nbytes / (ms / 1e3) / 1e9
     peak = float(_measured_peaks().get("hbm_gbs") or 6800.0)
     # DRAM bytes per launch from the committed ncu summary (taken on the 8192 x 8192 vector path)
-    traffic = (_traffic_from_profile("transpose_f32_8192.md", _stamp(TRANSPOSE_SOURCES))
-               if a.layout == "fast" and (rows, cols) == (8192, 8192) else None)
+    traffic = _traffic("transpose_f32_8192") if a.layout == "fast" and (rows, cols) == (8192, 8192) else None
     line = {"metric": "FP32 transpose GB/s (bytes read + written)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -333,7 +337,7 @@ def main():
     from dense_fp32_tiled_gb300 import synth
     sg.load_library()
 
-    w = _workload(a.workload)
+    w = _workload(a.workload, a.shape)
     dev = torch.device("cuda", local)
     A_h, B_h = w.inputs(ld_buffers=True)
     A = torch.from_numpy(A_h).to(dev)
@@ -381,11 +385,13 @@ def main():
         torch.cuda.synchronize(dev)
         clk.t0 = time.time()
         t_wall = time.perf_counter()
+        torch.cuda.nvtx.range_push("bench: timed steps (sgemm_f32_ws)")
         for i in range(a.steps):
             flush.zero_()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
@@ -418,8 +424,10 @@ def main():
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        torch.cuda.nvtx.range_push("bench: end-to-end steps (sgemm_f32_host)")
         for _ in range(e_steps):
             host_step()
+        torch.cuda.nvtx.range_pop()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms, e_value = combine_ranks(e0.elapsed_time(e1) / e_steps, flops, world, dev)
@@ -436,8 +444,7 @@ def main():
     # the committed DRAM counters were captured on the 4096^3 product only
     headline = w.name == synth.HEADLINE
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": (_traffic_from_profile("sgemm_f32_tiled_4096.md", _stamp(SIMT_SOURCES)) if headline
-                            else None),
+                "traffic": _traffic("sgemm_f32_4096") if headline else None,
                 "peak_basis": f"{sms} SMs x 128 FP32 FMA/clk x 2 FLOP x {sm_max:.0f} MHz (max SM clock)"}
     if sched_kind & 3 == 3:
         dp, tail = (("sgemm_f32_kmajor_kernel", "sgemm_f32_kmajor_tail_kernel") if sched_kind & 16 else
@@ -474,11 +481,13 @@ def main():
         t_starts = [torch.cuda.Event(enable_timing=True) for _ in range(tc_steps)]
         t_ends = [torch.cuda.Event(enable_timing=True) for _ in range(tc_steps)]
         torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_push("bench: tensor-core variant steps (sgemm_f32_3xtf32)")
         for i in range(tc_steps):
             flush.zero_()
             t_starts[i].record(stream)
             tc_step()
             t_ends[i].record(stream)
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(dev)
         tc_ms, tc_value = combine_ranks(statistics.mean(x.elapsed_time(y) for x, y in zip(t_starts, t_ends)),
                                         flops, world, dev)
@@ -489,7 +498,7 @@ def main():
               "gpu_launches": 2 * tc_steps,
               "roofline": {"bound": "tensor", "achieved": tc_achieved, "peak": tf32_peak, "unit": "TFLOP/s",
                            "frac": tc_achieved / tf32_peak,
-                           "traffic": _traffic_from_profile("sgemm_3xtf32_4096.md", _stamp(TC_SOURCES)),
+                           "traffic": _traffic("sgemm_3xtf32_4096") if headline else None,
                            "peak_basis": "TF32 dense = measured bf16 burst x 1.1/2.25 (nominal ratio); "
                                          "achieved counts the 3 TF32 products per FP32 product"}}
 
@@ -508,16 +517,6 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
-
-
-SIMT_SOURCES = ("sgemm_f32.cu", "smem_layout.cuh", "transpose_f32.cu")  # the headline step runs all three
-TC_SOURCES = ("sgemm_3xtf32.cu",)
-TRANSPOSE_SOURCES = ("transpose_f32.cu",)
-
-
-def _stamp(names):
-    from dense_fp32_tiled_gb300 import build as lib_build
-    return lib_build.kernel_stamp(names)
 
 
 if __name__ == "__main__":

@@ -13,7 +13,8 @@ import re
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libsgemm_f32.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "sgemm_f32.h")
-HEADER_PATHS = [HEADER_PATH, os.path.join(os.path.dirname(_PKG), "include", "transpose_f32.h")]
+HEADER_PATHS = [HEADER_PATH, os.path.join(os.path.dirname(_PKG), "include", "transpose_f32.h"),
+                os.path.join(os.path.dirname(_PKG), "include", "smem_bank_probe.h")]
 
 SGEMM_OK = 0
 _lib = None
@@ -79,6 +80,12 @@ def load_library():
     lib.sgemm_f32_smem_shape.restype = i32
     lib.sgemm_f32_smem_request.argtypes = [i32, i32, i32, i32, i64p, ip]
     lib.sgemm_f32_smem_request.restype = i32
+    lib.smem_bank_stride_probe.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_longlong)]
+    lib.smem_bank_stride_probe.restype = i32
+    lib.smem_bank_pattern_probe.argtypes = [i32, ctypes.POINTER(ctypes.c_int), i32, i32,
+                                            ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
+    lib.smem_bank_pattern_probe.restype = i32
     _lib = lib
     return lib
 
@@ -89,7 +96,7 @@ def declared_functions() -> list[str]:
     for path in HEADER_PATHS:
         with open(path) as f:
             text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
-        names |= set(re.findall(r"\b((?:sgemm|transpose)_f32\w*)\s*\(", text))
+        names |= set(re.findall(r"\b((?:sgemm|transpose)_f32\w*|smem_bank_\w+)\s*\(", text))
     return sorted(names)
 
 
@@ -408,3 +415,26 @@ def transpose(x, out=None, stream=None):
     if st != 0:
         raise RuntimeError(f"transpose_f32 failed with status {st}: {transpose_status_string(st)}")
     return out
+
+
+# ---- shared-memory stride sweep ---------------------------------------------
+def bank_stride_probe(stride: int, op: str = "load", warps: int = 8, iters: int = 4096):
+    """(cycles per warp-wide access, checksum) of smem_bank_stride_probe."""
+    cyc, chk = ctypes.c_double(), ctypes.c_longlong()
+    st = load_library().smem_bank_stride_probe(int(stride), {"load": 0, "store": 1}[op], int(warps), int(iters),
+                                               ctypes.byref(cyc), ctypes.byref(chk))
+    if st != 0:
+        raise RuntimeError(f"smem_bank_stride_probe failed with status {st}")
+    return cyc.value, chk.value
+
+
+def bank_pattern_probe(width_bytes: int, lane_word, warps: int = 8, iters: int = 4096):
+    """(cycles per warp-wide load, checksum) of smem_bank_pattern_probe for the
+    32 word offsets ``lane_word``."""
+    arr = (ctypes.c_int * 32)(*[int(x) for x in lane_word])
+    cyc, chk = ctypes.c_double(), ctypes.c_longlong()
+    st = load_library().smem_bank_pattern_probe(int(width_bytes), arr, int(warps), int(iters), ctypes.byref(cyc),
+                                                ctypes.byref(chk))
+    if st != 0:
+        raise RuntimeError(f"smem_bank_pattern_probe failed with status {st}")
+    return cyc.value, chk.value

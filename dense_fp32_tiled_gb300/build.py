@@ -75,7 +75,7 @@ def build(force: bool = False, quiet: bool = True) -> str:
     cmds = [[_nvcc(), *FLAGS, "-c", cu, "-o", obj] for cu, obj in zip(cus, objs)]
     procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True) for c in cmds]
     outs = [p.communicate() for p in procs]
-    link = [_nvcc(), *ARCH, "-shared", *objs, "-o", tmp]
+    link = [_nvcc(), *ARCH, "-shared", *objs, "-o", tmp, "-ldl"]  # NVTX3 loads a profiler's hooks with dlopen
     log = ["\n".join([" ".join(c), o + e]) for c, (o, e) in zip(cmds, outs)]
     failed = any(p.returncode != 0 for p in procs)
     if not failed:

@@ -30,6 +30,8 @@
 #include <mutex>
 #include <utility>
 
+#include "ctx_key.cuh"
+#include "nvtx_range.cuh"
 #include "sgemm_f32.h"
 
 namespace {
@@ -584,13 +586,18 @@ constexpr int SK_FIXUP_BLOCKS = 6;
 std::mutex g_setup_mutex;
 int g_setup_state[64];
 int g_max_pairs[64];
+unsigned long long g_setup_ctx[64];  // id of the CUDA context the set-up was made in
 
 // Per device: the architecture check, the shared-memory opt-in and the number
 // of CTA pairs that fit on the GPU at once (the persistent grid).
 int setup(int dev) {
     if (dev < 0 || dev >= 64) return SGEMM_ERR_DEVICE;
+    unsigned long long ctx = 0;
+    const bool known = sg_ctx::current_id(dev, &ctx);
     std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (known && g_setup_state[dev] != 0 && g_setup_ctx[dev] != ctx) g_setup_state[dev] = 0;  // a new context
     if (g_setup_state[dev] == 0) {
+        g_setup_ctx[dev] = ctx;
         int major = 0, minor = 0, sms = 0, st = SGEMM_OK;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -737,8 +744,11 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, co
         (void)cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
     }
-    split_kernel<<<static_cast<unsigned>(split_blocks), dim3(32, 8), 0, stream>>>(
-        A, lda, B, ldb, M, N, K, Kp, a_hi, a_lo, bt_hi, bt_lo, a_blocks, b_tiles_k);
+    {
+        sg_nvtx::Range r("sgemm_f32_3xtf32: split");
+        split_kernel<<<static_cast<unsigned>(split_blocks), dim3(32, 8), 0, stream>>>(
+            A, lda, B, ldb, M, N, K, Kp, a_hi, a_lo, bt_hi, bt_lo, a_blocks, b_tiles_k);
+    }
     if (cudaPeekAtLastError() != cudaSuccess) {
         (void)cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
@@ -790,6 +800,7 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, co
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
+    sg_nvtx::Range r_mma("sgemm_f32_3xtf32: MMA kernel");
     if (cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel, maps, C, ldc, M, N, pl, counts, partials, vc, timeout) !=
         cudaSuccess) {
         (void)cudaGetLastError();

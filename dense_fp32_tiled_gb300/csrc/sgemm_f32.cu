@@ -27,10 +27,13 @@
 
 #include <climits>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
 
+#include "ctx_key.cuh"
+#include "nvtx_range.cuh"
 #include "sgemm_f32.h"
 #include "smem_layout.cuh"
 #include "transpose_f32.h"
@@ -410,6 +413,10 @@ __device__ __forceinline__ void acc16_zero(Acc16 &acc) {
 // stage and runs 16 k steps.  `pipe` counts the tiles this CTA has loaded
 // before this range (load u goes to stage u % STAGES_AT, whose mbarrier
 // completes phase u / STAGES_AT), as in mma_k_range.
+// With DRAIN (a diagnostic kernel, never dispatched by default) one tile is in
+// flight at a time, issued after the k steps of the one before: no copy
+// writes shared memory while the fragments are read.
+template <bool DRAIN = false>
 __device__ __forceinline__ void kmajor16_k_range(const Maps &maps, const int m0, const int n0, const int kt0,
                                                  const int kt1, uint32_t &pipe, float *smem, const uint32_t bars,
                                                  Acc16 &acc) {
@@ -427,14 +434,18 @@ __device__ __forceinline__ void kmajor16_k_range(const Maps &maps, const int m0,
     };
     const int ra = frag16_row0(tid);
     const int cb = frag16_col0(tid);
+    if constexpr (DRAIN) {
+        if (kt0 < kt1) issue_tile(kt0);
+    } else {
 #pragma unroll
-    for (int s = 0; s < STAGES_AT - 1; ++s)
-        if (kt0 + s < kt1) issue_tile(kt0 + s);
+        for (int s = 0; s < STAGES_AT - 1; ++s)
+            if (kt0 + s < kt1) issue_tile(kt0 + s);
+    }
     for (int kt = kt0; kt < kt1; ++kt) {
         const uint32_t u = u0 + kt;
         mbar_wait_bounded(bars + 8 * (u % STAGES_AT), (u / STAGES_AT) & 1u, kWaitLimit, &g_copy_timeout);
         __syncthreads();
-        if (kt + STAGES_AT - 1 < kt1) issue_tile(kt + STAGES_AT - 1);
+        if (!DRAIN && kt + STAGES_AT - 1 < kt1) issue_tile(kt + STAGES_AT - 1);
         const uint32_t stage = u % STAGES_AT;
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
@@ -454,6 +465,10 @@ __device__ __forceinline__ void kmajor16_k_range(const Maps &maps, const int m0,
 #pragma unroll
                 for (int r = 0; r < TM; ++r) acc.c[r][j] = __ffma2_rn(make_float2(a[r], a[r]), bp[j], acc.c[r][j]);
             }
+        }
+        if constexpr (DRAIN) {
+            __syncthreads();  // every thread is done with this stage before the next copy lands
+            if (kt + 1 < kt1) issue_tile(kt + 1);
         }
     }
     pipe += static_cast<uint32_t>(kt1 > kt0 ? kt1 - kt0 : 0);
@@ -516,7 +531,9 @@ __device__ __forceinline__ void add_partial16(const float *slot, Acc16 &acc) {
     }
 }
 
-// Data-parallel schedule on the k-major copy of A: one CTA per C tile.
+// Data-parallel schedule on the k-major copy of A: one CTA per C tile.  The
+// DRAIN instantiation is the drained-ring diagnostic (see kmajor16_k_range).
+template <bool DRAIN = false>
 __global__ void __launch_bounds__(NT16, 2) sgemm_f32_kmajor_kernel(const Problem p, const __grid_constant__ Maps maps) {
     extern __shared__ float smem_raw[];
     __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
@@ -530,7 +547,7 @@ __global__ void __launch_bounds__(NT16, 2) sgemm_f32_kmajor_kernel(const Problem
     Acc16 acc;
     acc16_zero(acc);
     uint32_t pipe = 0;
-    kmajor16_k_range(maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
+    kmajor16_k_range<DRAIN>(maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
     store_tile16<false>(p, tm * BM, tn * BN, acc);
 }
 
@@ -586,6 +603,52 @@ __device__ __forceinline__ void raise_flag(unsigned *flag) {
     }
 }
 
+// The segments of one CTA of the stream-K schedules (below): first whole
+// data-parallel tiles (tile c, c + G, ...), then its share of the (tile,
+// K tile) iterations of the remaining tiles, cut at tile boundaries.
+struct SkWalk {
+    const Problem &p;  // the kernel parameter (read from parameter space, not held in registers)
+    int KT, G, dp_tiles;
+    long long total_iters, base, it, it_end;
+    int dp_lin;
+
+    __device__ __forceinline__ SkWalk(const Problem &prob, int dp) : p(prob) {
+        KT = (p.K + BK - 1) / BK;
+        G = gridDim.x;
+        dp_tiles = dp;
+        total_iters = static_cast<long long>(p.tiles_m * p.tiles_n - dp_tiles) * KT;
+        base = static_cast<long long>(dp_tiles) * KT;
+        it_end = base + total_iters * (blockIdx.x + 1) / G;
+        it = base + total_iters * blockIdx.x / G;
+        dp_lin = blockIdx.x;
+    }
+    // The next segment: tile lin (linear tile index), its C tile (tm, tn) and
+    // K tiles [k0, k1); false when the CTA is done.
+    __device__ __forceinline__ bool next(int &lin, int &tm, int &tn, int &k0, int &k1) {
+        if (dp_lin < dp_tiles) {
+            lin = dp_lin;
+            k0 = 0;
+            k1 = KT;
+            dp_lin += G;
+        } else if (it < it_end) {
+            lin = static_cast<int>(it / KT);
+            k0 = static_cast<int>(it % KT);
+            k1 = static_cast<int>(k0 + (it_end - it) < KT ? k0 + (it_end - it) : KT);
+            it += k1 - k0;
+        } else {
+            return false;
+        }
+        tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
+        return true;
+    }
+    // The last CTA holding a part of tile lin: the owner adds the parts of
+    // CTAs blockIdx.x + 1 .. last_part(lin).
+    __device__ __forceinline__ int last_part(int lin) const {
+        const long long last = static_cast<long long>(lin + 1) * KT - 1 - base;
+        return static_cast<int>(((last + 1) * G + total_iters - 1) / total_iters - 1);
+    }
+};
+
 // Stream-K schedule.  A persistent, co-resident grid of G CTAs first computes
 // tiles 0 .. dp_tiles-1 one whole tile at a time (tile c, c+G, ...: CTAs
 // running together work on neighbouring tiles, which keeps A and B panels in
@@ -615,38 +678,16 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
     const uint32_t bars = smem_u32(bar_mem);
     init_bars<TMA>(bars);
     uint32_t pipe = 0;
-    const int KT = (p.K + BK - 1) / BK;
-    const int T = p.tiles_m * p.tiles_n;
-    const int G = gridDim.x;
-    unsigned *error = flags + (partials ? G : T);
-    const long long total_iters = static_cast<long long>(T - dp_tiles) * KT;
-    const long long base = static_cast<long long>(dp_tiles) * KT;
-    const long long it_end = base + total_iters * (blockIdx.x + 1) / G;
-    long long it = base + total_iters * blockIdx.x / G;
-    int dp_lin = blockIdx.x;
+    SkWalk w(p, dp_tiles);
+    unsigned *error = flags + (partials ? gridDim.x : p.tiles_m * p.tiles_n);
     // One loop over segments (whole data-parallel tiles first, then this CTA's
     // stream-K range cut at tile boundaries), so the main loop is inlined once.
-    for (;;) {
-        int lin, k0, k1;
-        if (dp_lin < dp_tiles) {
-            lin = dp_lin;
-            k0 = 0;
-            k1 = KT;
-            dp_lin += G;
-        } else if (it < it_end) {
-            lin = static_cast<int>(it / KT);
-            k0 = static_cast<int>(it % KT);
-            k1 = static_cast<int>(k0 + (it_end - it) < KT ? k0 + (it_end - it) : KT);
-            it += k1 - k0;
-        } else {
-            break;
-        }
-        int tm, tn;
-        tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
+    int lin, tm, tn, k0, k1;
+    while (w.next(lin, tm, tn, k0, k1)) {
         Acc acc;
         acc_zero(acc);
         mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
-        if (k0 == 0 && k1 == KT) {
+        if (k0 == 0 && k1 == w.KT) {
             store_tile<false>(p, tm * BM, tn * BN, acc);
         } else if (k0 > 0) {  // hand the partial sums for k >= k0 over to the owner
             if (partials) {
@@ -657,8 +698,7 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
                 raise_flag(flags + lin);
             }
         } else if (partials) {  // owner: add the parts of CTAs blockIdx.x+1 .. c_last
-            const long long last = static_cast<long long>(lin + 1) * KT - 1 - base;
-            const int c_last = static_cast<int>(((last + 1) * G + total_iters - 1) / total_iters - 1);
+            const int c_last = w.last_part(lin);
             for (int c = blockIdx.x + 1; c <= c_last; ++c) {
                 wait_flag(flags + c, error);
                 add_partial(partials + static_cast<size_t>(c) * (BM * BN), acc);
@@ -687,36 +727,14 @@ sgemm_f32_kmajor_streamk_kernel(const Problem p, const __grid_constant__ Maps ma
     const uint32_t bars = smem_u32(bar_mem);
     init_bars<true>(bars);
     uint32_t pipe = 0;
-    const int KT = (p.K + BK - 1) / BK;
-    const int T = p.tiles_m * p.tiles_n;
-    const int G = gridDim.x;
-    unsigned *error = flags + (partials ? G : T);
-    const long long total_iters = static_cast<long long>(T - dp_tiles) * KT;
-    const long long base = static_cast<long long>(dp_tiles) * KT;
-    const long long it_end = base + total_iters * (blockIdx.x + 1) / G;
-    long long it = base + total_iters * blockIdx.x / G;
-    int dp_lin = blockIdx.x;
-    for (;;) {
-        int lin, k0, k1;
-        if (dp_lin < dp_tiles) {
-            lin = dp_lin;
-            k0 = 0;
-            k1 = KT;
-            dp_lin += G;
-        } else if (it < it_end) {
-            lin = static_cast<int>(it / KT);
-            k0 = static_cast<int>(it % KT);
-            k1 = static_cast<int>(k0 + (it_end - it) < KT ? k0 + (it_end - it) : KT);
-            it += k1 - k0;
-        } else {
-            break;
-        }
-        int tm, tn;
-        tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
+    SkWalk w(p, dp_tiles);
+    unsigned *error = flags + (partials ? gridDim.x : p.tiles_m * p.tiles_n);
+    int lin, tm, tn, k0, k1;
+    while (w.next(lin, tm, tn, k0, k1)) {
         Acc16 acc;
         acc16_zero(acc);
         kmajor16_k_range(maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
-        if (k0 == 0 && k1 == KT) {
+        if (k0 == 0 && k1 == w.KT) {
             store_tile16<false>(p, tm * BM, tn * BN, acc);
         } else if (k0 > 0) {  // hand the partial sums for k >= k0 over to the owner
             if (partials) {
@@ -727,8 +745,7 @@ sgemm_f32_kmajor_streamk_kernel(const Problem p, const __grid_constant__ Maps ma
                 raise_flag(flags + lin);
             }
         } else if (partials) {  // owner: add the parts of CTAs blockIdx.x+1 .. c_last
-            const long long last = static_cast<long long>(lin + 1) * KT - 1 - base;
-            const int c_last = static_cast<int>(((last + 1) * G + total_iters - 1) / total_iters - 1);
+            const int c_last = w.last_part(lin);
             for (int c = blockIdx.x + 1; c <= c_last; ++c) {
                 wait_flag(flags + c, error);
                 add_partial16(partials + static_cast<size_t>(c) * (BM * BN), acc);
@@ -883,8 +900,9 @@ __global__ void wait_selftest_kernel(int which, unsigned limit, unsigned *status
 // ---------------------------------------------------------------------------
 
 constexpr int kMaxDevices = 64;
-// (VA, VB) in {4, 1} x {4, 2, 1} with cp.async; (4, 4) with TMA; and the
-// kernels on the k-major copy of A (8 x 16 register tiles, NT16 threads).
+// Kernel variants: (VA, VB) in {4, 1} x {4, 2, 1} with cp.async (0..5) and
+// (4, 4) with TMA (6), for the 8 x 8 row-major kernels; 7 is the 8 x 16
+// kernel on the k-major copy of A.
 constexpr int kVariants = 8;
 constexpr int kTmaVariant = 6;
 constexpr int kAtVariant = 7;
@@ -894,7 +912,7 @@ const DpKernel kDp[kVariants] = {
     sgemm_f32_tiled_kernel<4, 4, false>, sgemm_f32_tiled_kernel<4, 2, false>,
     sgemm_f32_tiled_kernel<4, 1, false>, sgemm_f32_tiled_kernel<1, 4, false>,
     sgemm_f32_tiled_kernel<1, 2, false>, sgemm_f32_tiled_kernel<1, 1, false>,
-    sgemm_f32_tiled_kernel<4, 4, true>,  sgemm_f32_kmajor_kernel};
+    sgemm_f32_tiled_kernel<4, 4, true>,  sgemm_f32_kmajor_kernel<false>};
 const SkKernel kSk[kVariants] = {
     sgemm_f32_streamk_kernel<4, 4, false>, sgemm_f32_streamk_kernel<4, 2, false>,
     sgemm_f32_streamk_kernel<4, 1, false>, sgemm_f32_streamk_kernel<1, 4, false>,
@@ -903,9 +921,84 @@ const SkKernel kSk[kVariants] = {
 using TailKernel = void (*)(Problem, Maps, int, int, unsigned *, float *);
 // tensor-copy variants only: [0] A row-major, [1] A k-major (8 x 16 tiles)
 const TailKernel kTail[2] = {sgemm_f32_tail_kernel<4, 4, true>, sgemm_f32_kmajor_tail_kernel};
+// The drained-ring diagnostic kernel of the k-major variant (one CTA per
+// tile; SGEMM_F32_TUNE drain=on).
+const DpKernel kDrained[1] = {sgemm_f32_kmajor_kernel<true>};
+DpKernel dp_kernel(int v, bool drain) { return drain && v == kAtVariant ? kDrained[0] : kDp[v]; }
 bool is_tma(int v) { return v == kTmaVariant || v == kAtVariant; }
 // threads per CTA of variant v's kernels
 unsigned threads(int v) { return v == kAtVariant ? NT16 : NT; }
+
+// ---- tuning overrides --------------------------------------------------
+// SGEMM_F32_TUNE = "key=value,key=value" (read once, at the first call) forces
+// choices the cost models otherwise make, for tuning sweeps without a
+// rebuild.  Keys (any other key or value is ignored; "auto" = the default):
+//   kernels  = rowmajor8 | kmajor16 : the 8 x 8 row-major kernels only, or
+//              the k-major copy of A whenever the workspace has room;
+//   schedule = 0 | 1 | 2 | 3 : the schedule of sgemm_f32_ws when the
+//              workspace has room for it (3 needs tensor copies);
+//   parts    = 2 .. 16 : K parts of each split-tail tile;
+//   drain    = on : a diagnostic: the one-CTA-per-tile grid of the k-major
+//              kernels keeps one tile in flight and issues
+//              it only after the k steps of the one before, so no copy
+//              writes shared memory while fragments are read (slow; it
+//              exists to count shared-memory bank conflicts without the
+//              copy engines' concurrent writes).
+// A forced choice changes only how the work is split, so the product stays
+// within the same FP32 bound (not bit for bit the default's).
+struct Tune {
+    int kernels = -1;   // -1 auto, 0 rowmajor8, 1 kmajor16
+    int schedule = -1;
+    int parts = -1;
+    bool drain = false; // the drained-ring diagnostic kernels
+};
+const Tune &tune() {
+    static Tune t;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char *env = getenv("SGEMM_F32_TUNE");
+        if (env == nullptr) return;
+        char buf[256];
+        strncpy(buf, env, sizeof buf - 1);
+        buf[sizeof buf - 1] = 0;
+        for (char *item = buf; item != nullptr && *item != 0;) {
+            char *next = strchr(item, ',');
+            if (next != nullptr) *next++ = 0;
+            char *eq = strchr(item, '=');
+            if (eq == nullptr) {
+                item = next;
+                continue;
+            }
+            *eq = 0;
+            const char *key = item, *val = eq + 1;
+            item = next;
+            const long num = strtol(val, nullptr, 10);
+            if (!strcmp(key, "kernels")) {
+                t.kernels = !strcmp(val, "rowmajor8") ? 0 : !strcmp(val, "kmajor16") ? 1 : -1;
+            } else if (!strcmp(key, "schedule")) {
+                t.schedule = (val[0] >= '0' && val[0] <= '3' && val[1] == 0) ? static_cast<int>(num) : -1;
+            } else if (!strcmp(key, "parts")) {
+                t.parts = (num >= 2 && num <= 16) ? static_cast<int>(num) : -1;
+            } else if (!strcmp(key, "drain")) {
+                t.drain = !strcmp(val, "on");
+            }
+        }
+    });
+    return t;
+}
+
+// When a call takes the k-major copy of A: never (at = 0), where it pays
+// (1, the default) or whenever the workspace has room (2).
+struct Policy {
+    int at;
+};
+Policy policy() {
+    switch (tune().kernels) {
+        case 0: return {0};
+        case 1: return {2};
+        default: return {1};
+    }
+}
 
 // cuTensorMapEncodeTiled, fetched from the driver at run time (no link
 // against libcuda).  Null when unavailable: the cp.async kernels are used.
@@ -958,15 +1051,20 @@ struct DeviceInfo {
     int state;                    // 0 = not yet set up, 1 = ready, < 0 = status
     int sms;                      // multiprocessors
     int sk_per_sm[kVariants];     // co-resident stream-K CTAs per SM
+    unsigned long long ctx;       // id of the CUDA context the set-up was made in
 };
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 
 int setup_device(int dev, DeviceInfo *out) {
     if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    unsigned long long ctx = 0;
+    const bool known = sg_ctx::current_id(dev, &ctx);
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceInfo &d = g_dev[dev];
+    if (known && d.state != 0 && d.ctx != ctx) d.state = 0;  // a new context (e.g. after cudaDeviceReset)
     if (d.state == 0) {
+        d.ctx = ctx;
         int major = 0, minor = 0, st = SGEMM_OK;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -985,17 +1083,23 @@ int setup_device(int dev, DeviceInfo *out) {
                         break;
                     }
                 }
-                if (st == SGEMM_OK && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sk_per_sm[v], kSk[v],
-                                                                                    threads(v), SMEM_BYTES) !=
-                                          cudaSuccess)
+                // co-resident CTAs per SM: the smaller of the stream-K and the
+                // one-CTA-per-tile kernels' figures (the waves of both)
+                int sk = 0, dp = 0;
+                if (st == SGEMM_OK &&
+                    (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sk, kSk[v], threads(v), SMEM_BYTES) !=
+                         cudaSuccess ||
+                     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&dp, kDp[v], threads(v), SMEM_BYTES) !=
+                         cudaSuccess))
                     st = SGEMM_ERR_DEVICE;
+                d.sk_per_sm[v] = sk < dp ? sk : dp;
             }
-            // the k-major variant's waves are those of its 8 x 16 one-CTA-per-tile kernel too
-            int dp16 = 0;
-            if (st == SGEMM_OK &&
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&dp16, kDp[kAtVariant], NT16, SMEM_BYTES) != cudaSuccess)
-                st = SGEMM_ERR_DEVICE;
-            if (st == SGEMM_OK && dp16 < d.sk_per_sm[kAtVariant]) d.sk_per_sm[kAtVariant] = dp16;
+            for (const DpKernel f : kDrained)
+                if (st == SGEMM_OK &&
+                    (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
+                     cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                          cudaSharedmemCarveoutMaxShared) != cudaSuccess))
+                    st = SGEMM_ERR_DEVICE;
             for (const TailKernel f : kTail)
                 if (st == SGEMM_OK &&
                     (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
@@ -1089,14 +1193,19 @@ constexpr long long kMinItersPerCta = 4;
 //   plus about 4.5 %, and is chosen only when it is at least 3 % better.
 //   Fewer tiles than resident CTAs: the multi-part split is used when it
 //   adds more than 10 % CTAs.
+// SGEMM_F32_TUNE may force the schedule and the part count S.
 Plan plan_schedule(long long T, long long KT, long long G, long long sms, bool allow_tail) {
     Plan pl = {0, T, 0, 0, 0, 0, 0, 0};
     if (KT <= 0 || G <= 0) return pl;
-    if (T > G) {
+    const int forced = tune().schedule;
+    if (forced == 0) return pl;
+    const bool want_tail = forced == 3 || (forced < 0 && T > G);
+    if (forced != 2 && T > G) {
         const long long W = T / G, R = T % G;
-        if (R == 0) return pl;  // whole waves: already balanced
-        if (allow_tail && KT >= 2) {
+        if (R == 0 && forced < 0) return pl;  // whole waves: already balanced
+        if (want_tail && allow_tail && KT >= 2 && R > 0) {
             long long S = R <= sms ? 4 : (4 * G / R < 4 ? 4 : (4 * G / R > 8 ? 8 : 4 * G / R));
+            if (tune().parts > 0) S = tune().parts;
             if (S > KT) S = KT;
             pl.kind = 3;
             pl.grid = S * R;
@@ -1110,7 +1219,7 @@ Plan plan_schedule(long long T, long long KT, long long G, long long sms, bool a
         }
         const double dp_rounds = static_cast<double>(W) + (R <= sms ? 0.55 : 1.0);
         const double sk_rounds = static_cast<double>(T) / static_cast<double>(G) * 1.045;
-        if (sk_rounds > 0.97 * dp_rounds) return pl;
+        if (forced != 1 && sk_rounds > 0.97 * dp_rounds) return pl;
         pl.kind = 1;
         pl.grid = G;
         pl.dp_tiles = (W - 1) * G;  // the last T - dp_tiles tiles (between G and 2G) are split
@@ -1118,8 +1227,9 @@ Plan plan_schedule(long long T, long long KT, long long G, long long sms, bool a
         pl.bytes = static_cast<size_t>(pl.flag_words) * sizeof(unsigned);
         return pl;
     }
-    const long long g = (T * KT / kMinItersPerCta < G) ? T * KT / kMinItersPerCta : G;
-    if (static_cast<double>(g) <= 1.1 * static_cast<double>(T)) return pl;  // too few extra CTAs
+    long long g = (T * KT / kMinItersPerCta < G) ? T * KT / kMinItersPerCta : G;
+    if (forced != 2 && static_cast<double>(g) <= 1.1 * static_cast<double>(T)) return pl;  // too few extra CTAs
+    if (g < 1) g = 1;
     pl.kind = 2;
     pl.grid = g;
     pl.flag_words = g + 1;
@@ -1190,12 +1300,12 @@ struct Repack {
     size_t bytes;         // total workspace bytes this needs
 };
 Repack plan_repack(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const DeviceInfo &info,
-                   size_t avail) {
+                   size_t avail, const Policy &pol) {
     Repack r = {false, false, false, 0, 0, 0, 0, 0, 0, 0, 0};
     if (K <= 0 || encode_fn() == nullptr) return r;
     const bool ra = vector_class(A, lda) != 4, rb = vector_class(B, ldb) != 4;
     const long long T = tile_count(M, N), KT = (K + BK - 1) / BK;
-    const bool want_at = ra || kmajor_pays(M, N, K);
+    const bool want_at = pol.at == 2 || (pol.at == 1 && (ra || kmajor_pays(M, N, K)));
     if (!ra && !rb && !want_at) return r;
     const int v = want_at ? kAtVariant : kTmaVariant;
     const Plan pl = plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, true);
@@ -1259,7 +1369,8 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     const int st = setup_device(dev, &info);
     if (st != SGEMM_OK) return st;
 
-    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, flags != nullptr ? flag_bytes : 0);
+    const Policy pol = policy();
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, flags != nullptr ? flag_bytes : 0, pol);
     Maps maps;
     if (rp.at) {
         // every copy's address is known before anything is launched: encode
@@ -1270,6 +1381,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
         memset(&maps, 0, sizeof maps);
         if (!encode_maps(maps, M, N, K, at, rp.ldat, rp.b ? b2 : B, rp.b ? rp.ldb2 : ldb, true))
             return SGEMM_ERR_DEVICE;
+        sg_nvtx::Range r("sgemm_f32: k-major copy of A");
         if (transpose_f32(M, K, A, lda, at, rp.ldat, stream) != TRANSPOSE_OK) {
             (void)cudaGetLastError();
             return SGEMM_ERR_LAUNCH;
@@ -1287,6 +1399,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
         }
         flag_bytes = rp.plan_bytes;  // the schedule keeps to the region before the copies
     } else if (rp.a || rp.b) {
+        sg_nvtx::Range r("sgemm_f32: repack rows");
         char *ws = reinterpret_cast<char *>(flags);
         const unsigned blocks = static_cast<unsigned>(info.sms) * 8;
         if (rp.a) {
@@ -1332,9 +1445,10 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
                 (void)cudaGetLastError();
                 return SGEMM_ERR_LAUNCH;
             }
+            sg_nvtx::Range r("sgemm_f32: whole waves + split tail");
             cfg.gridDim = dim3(static_cast<unsigned>(pl.dp_tiles));
             cfg.blockDim = dim3(threads(v));
-            if (cudaLaunchKernelEx(&cfg, kDp[v], p, maps) != cudaSuccess) {
+            if (cudaLaunchKernelEx(&cfg, dp_kernel(v, tune().drain), p, maps) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return SGEMM_ERR_LAUNCH;
             }
@@ -1359,6 +1473,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     if (flags != nullptr && pl.kind != 0 && flag_bytes >= pl.bytes) {
         float *partials =
             pl.kind == 2 ? reinterpret_cast<float *>(reinterpret_cast<char *>(flags) + pl.partials_offset) : nullptr;
+        sg_nvtx::Range r("sgemm_f32: stream-K");
         err = cudaMemsetAsync(flags, 0, static_cast<size_t>(pl.flag_words) * sizeof(unsigned), stream);
         if (err == cudaSuccess) {
             cudaLaunchAttribute attr;
@@ -1383,9 +1498,10 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
         return SGEMM_ERR_LAUNCH;
     }
     if (!done) {
+        sg_nvtx::Range r("sgemm_f32: one CTA per tile");
         cfg.gridDim = dim3(static_cast<unsigned>(T));
         cfg.blockDim = dim3(threads(v));
-        err = cudaLaunchKernelEx(&cfg, kDp[v], p, maps);
+        err = cudaLaunchKernelEx(&cfg, dp_kernel(v, tune().drain), p, maps);
         if (err != cudaSuccess) {
             (void)cudaGetLastError();
             return SGEMM_ERR_LAUNCH;
@@ -1405,13 +1521,19 @@ static __device__ __align__(256) unsigned g_static_scratch[kStaticScratchWords];
 std::mutex g_static_mutex;
 unsigned *g_static_ptr[kMaxDevices];   // device address of g_static_scratch
 int g_static_state[kMaxDevices];       // 0 = not yet looked up, 1 = ready, < 0 = status
+unsigned long long g_static_ctx[kMaxDevices];  // context the address belongs to
 
-// Looks up, once per device and with that device current, the device
-// address of g_static_scratch (the host-side name is only a stand-in).
+// Looks up, once per device (and again in a new context of that device, e.g.
+// after cudaDeviceReset) and with that device current, the device address of
+// g_static_scratch (the host-side name is only a stand-in).
 int static_scratch(int dev, unsigned **out) {
     if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    unsigned long long ctx = 0;
+    const bool known = sg_ctx::current_id(dev, &ctx);
     std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (known && g_static_state[dev] != 0 && g_static_ctx[dev] != ctx) g_static_state[dev] = 0;
     if (g_static_state[dev] == 0) {
+        g_static_ctx[dev] = ctx;
         void *ptr = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
         if (e != cudaSuccess || ptr == nullptr) {
@@ -1471,7 +1593,7 @@ extern "C" size_t sgemm_f32_workspace_size_for(int M, int N, int K, const float 
         (void)cudaGetLastError();
         return base;
     }
-    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, SIZE_MAX);
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, SIZE_MAX, policy());
     return rp.bytes > base ? round256(rp.bytes) : base;
 }
 
@@ -1490,7 +1612,8 @@ extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int ld
     }
     const int sd = setup_device(dev, &info);
     if (sd != SGEMM_OK) return sd;
-    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, workspace_bytes);
+    const Policy pol = policy();
+    const Repack rp = plan_repack(M, N, K, A, lda, B, ldb, info, workspace_bytes, pol);
     int v = rp.at ? kAtVariant : kTmaVariant;  // the copies have 16-byte aligned rows
     if (!rp.a && !rp.b && !rp.at) {
         Maps maps;
@@ -1567,7 +1690,7 @@ extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n
         case 8: steps = 4 * A_VECS; break;
         default: return SGEMM_ERR_INVALID_ARG;
     }
-    if (n_warps) *n_warps = (kind == 11 || kind == 12) ? NT16 / 32 : NT / 32;
+    if (n_warps) *n_warps = kind >= 11 ? NT16 / 32 : NT / 32;
     if (n_steps) *n_steps = steps;
     if (n_stages) *n_stages = (kind == 2 || kind == 8) ? 2 : kind >= 11 ? STAGES_AT : STAGES;
     return SGEMM_OK;

@@ -26,6 +26,8 @@
 #include <cstdint>
 #include <mutex>
 
+#include "ctx_key.cuh"
+#include "nvtx_range.cuh"
 #include "sgemm_f32.h"
 
 namespace {
@@ -112,13 +114,20 @@ HostLayout host_layout(int M, int N, int K) {
 }
 
 // One pair of non-blocking copy streams per device, made on first use.
+// A new context of the device (e.g. after cudaDeviceReset, which destroys
+// the streams with the old one) gets a new pair.
 std::mutex g_stream_mutex;
 cudaStream_t g_h2d[kMaxDevices], g_d2h[kMaxDevices];
+unsigned long long g_stream_ctx[kMaxDevices];
 
 int copy_streams(int dev, cudaStream_t &h2d, cudaStream_t &d2h) {
     if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    unsigned long long ctx = 0;
+    const bool known = sg_ctx::current_id(dev, &ctx);
     std::lock_guard<std::mutex> lock(g_stream_mutex);
+    if (known && g_h2d[dev] != nullptr && g_stream_ctx[dev] != ctx) g_h2d[dev] = g_d2h[dev] = nullptr;
     if (g_h2d[dev] == nullptr) {
+        g_stream_ctx[dev] = ctx;
         cudaStream_t a = nullptr, b = nullptr;
         if (cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking) != cudaSuccess ||
             cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking) != cudaSuccess) {
@@ -205,10 +214,12 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     };
     // columns [c0, c0 + nc) of B, all K rows
     auto copy_b = [&](int c0, int nc) {
+        sg_nvtx::Range r("sgemm_f32_host: copy in B block");
         return K == 0 || cudaMemcpy2DAsync(dB + c0, static_cast<size_t>(N4) * 4, B + c0, static_cast<size_t>(ldb) * 4,
                                            static_cast<size_t>(nc) * 4, K, cudaMemcpyHostToDevice, h2d) == cudaSuccess;
     };
     auto copy_a = [&](int p) {
+        sg_nvtx::Range r("sgemm_f32_host: copy in A panel");
         const int r0 = pn.start[p], nr = pn.rows(p);
         return (K == 0 || cudaMemcpy2DAsync(dA + static_cast<size_t>(r0) * K4, static_cast<size_t>(K4) * 4,
                                             A + static_cast<size_t>(r0) * lda, static_cast<size_t>(lda) * 4,
@@ -250,6 +261,7 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
         if (st != SGEMM_OK) return fail(st);
         if (cudaEventRecord(e_c[p], stream) != cudaSuccess || cudaStreamWaitEvent(d2h, e_c[p], 0) != cudaSuccess)
             return fail(SGEMM_ERR_LAUNCH);
+        sg_nvtx::Range r("sgemm_f32_host: copy out C panel");
         if (cudaMemcpy2DAsync(C + static_cast<size_t>(r0) * ldc, static_cast<size_t>(ldc) * 4,
                               dC + static_cast<size_t>(r0) * N4, static_cast<size_t>(N4) * 4,
                               static_cast<size_t>(N) * 4, nr, cudaMemcpyDeviceToHost, d2h) != cudaSuccess)

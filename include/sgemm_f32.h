@@ -21,7 +21,8 @@
  * overlap on the GPU share its scratch: see there).  No product entry point
  * allocates device memory; only the two wait self-tests allocate (and free)
  * a few bytes.  The first call on a device sets up that device's kernel
- * attributes (once, under a lock).
+ * attributes (once, under a lock).  That set-up belongs to the CUDA context
+ * current at the time: after cudaDeviceReset the next call sets up again.
  */
 #ifndef SGEMM_F32_H
 #define SGEMM_F32_H
@@ -245,7 +246,9 @@ size_t sgemm_f32_host_workspace_size(int M, int N, int K);
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and keeps it; make that first call before any stream
- * capture begins.  Every call shares the one array, which keeps whatever the
+ * capture begins.  The address belongs to the CUDA context it was looked up
+ * in: a call made in a new context of the device (after cudaDeviceReset, for
+ * instance) looks it up again.  Every call shares the one array, which keeps whatever the
  * last call left there: each call zero-fills the words it uses on `stream`
  * before its kernel, and calls that overlap on the GPU (different streams,
  * or different host threads) race on the array and must not be issued.

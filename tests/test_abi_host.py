@@ -150,3 +150,15 @@ def test_schedule_query_checks_arguments_on_host(lib):
     assert sg.ws_schedule(4, 4, 8, FAKE, 7, FAKE * 2, 4, FAKE * 3, 4) == (-2, 0, 0)
     assert sg.ws_schedule(0, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4) == (0, 0, 0)
     assert lib.sgemm_f32_ws_schedule(4, 4, 4, FAKE, 4, FAKE * 2, 4, FAKE * 3, 4, 0, None, None) == -3
+
+
+def test_bank_probe_rejects_bad_arguments_on_the_host(lib):
+    # the checks come before any CUDA call, so this needs no GPU
+    import ctypes
+    cyc, chk = ctypes.c_double(), ctypes.c_longlong()
+    probe = lib.smem_bank_stride_probe
+    for args in [(0, 0, 8, 64), (65, 0, 8, 64), (1, 2, 8, 64), (1, 0, 0, 64), (1, 0, 9, 64), (1, 0, 8, 32),
+                 (1, 0, 8, 100), (1, 0, 8, 65536 + 64)]:
+        assert probe(*args, ctypes.byref(cyc), ctypes.byref(chk)) == -7, args
+    assert probe(1, 0, 8, 64, None, ctypes.byref(chk)) == -3
+    assert probe(1, 0, 8, 64, ctypes.byref(cyc), None) == -3
