@@ -405,14 +405,15 @@ __device__ __forceinline__ void acc16_zero(Acc16 &acc) {
 }
 
 // Accumulates the product of C tile (m0, n0) over K tiles [kt0, kt1) into
-// acc, with A given as its k-major copy At (K x M; maps.a describes it).
-// Each stage of a STAGES_AT-deep ring receives a 16 x 128 box of At and a
-// 16 x 128 box of B by tensor copy, completing on the stage's mbarrier.
-// Iteration kt waits for tile kt, then a barrier (every thread has finished
-// tile kt-1, whose stage is free), issues tile kt + STAGES_AT - 1 into that
-// stage and runs 16 k steps.  `pipe` counts the tiles this CTA has loaded
-// before this range (load u goes to stage u % STAGES_AT, whose mbarrier
-// completes phase u / STAGES_AT), as in mma_k_range.
+// acc, with A given as its k-major copy At (K x M; maps.a describes it) and
+// K tiles BK_AT deep.  Each stage of a STAGES_AT-deep ring receives a
+// BK_AT x 128 box of At and a BK_AT x 128 box of B by tensor copy,
+// completing on the stage's mbarrier.  Iteration kt waits for tile kt, then a
+// barrier (every thread has finished tile kt-1, whose stage is free), issues
+// tile kt + STAGES_AT - 1 into that stage and runs BK_AT k steps.  `pipe`
+// counts the tiles this CTA has loaded before this range (load u goes to
+// stage u % STAGES_AT, whose mbarrier completes phase u / STAGES_AT), as in
+// mma_k_range.
 // With DRAIN (a diagnostic kernel, never dispatched by default) one tile is in
 // flight at a time, issued after the k steps of the one before: no copy
 // writes shared memory while the fragments are read.
@@ -427,9 +428,9 @@ __device__ __forceinline__ void kmajor16_k_range(const Maps &maps, const int m0,
         if (tid == 0) {
             const uint32_t stage = (u0 + kt) % STAGES_AT;
             const uint32_t bar = bars + 8 * stage;
-            mbar_expect_tx(bar, STAGE_FLOATS * 4);
-            tma_load_2d(sbase + at_word(stage, 0, 0) * 4, &maps.a, m0, kt * BK, bar);
-            tma_load_2d(sbase + bs_word(stage, 0, 0) * 4, &maps.b, n0, kt * BK, bar);
+            mbar_expect_tx(bar, AT_STAGE_FLOATS * 4);
+            tma_load_2d(sbase + at_word(stage, 0, 0) * 4, &maps.a, m0, kt * BK_AT, bar);
+            tma_load_2d(sbase + atb_word(stage, 0, 0) * 4, &maps.b, n0, kt * BK_AT, bar);
         }
     };
     const int ra = frag16_row0(tid);
@@ -448,14 +449,14 @@ __device__ __forceinline__ void kmajor16_k_range(const Maps &maps, const int m0,
         if (!DRAIN && kt + STAGES_AT - 1 < kt1) issue_tile(kt + STAGES_AT - 1);
         const uint32_t stage = u % STAGES_AT;
 #pragma unroll
-        for (int k = 0; k < BK; ++k) {
+        for (int k = 0; k < BK_AT; ++k) {
             const float4 a0 = *reinterpret_cast<const float4 *>(smem + at_word(stage, k, ra));
             const float4 a1 = *reinterpret_cast<const float4 *>(smem + at_word(stage, k, ra + 32));
             const float a[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             float2 bp[TN16 / 2];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                const float4 b = *reinterpret_cast<const float4 *>(smem + bs_word(stage, k, cb + 16 * g));
+                const float4 b = *reinterpret_cast<const float4 *>(smem + atb_word(stage, k, cb + 16 * g));
                 bp[2 * g] = make_float2(b.x, b.y);
                 bp[2 * g + 1] = make_float2(b.z, b.w);
             }
@@ -547,7 +548,7 @@ __global__ void __launch_bounds__(NT16, 2) sgemm_f32_kmajor_kernel(const Problem
     Acc16 acc;
     acc16_zero(acc);
     uint32_t pipe = 0;
-    kmajor16_k_range<DRAIN>(maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
+    kmajor16_k_range<DRAIN>(maps, tm * BM, tn * BN, 0, (p.K + BK_AT - 1) / BK_AT, pipe, smem, bars, acc);
     store_tile16<false>(p, tm * BM, tn * BN, acc);
 }
 
@@ -605,15 +606,16 @@ __device__ __forceinline__ void raise_flag(unsigned *flag) {
 
 // The segments of one CTA of the stream-K schedules (below): first whole
 // data-parallel tiles (tile c, c + G, ...), then its share of the (tile,
-// K tile) iterations of the remaining tiles, cut at tile boundaries.
+// K tile) iterations of the remaining tiles, cut at tile boundaries.  K tiles
+// are bk deep (BK, or BK_AT for the k-major kernels).
 struct SkWalk {
     const Problem &p;  // the kernel parameter (read from parameter space, not held in registers)
     int KT, G, dp_tiles;
     long long total_iters, base, it, it_end;
     int dp_lin;
 
-    __device__ __forceinline__ SkWalk(const Problem &prob, int dp) : p(prob) {
-        KT = (p.K + BK - 1) / BK;
+    __device__ __forceinline__ SkWalk(const Problem &prob, int dp, int bk) : p(prob) {
+        KT = (p.K + bk - 1) / bk;
         G = gridDim.x;
         dp_tiles = dp;
         total_iters = static_cast<long long>(p.tiles_m * p.tiles_n - dp_tiles) * KT;
@@ -678,7 +680,7 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
     const uint32_t bars = smem_u32(bar_mem);
     init_bars<TMA>(bars);
     uint32_t pipe = 0;
-    SkWalk w(p, dp_tiles);
+    SkWalk w(p, dp_tiles, BK);
     unsigned *error = flags + (partials ? gridDim.x : p.tiles_m * p.tiles_n);
     // One loop over segments (whole data-parallel tiles first, then this CTA's
     // stream-K range cut at tile boundaries), so the main loop is inlined once.
@@ -727,7 +729,7 @@ sgemm_f32_kmajor_streamk_kernel(const Problem p, const __grid_constant__ Maps ma
     const uint32_t bars = smem_u32(bar_mem);
     init_bars<true>(bars);
     uint32_t pipe = 0;
-    SkWalk w(p, dp_tiles);
+    SkWalk w(p, dp_tiles, BK_AT);
     unsigned *error = flags + (partials ? gridDim.x : p.tiles_m * p.tiles_n);
     int lin, tm, tn, k0, k1;
     while (w.next(lin, tm, tn, k0, k1)) {
@@ -819,7 +821,7 @@ sgemm_f32_kmajor_tail_kernel(const Problem p, const __grid_constant__ Maps maps,
     const uint32_t bars = smem_u32(bar_mem);
     init_bars<true>(bars);
     const int c = blockIdx.x, tile = c / parts, part = c - tile * parts;
-    const int KT = (p.K + BK - 1) / BK;
+    const int KT = (p.K + BK_AT - 1) / BK_AT;
     const int k0 = static_cast<int>(static_cast<long long>(KT) * part / parts);
     const int k1 = static_cast<int>(static_cast<long long>(KT) * (part + 1) / parts);
     int tm, tn;
@@ -900,6 +902,9 @@ __global__ void wait_selftest_kernel(int which, unsigned limit, unsigned *status
 // ---------------------------------------------------------------------------
 
 constexpr int kMaxDevices = 64;
+// Dynamic shared memory the cta_per_sm=1 diagnostic asks for: more than half
+// of an SM's, so two CTAs never share one.
+constexpr int kOneCtaSmem = 120 * 1024;
 // Kernel variants: (VA, VB) in {4, 1} x {4, 2, 1} with cp.async (0..5) and
 // (4, 4) with TMA (6), for the 8 x 8 row-major kernels; 7 is the 8 x 16
 // kernel on the k-major copy of A.
@@ -926,8 +931,10 @@ const TailKernel kTail[2] = {sgemm_f32_tail_kernel<4, 4, true>, sgemm_f32_kmajor
 const DpKernel kDrained[1] = {sgemm_f32_kmajor_kernel<true>};
 DpKernel dp_kernel(int v, bool drain) { return drain && v == kAtVariant ? kDrained[0] : kDp[v]; }
 bool is_tma(int v) { return v == kTmaVariant || v == kAtVariant; }
-// threads per CTA of variant v's kernels
+// threads per CTA, dynamic shared memory and K-tile depth of variant v's kernels
 unsigned threads(int v) { return v == kAtVariant ? NT16 : NT; }
+int smem_of(int v) { return v == kAtVariant ? SMEM_AT_BYTES : SMEM_BYTES; }
+int bk_of(int v) { return v == kAtVariant ? BK_AT : BK; }
 
 // ---- tuning overrides --------------------------------------------------
 // SGEMM_F32_TUNE = "key=value,key=value" (read once, at the first call) forces
@@ -943,7 +950,11 @@ unsigned threads(int v) { return v == kAtVariant ? NT16 : NT; }
 //              it only after the k steps of the one before, so no copy
 //              writes shared memory while fragments are read (slow; it
 //              exists to count shared-memory bank conflicts without the
-//              copy engines' concurrent writes).
+//              copy engines' concurrent writes);
+//   cta_per_sm = 1 : a diagnostic: the one-CTA-per-tile grid asks for
+//              enough shared memory that only one CTA fits on an SM (the
+//              kernels use the first SMEM_BYTES of it), so that no second
+//              CTA's copies or loads share the SM.
 // A forced choice changes only how the work is split, so the product stays
 // within the same FP32 bound (not bit for bit the default's).
 struct Tune {
@@ -951,6 +962,7 @@ struct Tune {
     int schedule = -1;
     int parts = -1;
     bool drain = false; // the drained-ring diagnostic kernels
+    bool one_cta = false; // one CTA per SM in the one-CTA-per-tile grid (diagnostic)
 };
 const Tune &tune() {
     static Tune t;
@@ -981,6 +993,8 @@ const Tune &tune() {
                 t.parts = (num >= 2 && num <= 16) ? static_cast<int>(num) : -1;
             } else if (!strcmp(key, "drain")) {
                 t.drain = !strcmp(val, "on");
+            } else if (!strcmp(key, "cta_per_sm")) {
+                t.one_cta = num == 1;
             }
         }
     });
@@ -1025,18 +1039,19 @@ EncodeTiledFn encode_fn() {
 // Describes A (K x M elements, rows lda apart; box 16 x 128, 64-byte
 // swizzle) and B (N x K, rows ldb apart; box 128 x 16, no swizzle) for the
 // tensor copies.  With a_kmajor, A is the k-major copy At (M x K elements in
-// the map's order, rows lda apart: box 128 x 16, no swizzle, the As
-// layout).  Needs 16-byte aligned bases and row strides.
+// the map's order, rows lda apart: box 128 x BK_AT, no swizzle, the As
+// layout) and B's box is 128 x BK_AT.  Needs 16-byte aligned bases and row
+// strides.
 bool encode_maps(Maps &maps, int M, int N, int K, const float *A, int lda, const float *B, int ldb,
                  bool a_kmajor = false) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
     const cuuint64_t a_dim[2] = {static_cast<cuuint64_t>(a_kmajor ? M : K), static_cast<cuuint64_t>(a_kmajor ? K : M)};
     const cuuint64_t a_stride[1] = {static_cast<cuuint64_t>(lda) * 4};
-    const cuuint32_t a_box[2] = {a_kmajor ? BM : BK, a_kmajor ? BK : BM};
+    const cuuint32_t a_box[2] = {a_kmajor ? BM : BK, a_kmajor ? BK_AT : BM};
     const cuuint64_t b_dim[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
     const cuuint64_t b_stride[1] = {static_cast<cuuint64_t>(ldb) * 4};
-    const cuuint32_t b_box[2] = {BN, BK};
+    const cuuint32_t b_box[2] = {BN, a_kmajor ? static_cast<cuuint32_t>(BK_AT) : static_cast<cuuint32_t>(BK)};
     const cuuint32_t ones[2] = {1, 1};
     return enc(&maps.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(A), a_dim, a_stride, a_box, ones,
                CU_TENSOR_MAP_INTERLEAVE_NONE, a_kmajor ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
@@ -1075,7 +1090,7 @@ int setup_device(int dev, DeviceInfo *out) {
             for (int v = 0; v < kVariants && st == SGEMM_OK; ++v) {
                 const void *fns[2] = {reinterpret_cast<const void *>(kDp[v]), reinterpret_cast<const void *>(kSk[v])};
                 for (const void *f : fns) {
-                    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+                    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_of(v)) !=
                             cudaSuccess ||
                         cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
@@ -1087,23 +1102,30 @@ int setup_device(int dev, DeviceInfo *out) {
                 // one-CTA-per-tile kernels' figures (the waves of both)
                 int sk = 0, dp = 0;
                 if (st == SGEMM_OK &&
-                    (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sk, kSk[v], threads(v), SMEM_BYTES) !=
+                    (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sk, kSk[v], threads(v), smem_of(v)) !=
                          cudaSuccess ||
-                     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&dp, kDp[v], threads(v), SMEM_BYTES) !=
+                     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&dp, kDp[v], threads(v), smem_of(v)) !=
                          cudaSuccess))
                     st = SGEMM_ERR_DEVICE;
                 d.sk_per_sm[v] = sk < dp ? sk : dp;
             }
+            // the one-CTA-per-tile kernels may be launched with the padded
+            // request of the cta_per_sm=1 diagnostic
+            for (int v = 0; v < kVariants && st == SGEMM_OK; ++v)
+                if (cudaFuncSetAttribute(kDp[v], cudaFuncAttributeMaxDynamicSharedMemorySize, kOneCtaSmem) !=
+                    cudaSuccess)
+                    st = SGEMM_ERR_DEVICE;
             for (const DpKernel f : kDrained)
                 if (st == SGEMM_OK &&
-                    (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
+                    (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kOneCtaSmem) != cudaSuccess ||
                      cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                           cudaSharedmemCarveoutMaxShared) != cudaSuccess))
                     st = SGEMM_ERR_DEVICE;
-            for (const TailKernel f : kTail)
+            for (int t = 0; t < 2; ++t)
                 if (st == SGEMM_OK &&
-                    (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess ||
-                     cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                    (cudaFuncSetAttribute(kTail[t], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          t == 1 ? SMEM_AT_BYTES : SMEM_BYTES) != cudaSuccess ||
+                     cudaFuncSetAttribute(kTail[t], cudaFuncAttributePreferredSharedMemoryCarveout,
                                           cudaSharedmemCarveoutMaxShared) != cudaSuccess))
                     st = SGEMM_ERR_DEVICE;
         }
@@ -1257,22 +1279,23 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 constexpr double kRepackMinFlops = 2e9;
 
 // Whether transposing a 16-byte aligned A into its k-major copy first pays.
-// Measured on GB300, transpose included (us, row-major -> k-major; same
-// results bit for bit): the k-major kernels (8 x 16 register tiles) take
-// about 4.5 % less time than the row-major ones, whatever the schedule:
-//   one CTA per tile / split tail: 3072^3 901 -> 874, 4096^3 1985 -> 1918,
-//     6144^3 6630 -> 6361, 8192^3 15655 -> 14993, 2500x2100x4096 672 -> 663;
-//   stream-K (fewer tiles than resident CTAs): 512x8192x8192 1060 -> 1023,
-//     256x16384x4096 539 -> 522, 1024x4096x4096 538 -> 525, 2048x2048x4096
-//     537 -> 529, but 4096x1024x4096 538 -> 541, 1536^3 129 -> 130 and
-//     16384x256x4096 540 -> 598, where the transpose costs more.
+// Measured on GB300, transpose included (TFLOP/s, row-major 8 x 8 kernels ->
+// k-major 8 x 16 kernels with 32-deep K tiles, the same schedule rules): the
+// k-major kernels take about 6 % less time than the row-major ones:
+//   one CTA per tile / split tail: 3072^3 64.51 -> 67.66, 4096^3 69.34 ->
+//     73.04, 6144^3 70.14 -> 74.27, 8192^3 70.39 -> 74.64;
+//   stream-K (fewer tiles than resident CTAs): 2048^3 62.10 -> 64.39,
+//     2048x2048x4096 64.02 -> 66.87, 256x16384x4096 63.93 -> 67.80; but
+//     1024^3 40.36 -> 37.19, 16384x256x4096 63.81 -> 58.98, 16384x512x4096
+//     67.32 -> 66.10 and 32768x256x4096 67.32 -> 61.62, where the transpose
+//     costs more than it saves (A is large next to the product).
 // The transpose moves 8 M K bytes at about 5.5 TB/s plus a launch (4096^2
-// 26.8 us, 16384 x 4096 84.3 us).  So the copy is taken when the expected
-// saving, 4.5 % of 2MNK at 70 TFLOP/s, exceeds 1.2 x the transpose's time.
-// An A whose rows are not 16-byte aligned is copied anyway, and then always
+// 21 us, 16384 x 4096 84 us).  So the copy is taken when the expected
+// saving, 6 % of 2MNK at 68 TFLOP/s, exceeds 1.2 x the transpose's time.  An
+// A whose rows are not 16-byte aligned is copied anyway, and then always
 // into the k-major copy.
 bool kmajor_pays(int M, int N, int K) {
-    const double saving = 0.045 * 2.0 * M * N * K / 70e12;
+    const double saving = 0.06 * 2.0 * M * N * K / 68e12;
     const double copy = 8.0 * M * K / 5.5e12 + 4e-6;
     return saving > 1.2 * copy;
 }
@@ -1304,10 +1327,10 @@ Repack plan_repack(int M, int N, int K, const float *A, int lda, const float *B,
     Repack r = {false, false, false, 0, 0, 0, 0, 0, 0, 0, 0};
     if (K <= 0 || encode_fn() == nullptr) return r;
     const bool ra = vector_class(A, lda) != 4, rb = vector_class(B, ldb) != 4;
-    const long long T = tile_count(M, N), KT = (K + BK - 1) / BK;
     const bool want_at = pol.at == 2 || (pol.at == 1 && (ra || kmajor_pays(M, N, K)));
     if (!ra && !rb && !want_at) return r;
     const int v = want_at ? kAtVariant : kTmaVariant;
+    const long long T = tile_count(M, N), KT = (K + bk_of(v) - 1) / bk_of(v);
     const Plan pl = plan_schedule(T, KT, static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, true);
     r.lda2 = (K + 3) / 4 * 4;
     r.ldb2 = (N + 3) / 4 * 4;
@@ -1429,12 +1452,12 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     p.vc = vector_class(C, ldc);
     const long long T = static_cast<long long>(p.tiles_m) * p.tiles_n;
     const long long G = static_cast<long long>(info.sk_per_sm[v]) * info.sms;
-    const long long KT = (K + BK - 1) / BK;
+    const long long KT = (K + bk_of(v) - 1) / bk_of(v);
     Plan pl = plan_schedule(T, KT, G, info.sms, is_tma(v));
 
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem_of(v);
     cfg.stream = stream;
     if (pl.kind == 3) {
         if (flags != nullptr && flag_bytes >= pl.bytes) {
@@ -1501,6 +1524,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
         sg_nvtx::Range r("sgemm_f32: one CTA per tile");
         cfg.gridDim = dim3(static_cast<unsigned>(T));
         cfg.blockDim = dim3(threads(v));
+        if (tune().one_cta) cfg.dynamicSmemBytes = kOneCtaSmem;
         err = cudaLaunchKernelEx(&cfg, dp_kernel(v, tune().drain), p, maps);
         if (err != cudaSuccess) {
             (void)cudaGetLastError();
@@ -1620,7 +1644,7 @@ extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int ld
         v = choose_variant(M, N, K, A, lda, B, ldb, maps);
     }
     const size_t avail = (rp.a || rp.b || rp.at) ? rp.plan_bytes : workspace_bytes;
-    const Plan pl = effective_plan(tile_count(M, N), (K + BK - 1) / BK,
+    const Plan pl = effective_plan(tile_count(M, N), (K + bk_of(v) - 1) / bk_of(v),
                                    static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, is_tma(v), avail);
     *kind = pl.kind | (rp.a ? 4 : 0) | (rp.b ? 8 : 0) | (rp.at ? 16 : 0);
     *words = pl.flag_words;
@@ -1680,9 +1704,9 @@ extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n
         case 0: steps = A_COPIES16; break;
         case 1: steps = b_copies<4>(); break;
         case 2:
-        case 3:
-        case 11: steps = 2 * BK; break;
-        case 12: steps = 4 * BK; break;
+        case 3: steps = 2 * BK; break;
+        case 11: steps = 2 * BK_AT; break;
+        case 12: steps = 4 * BK_AT; break;
         case 4: steps = b_copies<2>(); break;
         case 5: steps = b_copies<1>(); break;
         case 6: steps = A_COPIES4; break;
@@ -1718,7 +1742,7 @@ extern "C" int sgemm_f32_smem_request(int kind, int warp, int step, int stage, i
             case 2: word = as_word(stage, step >> 1, frag_row0(tid) + 16 * (step & 1)); width = 16; break;
             case 3: word = bs_word(stage, step >> 1, frag_col0(tid) + 32 * (step & 1)); width = 16; break;
             case 11: word = at_word(stage, step >> 1, frag16_row0(tid) + 32 * (step & 1)); width = 16; break;
-            case 12: word = bs_word(stage, step >> 2, frag16_col0(tid) + 16 * (step & 3)); width = 16; break;
+            case 12: word = atb_word(stage, step >> 2, frag16_col0(tid) + 16 * (step & 3)); width = 16; break;
         }
         byte_offset[lane] = static_cast<int64_t>(word) * 4;
     }

@@ -20,12 +20,12 @@ constexpr int kWords = 4096;
 template <int OP, int U>
 __device__ __forceinline__ void access(uint32_t lane_addr, int lane_word, unsigned &acc) {
     if constexpr (OP == 0) {
-        asm volatile("{\n .reg .b32 t;\n ld.shared.b32 t, [%1+%2];\n add.u32 %0, %0, t;\n}\n"
+        asm volatile("{\n .reg .b32 t;\n ld.volatile.shared.b32 t, [%1+%2];\n add.u32 %0, %0, t;\n}\n"
                      : "+r"(acc)
                      : "r"(lane_addr), "n"(128 * U)
                      : "memory");
     } else {
-        asm volatile("st.shared.b32 [%0+%1], %2;" ::"r"(lane_addr), "n"(128 * U), "r"(lane_word + 32 * U)
+        asm volatile("st.volatile.shared.b32 [%0+%1], %2;" ::"r"(lane_addr), "n"(128 * U), "r"(lane_word + 32 * U)
                      : "memory");
     }
 }
@@ -64,24 +64,26 @@ __global__ void __launch_bounds__(256) bank_stride_kernel(int stride, int iters,
 }
 
 // One warp-wide access pattern: lane l reads W bytes at word lane_word[l] +
-// 64 (u % 8) in access u (a shift by 64 words keeps every bank, so all eight
-// offsets need the same passes; every word stays below 2048 + 448 + 4 < 4096).
+// 32 u in access u of each group of 64 (a shift by 32 words keeps every bank;
+// every word stays below 2048 + 32 * 63 + 4 < 4096).  The loads are volatile,
+// so none is merged with another or moved out of the loop, and only the
+// first word of each is added into acc (one add per load keeps instruction
+// issue below the pipe's rate for all but the cheapest patterns).
 struct LaneWords {
     int w[32];
 };
 template <int W, int U>
 __device__ __forceinline__ void vload(uint32_t lane_addr, unsigned &acc) {
-    constexpr int off = 256 * (U % 8);
+    constexpr int off = 128 * U;
     if constexpr (W == 4) {
-        asm volatile("{\n .reg .b32 t;\n ld.shared.b32 t, [%1+%2];\n add.u32 %0, %0, t;\n}\n"
+        asm volatile("{\n .reg .b32 t;\n ld.volatile.shared.b32 t, [%1+%2];\n add.u32 %0, %0, t;\n}\n"
                      : "+r"(acc) : "r"(lane_addr), "n"(off) : "memory");
     } else if constexpr (W == 8) {
-        asm volatile("{\n .reg .b32 t0, t1;\n ld.shared.v2.b32 {t0, t1}, [%1+%2];\n add.u32 %0, %0, t0;\n"
-                     " add.u32 %0, %0, t1;\n}\n"
+        asm volatile("{\n .reg .b32 t0, t1;\n ld.volatile.shared.v2.b32 {t0, t1}, [%1+%2];\n add.u32 %0, %0, t0;\n}\n"
                      : "+r"(acc) : "r"(lane_addr), "n"(off) : "memory");
     } else {
-        asm volatile("{\n .reg .b32 t0, t1, t2, t3;\n ld.shared.v4.b32 {t0, t1, t2, t3}, [%1+%2];\n"
-                     " add.u32 %0, %0, t0;\n add.u32 %0, %0, t1;\n add.u32 %0, %0, t2;\n add.u32 %0, %0, t3;\n}\n"
+        asm volatile("{\n .reg .b32 t0, t1, t2, t3;\n ld.volatile.shared.v4.b32 {t0, t1, t2, t3}, [%1+%2];\n"
+                     " add.u32 %0, %0, t0;\n}\n"
                      : "+r"(acc) : "r"(lane_addr), "n"(off) : "memory");
     }
 }

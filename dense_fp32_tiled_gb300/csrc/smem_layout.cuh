@@ -25,11 +25,11 @@
 //        take 4 consecutive m (16-byte aligned), so As needs no padding.
 //
 // With A supplied already transposed (the k-major copy At = A^T, K x M,
-// that sgemm_f32_ws can make in its workspace), the A half of each stage
-// receives a 16 x 128 k-major tile directly from a tensor copy: logical
-// (k, m) at word k*BM + m, the As layout, so the fragment reads are the same
-// and no shared store is needed.  The As buffers are then unused, and the
-// same shared block holds STAGES_AT stages.
+// that sgemm_f32_ws can make in its workspace), each stage of a separate
+// STAGES_AT-deep ring receives a BK_AT x 128 tile of B (row-major, atb_word)
+// and a BK_AT x 128 k-major tile of At (logical (k, m) at word k*BM + m, the
+// As layout, at_word) directly from tensor copies, so the fragment reads are
+// those of As and no shared store is needed.
 //
 #pragma once
 
@@ -46,7 +46,8 @@ constexpr int BN = 128;          // CTA tile cols (N)
 constexpr int BK = 16;           // K depth of one pipeline stage
 constexpr int NT = 256;          // threads per CTA (8 warps)
 constexpr int STAGES = 3;        // copy ring depth (tiles in flight: STAGES - 1)
-constexpr int STAGES_AT = 4;     // ring depth when A arrives k-major (no As buffers)
+constexpr int BK_AT = 32;        // K depth of one stage when A arrives k-major
+constexpr int STAGES_AT = 3;     // ring depth when A arrives k-major (no As buffers)
 constexpr int TM = 8;            // per-thread register tile rows
 constexpr int TN = 8;            // per-thread register tile cols
 constexpr int WARPS_M = 4;       // warp grid over the CTA tile
@@ -65,7 +66,9 @@ constexpr int A_VECS = BM * BK / (4 * NT);  // float4 of A a thread transposes p
 
 static_assert(WARPS_M * WARPS_N * 32 == NT, "warp grid");
 static_assert(WM == 4 * TM && WN == 8 * TN, "lane grid 4 x 8");
-static_assert(STAGES_AT * STAGE_FLOATS <= SMEM_FLOATS, "k-major A ring fits the same block");
+// the k-major ring: per stage a BK_AT x BN tile of B, then a BK_AT x BM tile of At
+constexpr int AT_STAGE_FLOATS = BK_AT * BN + BK_AT * BM;
+constexpr int SMEM_AT_BYTES = STAGES_AT * AT_STAGE_FLOATS * 4 + SMEM_ALIGN;
 static_assert((STAGE_FLOATS * 4) % 128 == 0 && (AS_FLOATS * 4) % 128 == 0, "regions start on a bank row");
 static_assert(NT == 256 && BM == 128 && BK == 16, "A copy and transpose maps cover 128 rows x 16 k");
 
@@ -75,7 +78,8 @@ SG_HD int ar_word(int stage, int m, int k) {
     return stage * STAGE_FLOATS + B_STAGE_FLOATS + m * BK + 4 * ((k >> 2) ^ ((m >> 1) & 3)) + (k & 3);
 }
 SG_HD int as_word(int buf, int k, int m) { return AS_BASE + buf * AS_FLOATS + k * BM + m; }
-SG_HD int at_word(int stage, int k, int m) { return stage * STAGE_FLOATS + B_STAGE_FLOATS + k * BM + m; }
+SG_HD int atb_word(int stage, int k, int n) { return stage * AT_STAGE_FLOATS + k * BN + n; }
+SG_HD int at_word(int stage, int k, int m) { return stage * AT_STAGE_FLOATS + BK_AT * BN + k * BM + m; }
 
 // ---- global->shared copy maps -----------------------------------------
 // A (16-byte class): copy q of thread t moves the 4 floats A[m][k..k+3] with

@@ -123,9 +123,11 @@ int sgemm_f32(int M, int N, int K,
  *      repacked B below if B needs it, the call first transposes A into At
  *      (the transpose_f32 kernel) and runs kernels that load k-major A tiles
  *      straight into the layout the FMA loop reads (128-thread CTAs, 8 x 16
- *      register tiles): no transpose in shared memory and no shared store in
- *      the K loop.  The summation order is
- *      unchanged, so the result equals the call without the copy bit for bit.
+ *      register tiles, K tiles 32 deep): no transpose in shared memory and
+ *      no shared store in the K loop.  With one CTA per tile the summation
+ *      order is unchanged, so the result equals the call without the copy
+ *      bit for bit; the split schedules cut K at multiples of 32 instead of
+ *      16, so there the two agree within FP32 rounding.
  *   repacked rows: otherwise, when A's or B's rows are not 16-byte aligned
  *      and the workspace has room for the schedule plus a copy of that
  *      operand with 16-byte aligned rows (leading dimension rounded up to 4),
@@ -171,11 +173,11 @@ size_t sgemm_f32_workspace_size(int M, int N, int K);
  *     2 GFLOP (2*M*N*K): room for the k-major copy of an unaligned A and the
  *     repacked copy of an unaligned B (smaller products measured faster
  *     without the copies);
- *   - the k-major copy of A pays: its expected saving, 4.5 % of the
- *     product's time at 70 TFLOP/s, exceeds 1.2 times the transpose's time
+ *   - the k-major copy of A pays: its expected saving, 6 % of the
+ *     product's time at 68 TFLOP/s, exceeds 1.2 times the transpose's time
  *     (8*M*K bytes at 5.5 TB/s plus 4 us).  This holds for large N (4096^3:
- *     69.2 -> 71.7 TFLOP/s measured on GB300), not for 16384 x 256 x 4096 or
- *     2048^3.
+ *     69.3 -> 73.0 TFLOP/s measured on GB300; 2048^3: 62.1 -> 64.4), not for
+ *     16384 x 256 x 4096 or 1024^3.
  * The pointers are only inspected for alignment. */
 size_t sgemm_f32_workspace_size_for(int M, int N, int K,
                                     const float *A, int lda,

@@ -21,7 +21,8 @@
  *   iters  : 64 .. 65536 accesses per warp (a multiple of 64).
  *   Access j of every warp's lane l touches word l * stride + 32 * (j % 64)
  *   (below 4096) of a 4096-word int array s[] that holds s[i] = i before the
- *   loop (loads), or -1 (stores, which write the word's own index).
+ *   loop (loads), or -1 (stores, which write the word's own index).  The
+ *   accesses are volatile: each one is issued, none merged or moved.
  *   *cycles_per_access (out): SM clock cycles from the barrier before the
  *       loop to the barrier after it, divided by warps * iters: about the
  *       passes one warp-wide access needs when the shared-memory pipe is the
@@ -55,11 +56,11 @@ int smem_bank_stride_probe(int stride, int op, int warps, int iters, double *cyc
  *   width_bytes : 4, 8 or 16 bytes per lane.
  *   lane_word   : HOST array of 32 word offsets, 0 <= lane_word[l] < 2048,
  *                 each a multiple of width_bytes / 4: lane l reads
- *                 width_bytes bytes at word lane_word[l] + 64 * (j % 8) in
- *                 access j (a shift by 64 words keeps every bank).
+ *                 width_bytes bytes at word lane_word[l] + 32 * (j % 64) in
+ *                 access j (a shift by 32 words keeps every bank).
  *   warps, iters, cycles_per_access : as for smem_bank_stride_probe (loads).
- *   *checksum (out): the sum over all threads of the words read, with s[i] = i
- *                 before the loop.
+ *   *checksum (out): the sum over all threads of the first word of each
+ *                 vector read, with s[i] = i before the loop.
  * Synchronous; the same status codes as smem_bank_stride_probe.
  */
 int smem_bank_pattern_probe(int width_bytes, const int *lane_word, int warps, int iters,

@@ -8,7 +8,9 @@ broadcast mixes, and the exact lane offsets of the product kernels' own
 fragment reads.  Their measured counts are in lds_wavefronts_heldout_sm103.txt,
 and tests/test_bank_model.py checks that the unchanged model predicts them.
 
-Run on a GPU, this script launches smem_bank_pattern_probe once per pattern,
+Run on a GPU, this script launches smem_bank_pattern_probe once per pattern
+(each lane's word offsets are what the probe reads, shifted by whole bank
+rows between accesses),
 in the order of PATTERNS, so that
 
     ncu --clock-control none -k regex:bank_pattern_kernel \\
@@ -43,7 +45,7 @@ EXPRS = [
 KERNEL_READS = [
     (2, 5, 7, 1, "8 x 8 kernels, A fragment read"),
     (3, 6, 20, 2, "8 x 8 kernels, B fragment read"),
-    (11, 2, 9, 3, "k-major 8 x 16 kernels, A fragment read"),
+    (11, 2, 9, 2, "k-major 8 x 16 kernels, A fragment read"),
     (12, 3, 37, 1, "k-major 8 x 16 kernels, B fragment read"),
 ]
 WIDE = [(w, e) for e in EXPRS for w in (16, 8)]

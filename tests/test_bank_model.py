@@ -141,3 +141,51 @@ def test_measured_stride_sweep_matches_gcd_law_and_model(oracle_lib):
             assert r["wavefronts"] == wavefronts
             seen.add((op, stride))
     assert seen == {(op, s) for op in ("lds32", "sts32") for s in range(1, 34)}
+
+
+def _heldout():
+    import sys
+    sys.path.insert(0, os.path.join(HERE, "golden"))
+    import lds_heldout_patterns as P
+    measured = {}
+    with open(os.path.join(HERE, "golden", "lds_wavefronts_heldout_sm103.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                name, val = line.rsplit("=", 1)
+                measured[name.strip()] = int(val)
+    return P, measured
+
+
+def test_heldout_wide_load_wavefronts(oracle_lib):
+    # patterns chosen after the wide-access rule was fitted (new permutations,
+    # strided and broadcast mixes, and the product kernels' own fragment
+    # reads, as the library reports them); the unchanged rule must predict
+    # every measured count
+    pytest.importorskip("ctypes")
+    from dense_fp32_tiled_gb300 import build as sg_build
+    import dense_fp32_tiled_gb300 as sg
+    sg_build.build()
+    sg.load_library()
+    P, measured = _heldout()
+    pats = P.patterns()
+    assert len(pats) == len(measured) >= 30
+    widths = {w for _, w, _ in pats}
+    assert widths == {4, 8, 16}
+    for name, width, words in pats:
+        r = oracle_lib.shared_request([4 * x for x in words], width)
+        assert r["wavefronts"] == measured[name], (name, r, measured[name])
+
+
+def test_heldout_patterns_are_new():
+    # none of the held-out expressions is one of the fitted ones
+    P, _ = _heldout()
+    fitted = set()
+    with open(os.path.join(HERE, "golden", "lds_wavefronts_sm103.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                w, expr = line.split("=")[0].split(None, 1)
+                fitted.add((int(w), expr.strip().replace(" ", "")))
+    for w, e in P.WIDE + P.NARROW:
+        assert (w, e.replace(" ", "")) not in fitted, (w, e)

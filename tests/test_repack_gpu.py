@@ -96,19 +96,31 @@ def test_copied_operands_match_the_oracle(oracle_lib, M, N, K, lda, ldb, ldc, a_
     tol.assert_close(C, Cr, Sr, K, f"copied {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(129, 1030, 2049), (61, 300, 1025)])
-def test_room_for_the_row_repack_only(oracle_lib, M, N, K):
+@pytest.mark.parametrize("tiles_m,K", [(8, 1023), (4, 511)])
+def test_room_for_the_row_repack_only(oracle_lib, tiles_m, K):
     """A workspace with room for the row repack of A but not for its k-major
-    copy takes the row repack.  129 x 2049 repacks into 2052-float rows
-    (1.06 MB), its k-major copy needs 2049 rows of 132 floats (1.08 MB)."""
+    copy takes the row repack.  The tiles are exactly one wave of the CTAs the
+    GPU holds at once (2 per SM), so both kernel families run one CTA per
+    tile and the schedule needs no workspace; M = 1 and K = 3 (mod 4) with
+    3K > M make the k-major copy (K rows of M rounded up to 4) larger than the
+    row repack (M rows of K rounded up to 4)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if (2 * sms) % tiles_m:
+        pytest.skip("the SM count does not split into whole tile columns")
+    M, N = 128 * tiles_m - 3, 128 * (2 * sms // tiles_m)
+    assert M % 4 == 1 and K % 4 == 3 and 3 * K > M
     assert _a_kmajor(M, K) > _a_repack(M, K)
-    nbytes = sg.workspace_size(M, N, K) + _a_repack(M, K) + (_b_repack(K, N) if N % 4 else 0)
+    nbytes = _a_repack(M, K)
     A = synth.matrix(M, K, 352, 0, ld=K, pad_value=np.nan)
     B = synth.matrix(K, N, 352, 1, ld=N, pad_value=np.nan)
     C, kind = _run(M, N, K, A, K, B, N, N, nbytes=nbytes)
-    assert kind & 28 == 4 | (8 if N % 4 else 0)
+    assert kind == 4, kind  # one CTA per tile, A row-repacked
     Cr, Sr = oracle_lib.gemm(A, B, M=M, N=N, K=K, lda=K, ldb=N)
     tol.assert_close(C, Cr, Sr, K, f"row-repacked {M}x{N}x{K}")
+    # with room for the k-major copy as well, that copy is taken instead
+    C2, kind2 = _run(M, N, K, A, K, B, N, N, nbytes=_a_kmajor(M, K))
+    assert kind2 == 16, kind2
+    tol.assert_close(C2, Cr, Sr, K, f"k-major {M}x{N}x{K}")
 
 
 def test_repacked_integer_exact_and_same_as_aligned_copy(oracle_lib):
@@ -141,13 +153,18 @@ def test_smaller_workspace_keeps_the_unrepacked_path(oracle_lib):
 
 
 def test_size_query_asks_for_repack_room_only_for_large_products():
+    # unaligned rows: room for the copies from 2 GFLOP on; aligned rows: room
+    # only where the k-major copy pays on its own (2048 x 2048 x 2049 does,
+    # 1536^3 and the ragged product do not)
     from tests._gpu import dev_buffer
-    for (M, N, K), large in (((1000, 1030, 777), False), ((2048, 2048, 2049), True), ((1536, 1536, 1537), True)):
+    for (M, N, K), large, pays in (((1000, 1030, 777), False, False), ((2048, 2048, 2049), True, True),
+                                   ((1536, 1536, 1537), True, False)):
         tA, pA = dev_buffer(np.zeros(4, np.float32))
         base = sg.workspace_size(M, N, K)
         got = sg.workspace_size_for(M, N, K, pA, K, pA, N)
         assert (got > base) == large, (M, N, K)
-        assert sg.workspace_size_for(M, N, K, pA, (K + 3) // 4 * 4, pA, (N + 3) // 4 * 4) == base
+        aligned = sg.workspace_size_for(M, N, K, pA, (K + 3) // 4 * 4, pA, (N + 3) // 4 * 4)
+        assert (aligned > base) == pays, (M, N, K)
 
 
 def test_torch_wrapper_uses_the_repack(oracle_lib):

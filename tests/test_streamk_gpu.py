@@ -112,7 +112,7 @@ def test_words_past_the_used_ones_are_untouched():
     tA, pA = dev_buffer(A)
     tB, pB = dev_buffer(B)
     C = torch.empty(M, N, device="cuda")
-    nbytes = sg.workspace_size(M, N, K)  # no room to repack A
+    nbytes = (_tiles(M, N) + 1) * 4  # schedule 1's flags only: no room to copy A
     sst, kind, used = sg.ws_schedule(M, N, K, pA, K, pB, N, C.data_ptr(), N, nbytes)
     assert sst == 0 and kind == 1 and used == _tiles(M, N) + 1
     ws = torch.full((nbytes // 4 + 8,), 7, dtype=torch.int32, device="cuda")
