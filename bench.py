@@ -359,7 +359,8 @@ def main():
         if st != 0:
             raise sg.SgemmError(st)
     # kernels of ours per step: schedule 3 runs a one-CTA-per-tile grid and a
-    # split-tail grid; each copied operand (bits 4, 8: rows repacked; 16: A
+    # split-tail grid, the others (bit 32, the cluster split of K, included)
+    # one grid; each copied operand (bits 4, 8: rows repacked; 16: A
     # transposed into its k-major copy) adds its copy kernel
     _, sched_kind, _ = sg.ws_schedule(w.M, w.N, w.K, A.data_ptr(), w.lda, B.data_ptr(), w.ldb, C.data_ptr(), w.ldc,
                                       ws_bytes)
@@ -451,6 +452,9 @@ def main():
                     ("sgemm_f32_tiled_kernel", "sgemm_f32_tail_kernel"))
         roofline["kernels"] = (f"{dp} (whole waves) + {tail} (leftover tiles in K parts), overlapped; achieved and "
                                "traffic cover the whole step")
+    if sched_kind & 32:
+        roofline["kernels"] = ("sgemm_f32_clusterk_kernel: clusters of CTAs split each tile's K, partial sums added "
+                               "through distributed shared memory; achieved covers the whole step")
     if sched_kind & 12:
         roofline["repack"] = ("repack_rows_kernel copies " + " and ".join(
             n for n, bit in (("A", 4), ("B", 8)) if sched_kind & bit) +

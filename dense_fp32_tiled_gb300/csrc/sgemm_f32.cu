@@ -385,6 +385,112 @@ __global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p,
     store_tile<false>(p, tm * BM, tn * BN, acc);
 }
 
+// ---- cluster split of K ----------------------------------------------------
+// For products with few tiles (at most half the CTAs the GPU holds at once) a
+// cluster of S CTAs (2 <= S <= 8) computes one tile of C: CTA r of the
+// cluster accumulates K tiles [KT r / S, KT (r+1) / S) with the 8 x 8
+// kernels' main loop, leaves its partial sums in its own shared memory (the
+// ring's space, pt_word layout), and after a cluster barrier sums rows
+// [128 r / S, 128 (r+1) / S) of the tile over the S CTAs' shared memory
+// (distributed shared memory, in rank order, so the result does not depend
+// on timing) and stores them to C.  A second cluster barrier keeps every
+// CTA's shared memory alive until its peers have read it.  No workspace, no
+// flags and no wait between CTAs other than the hardware's cluster barrier.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(n));
+    return n;
+}
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// The address of shared-memory address `addr` of this CTA in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+// Stores 4 consecutive values of row `row` of C from column `col` on,
+// guarded by M and N, with the widest stores C's alignment class allows.
+__device__ __forceinline__ void store_c4(const Problem &p, const int row, const int col, const float4 v) {
+    if (row >= p.M || col >= p.N) return;
+    float *c = p.C + static_cast<size_t>(row) * p.ldc + col;
+    if (col + 3 < p.N && p.vc == 4) {
+        *reinterpret_cast<float4 *>(c) = v;
+    } else if (col + 3 < p.N && p.vc == 2) {
+        *reinterpret_cast<float2 *>(c) = make_float2(v.x, v.y);
+        *reinterpret_cast<float2 *>(c + 2) = make_float2(v.z, v.w);
+    } else {
+        const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (col + i < p.N) c[i] = e[i];
+    }
+}
+
+template <int VA, int VB, bool TMA>
+__global__ void __launch_bounds__(NT, 2) sgemm_f32_clusterk_kernel(const Problem p, const __grid_constant__ Maps maps) {
+    extern __shared__ float smem_raw[];
+    __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
+    float *smem = aligned_smem(smem_raw);
+    const uint32_t bars = smem_u32(bar_mem);
+    init_bars<TMA>(bars);
+    const int S = static_cast<int>(cluster_nctarank());
+    const int rank = static_cast<int>(cluster_ctarank());
+    int tm, tn;
+    tile_of(static_cast<int>(blockIdx.x) / S, p.tiles_m, p.tiles_n, tm, tn);
+    const int KT = (p.K + BK - 1) / BK;
+    const int k0 = static_cast<int>(static_cast<long long>(KT) * rank / S);
+    const int k1 = static_cast<int>(static_cast<long long>(KT) * (rank + 1) / S);
+    Acc acc;
+    acc_zero(acc);
+    uint32_t pipe = 0;
+    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
+    __syncthreads();  // every thread is done with the ring: its space becomes the partial tile
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int q = 0; q < 2 * TM; ++q) {
+        int row, col;
+        pt_store_coord(tid, q, row, col);
+        const int i = q >> 1, h = q & 1;
+        *reinterpret_cast<float4 *>(smem + pt_word(row, col)) =
+            make_float4(acc.c[i][2 * h].x, acc.c[i][2 * h].y, acc.c[i][2 * h + 1].x, acc.c[i][2 * h + 1].y);
+    }
+    cluster_barrier();  // every CTA's partial tile is complete and visible to the cluster
+    // this CTA sums rows [r0, r1) of the tile
+    const int r0 = BM * rank / S, r1 = BM * (rank + 1) / S;
+    const uint32_t base = smem_u32(smem);
+    for (int j = 0;; ++j) {
+        int row, col;
+        pt_sum_coord(tid, j, r0, row, col);
+        if (row >= r1) break;
+        const uint32_t addr = base + static_cast<uint32_t>(pt_word(row, col)) * 4u;
+        float4 sum = ld_dsmem_f4(map_peer(addr, 0));
+        for (int q = 1; q < S; ++q) {
+            const float4 v = ld_dsmem_f4(map_peer(addr, static_cast<uint32_t>(q)));
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+        }
+        store_c4(p, tm * BM + row, tn * BN + col, sum);
+    }
+    cluster_barrier();  // no CTA leaves while a peer may still read its shared memory
+}
+
 // ---- k-major kernels with 8 x 16 register tiles --------------------------
 // The one-CTA-per-tile and split-tail kernels of the k-major path: 128
 // threads (2 x 2 warps of 64 x 64), each holding an 8 x 16 register tile,
@@ -923,6 +1029,12 @@ const SkKernel kSk[kVariants] = {
     sgemm_f32_streamk_kernel<4, 1, false>, sgemm_f32_streamk_kernel<1, 4, false>,
     sgemm_f32_streamk_kernel<1, 2, false>, sgemm_f32_streamk_kernel<1, 1, false>,
     sgemm_f32_streamk_kernel<4, 4, true>,  sgemm_f32_kmajor_streamk_kernel};
+// The cluster split of K for the 8 x 8 variants (none for the k-major one).
+const DpKernel kCk[kVariants] = {
+    sgemm_f32_clusterk_kernel<4, 4, false>, sgemm_f32_clusterk_kernel<4, 2, false>,
+    sgemm_f32_clusterk_kernel<4, 1, false>, sgemm_f32_clusterk_kernel<1, 4, false>,
+    sgemm_f32_clusterk_kernel<1, 2, false>, sgemm_f32_clusterk_kernel<1, 1, false>,
+    sgemm_f32_clusterk_kernel<4, 4, true>,  nullptr};
 using TailKernel = void (*)(Problem, Maps, int, int, unsigned *, float *);
 // tensor-copy variants only: [0] A row-major, [1] A k-major (8 x 16 tiles)
 const TailKernel kTail[2] = {sgemm_f32_tail_kernel<4, 4, true>, sgemm_f32_kmajor_tail_kernel};
@@ -1109,6 +1221,13 @@ int setup_device(int dev, DeviceInfo *out) {
                     st = SGEMM_ERR_DEVICE;
                 d.sk_per_sm[v] = sk < dp ? sk : dp;
             }
+            for (int v = 0; v < kVariants && st == SGEMM_OK; ++v)
+                if (kCk[v] != nullptr &&
+                    (cudaFuncSetAttribute(kCk[v], cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+                         cudaSuccess ||
+                     cudaFuncSetAttribute(kCk[v], cudaFuncAttributePreferredSharedMemoryCarveout,
+                                          cudaSharedmemCarveoutMaxShared) != cudaSuccess))
+                    st = SGEMM_ERR_DEVICE;
             // the one-CTA-per-tile kernels may be launched with the padded
             // request of the cta_per_sm=1 diagnostic
             for (int v = 0; v < kVariants && st == SGEMM_OK; ++v)
@@ -1378,6 +1497,30 @@ Plan effective_plan(long long T, long long KT, long long G, long long sms, bool 
     return pl;
 }
 
+// Cluster size of the cluster split of K for T output tiles of KT K tiles
+// with G CTAs resident at once, or 0 when it does not apply: products with at
+// most G / 2 tiles (the split then fills the GPU without a second wave), at
+// least 2 K tiles per CTA, on the 8 x 8 kernels (variant v).  S = the most
+// CTAs per tile that keep all of them resident, at most 8 (the portable
+// cluster size).  When the stream-K schedule over all tiles could run instead
+// (`streamk`: the workspace has room for it), the split is taken only if its
+// CTAs get at most 3 K tiles more than stream-K's: measured on GB300, the
+// split saves stream-K's fixed costs (flag memset, hand-over waits, the
+// owner's serial sum of the parts), worth about 3 K tiles of one CTA
+// (1024^3: 53.1 -> 49.5 us, S = 4, 16 K tiles per CTA against 13.5; 256^3
+// 20.2 -> 12.8 us; 512^3 22.6 -> 20.8 us), and loses when its grid leaves
+// more slots empty (2048 x 1024 x 1024: S = 2, 32 K tiles per CTA against 27,
+// 82.6 -> 88.4 us).  SGEMM_F32_TUNE schedule=0..3 turns it off.
+int cluster_split(long long T, long long KT, long long G, int v, bool streamk) {
+    if (v >= kAtVariant || kCk[v] == nullptr || tune().schedule >= 0 || T <= 0 || 2 * T > G) return 0;
+    long long S = G / T;
+    if (S > 8) S = 8;
+    if (S > KT / 2) S = KT / 2;
+    if (S < 2) return 0;
+    if (streamk && static_cast<double>((KT + S - 1) / S) > static_cast<double>(T * KT) / G + 3.0) return 0;
+    return static_cast<int>(S);
+}
+
 // Runs one product whose arguments passed check_args (M, N > 0).  Uses a
 // stream-K schedule when the workspace `flags` (flag_bytes long) is large
 // enough for the plan chosen for this shape; else one CTA per tile.
@@ -1459,6 +1602,23 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem_of(v);
     cfg.stream = stream;
+    const bool streamk = flags != nullptr && pl.kind == 2 && flag_bytes >= pl.bytes;
+    if (const int S = cluster_split(T, KT, G, v, streamk)) {
+        sg_nvtx::Range r("sgemm_f32: cluster split of K");
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(S);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(T * S));
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kCk[v], p, maps) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_LAUNCH;
+        }
+        return SGEMM_OK;
+    }
     if (pl.kind == 3) {
         if (flags != nullptr && flag_bytes >= pl.bytes) {
             unsigned *counts = flags;
@@ -1644,9 +1804,15 @@ extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int ld
         v = choose_variant(M, N, K, A, lda, B, ldb, maps);
     }
     const size_t avail = (rp.a || rp.b || rp.at) ? rp.plan_bytes : workspace_bytes;
-    const Plan pl = effective_plan(tile_count(M, N), (K + bk_of(v) - 1) / bk_of(v),
-                                   static_cast<long long>(info.sk_per_sm[v]) * info.sms, info.sms, is_tma(v), avail);
-    *kind = pl.kind | (rp.a ? 4 : 0) | (rp.b ? 8 : 0) | (rp.at ? 16 : 0);
+    const long long T = tile_count(M, N), KT = (K + bk_of(v) - 1) / bk_of(v);
+    const long long G = static_cast<long long>(info.sk_per_sm[v]) * info.sms;
+    const int copies = (rp.a ? 4 : 0) | (rp.b ? 8 : 0) | (rp.at ? 16 : 0);
+    const Plan pl = effective_plan(T, KT, G, info.sms, is_tma(v), avail);
+    if (K > 0 && cluster_split(T, KT, G, v, pl.kind == 2)) {
+        *kind = 32 | copies;  // cluster split of K: no schedule words
+        return SGEMM_OK;
+    }
+    *kind = pl.kind | copies;
     *words = pl.flag_words;
     return SGEMM_OK;
 }
@@ -1712,11 +1878,13 @@ extern "C" int sgemm_f32_smem_shape(int kind, int *n_warps, int *n_steps, int *n
         case 6: steps = A_COPIES4; break;
         case 7: steps = A_VECS; break;
         case 8: steps = 4 * A_VECS; break;
+        case 13: steps = 2 * TM; break;
+        case 14: steps = BM / (NT / 32); break;
         default: return SGEMM_ERR_INVALID_ARG;
     }
-    if (n_warps) *n_warps = kind >= 11 ? NT16 / 32 : NT / 32;
+    if (n_warps) *n_warps = (kind == 11 || kind == 12) ? NT16 / 32 : NT / 32;
     if (n_steps) *n_steps = steps;
-    if (n_stages) *n_stages = (kind == 2 || kind == 8) ? 2 : kind >= 11 ? STAGES_AT : STAGES;
+    if (n_stages) *n_stages = (kind == 2 || kind == 8) ? 2 : kind >= 13 ? 1 : kind >= 11 ? STAGES_AT : STAGES;
     return SGEMM_OK;
 }
 
@@ -1743,6 +1911,8 @@ extern "C" int sgemm_f32_smem_request(int kind, int warp, int step, int stage, i
             case 3: word = bs_word(stage, step >> 1, frag_col0(tid) + 32 * (step & 1)); width = 16; break;
             case 11: word = at_word(stage, step >> 1, frag16_row0(tid) + 32 * (step & 1)); width = 16; break;
             case 12: word = atb_word(stage, step >> 2, frag16_col0(tid) + 16 * (step & 3)); width = 16; break;
+            case 13: pt_store_coord(tid, step, x, k); word = pt_word(x, k); width = 16; break;
+            case 14: pt_sum_coord(tid, step, 0, x, k); word = pt_word(x, k); width = 16; break;
         }
         byte_offset[lane] = static_cast<int64_t>(word) * 4;
     }

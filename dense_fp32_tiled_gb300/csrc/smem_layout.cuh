@@ -160,6 +160,28 @@ SG_HD int frag16_row(int tid, int i) { return frag16_row0(tid) + (i & 3) + 32 * 
 SG_HD int frag16_col(int tid, int j) { return frag16_col0(tid) + (j & 3) + 16 * (j >> 2); }
 static_assert(NT16 == 4 * 32 && 2 * (8 * 4 * 2) == BM && 2 * (4 * 4 * 4) == BN, "2 x 2 warps of 64 x 64");
 
+// ---- partial tile of the cluster split of K --------------------------------
+// After its K loop each CTA of a cluster leaves its 128 x 128 partial sums in
+// its own shared memory (reusing the ring), logical (row, col) at
+// row*BN + 4*((col/4) ^ (row % 8)) + col % 4: the 8 x 8 threads' 128-bit
+// stores (a quarter-warp: 2 rows x 4 column groups, rows 4 apart) fall on 8
+// distinct bank groups, and a warp reading one row (32 groups) needs the
+// minimum 4 passes.
+SG_HD int pt_word(int row, int col) { return row * BN + 4 * ((col >> 2) ^ (row & 7)) + (col & 3); }
+static_assert(BM * BN <= SMEM_FLOATS, "the partial tile fits the shared block");
+// Store q (0 .. 2 TM - 1) of thread tid: row q/2 of its 8 x 8 tile, the four
+// columns of half q%2.
+SG_HD void pt_store_coord(int tid, int q, int &row, int &col) {
+    row = frag_row(tid, q >> 1);
+    col = frag_col0(tid) + 32 * (q & 1);
+}
+// Read j of thread tid when summing the rows from r0 on: warp w takes rows
+// r0 + w, r0 + w + 8, ..., lane l the columns 4 l .. 4 l + 3.
+SG_HD void pt_sum_coord(int tid, int j, int r0, int &row, int &col) {
+    row = r0 + (tid >> 5) + (NT / 32) * j;
+    col = 4 * (tid & 31);
+}
+
 // ---- tile rasterisation ------------------------------------------------
 // Linear CTA index -> (tile row, tile col), walking GROUP_M tile rows at a
 // time so CTAs resident together share A row panels and B column panels.

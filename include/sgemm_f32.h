@@ -62,6 +62,14 @@ typedef enum {
  * its row stride.  The caller owns all memory; A and B are only read, C is
  * only written.  C must not overlap A or B (checked on address ranges).
  *
+ * Schedule: one CTA per 128 x 128 output tile; or, for products with at
+ * most G / 2 tiles (G = 2 CTAs per SM) and at least 4 K tiles of 16, the
+ * cluster split of K: each tile runs on a thread-block cluster of S CTAs
+ * (S = min(G / tiles, 8, K tiles / 2)), CTA r summing K tiles
+ * [KT r / S, KT (r+1) / S); the S partial tiles stay in shared memory and
+ * are added in rank order over distributed shared memory, so the result does
+ * not depend on timing.  Either way one kernel launch, no device memory.
+ *
  * Edge cases: M == 0 or N == 0 returns SGEMM_OK without launching anything.
  * K == 0 sets C to zero (the empty sum); A and B may then be NULL.
  *
@@ -106,6 +114,11 @@ int sgemm_f32(int M, int N, int K,
  *      as SMs free up; the part that finishes a tile last adds all parts
  *      (one count per leftover tile, then S * R slots of 64 KiB).
  *   0  otherwise, or with a smaller workspace: exactly as sgemm_f32.
+ * The cluster split of K (see sgemm_f32) takes precedence where it applies,
+ * except over schedule 2 when that gives its CTAs more than 3 K tiles fewer
+ * each (measured on GB300: the cluster split saves schedule 2's flag reset,
+ * hand-over waits and serial sum of the parts, worth about 3 K tiles of one
+ * CTA); it uses no workspace.
  * sgemm_f32_workspace_size reports the bytes for the current device.  The
  * call zero-fills the words it uses at the start of the workspace on
  * `stream` before the kernels, so the workspace needs no preparation and its
@@ -149,8 +162,10 @@ int sgemm_f32_ws(int M, int N, int K,
 /* What sgemm_f32_ws would run for these arguments on the current device
  * with a workspace of workspace_bytes bytes (host-only; launches nothing):
  * *kind = the schedule (0 to 3, as listed above) in bits 0-1, plus 4 if A is
- * repacked, 8 if B is repacked and 16 if A is transposed into its k-major
- * copy; *words = the 32-bit words at the start of
+ * repacked, 8 if B is repacked, 16 if A is transposed into its k-major copy
+ * and 32 for the cluster split of K (then bits 0-1 are 0 and *words is 0);
+ * with workspace_bytes = 0 it reports what sgemm_f32 runs.
+ * *words = the 32-bit words at the start of
  * the workspace that the call zero-fills and leaves zero on success (flags
  * and error word, or tile counts).  Returns the argument-check status of
  * sgemm_f32_ws, or SGEMM_ERR_DEVICE without a usable device. */
@@ -339,13 +354,19 @@ const char *sgemm_f32_status_string(int status);
  *          7 = A transpose read (raw tile -> registers, 16-byte),
  *          8 = A transpose store (registers -> k-major tile, 4-byte),
  *          2 = A fragment read (16-byte), 3 = B fragment read (16-byte);
- *          with the k-major copy of A (no transpose, a 4-deep ring, 8 x 16
+ *          with the k-major copy of A (no transpose, a 3-deep ring, 8 x 16
  *          register tiles, 4 warps): 11 = A fragment read from the ring
- *          stage, 12 = B fragment read.
+ *          stage, 12 = B fragment read;
+ *          the cluster split of K (one stage): 13 = a CTA's store of its
+ *          partial 128 x 128 tile, 14 = the read of one row of a partial
+ *          tile when the cluster sums them (the rows from 0 on; a CTA's
+ *          range starts at another row, which shifts every lane alike).
  *   warp : warp index in the CTA, 0 <= warp < *n_warps.
  *   step : which instruction of that warp, 0 <= step < *n_steps (copies,
  *          transpose reads and stores: index within one tile; fragment
- *          reads: 2*k + half, k < BK; kind 12: 4*k + quarter).
+ *          reads: 2*k + half, k < BK; kind 12: 4*k + quarter; kind 13:
+ *          2*i + half, row i of the thread's 8 x 8 tile; kind 14: the j-th
+ *          row of the warp, row 8*j + warp).
  *   stage: ring stage (copies, transpose reads, B reads, kinds 11 and 12)
  *          or k-major buffer (A reads, transpose stores) the access targets,
  *          0 <= stage < *n_stages.

@@ -5,9 +5,10 @@ rows) and through the 3xTF32 variant, against the FP64 oracle (needs a
 GB300).
 
 Shapes are drawn log-uniformly so that small products (one CTA per tile,
-multi-part split), products with a partial last wave (split tail or two-part
-split) and copied operands all occur; the test asserts that each of them
-did.  Large products are checked on seeded sampled outputs, the rest in full.
+multi-part split, cluster split of K), products with a partial last wave
+(split tail or two-part split) and copied operands all occur; the test
+asserts that each of them did.  Large products are checked on seeded
+sampled outputs, the rest in full.
 """
 import numpy as np
 import pytest
@@ -82,7 +83,7 @@ def test_random_shapes_every_schedule(oracle_lib):
         sst, kind, words = sg.ws_schedule(M, N, K, pA, lda, pB, ldb, pC, ldc, nbytes)
         assert sst == 0
         seen.add(kind & 3)
-        seen |= {b for b in (4, 8, 16) if kind & b}
+        seen |= {b for b in (4, 8, 16, 32) if kind & b}
         what = f"case {i}: {M}x{N}x{K} ld {lda},{ldb},{ldc} off {oa},{ob},{oc} kind {kind}"
         assert sg.sgemm_f32_ws(M, N, K, pA, lda, pB, ldb, pC, ldc, ws.data_ptr(), nbytes, s) == 0, what
         torch.cuda.synchronize()
@@ -100,5 +101,5 @@ def test_random_shapes_every_schedule(oracle_lib):
             raw = tC.cpu().numpy()[oc:oc + c_elems]
             C = np.stack([raw[r * ldc:r * ldc + N] for r in range(M)])
             _check(oracle_lib, A, B, C, M, N, K, lda, ldb, "3xTF32 " + what, 500 + i)
-    assert {0, 1, 2, 3, 8, 16} <= seen, f"schedules and copies seen: {sorted(seen)}"
+    assert {0, 1, 2, 3, 8, 16, 32} <= seen, f"schedules and copies seen: {sorted(seen)}"
     assert sg.copy_timeouts() == 0 and sg.tc_timeouts() == 0

@@ -166,9 +166,12 @@ def test_alias_rejected_with_device_pointers():
 
 
 def test_transpose_identity(oracle_lib):
-    # (A.B)^T = B^T.A^T.  One CTA per tile sums each output's FMAs in k order,
-    # so the two agree bit for bit; the balanced schedule cuts K at points that
-    # depend on the tile's position, so there they agree to FP32 rounding.
+    # (A.B)^T = B^T.A^T.  Without a workspace every output's FMAs run in k
+    # order within K parts whose cut points depend only on the tile and K-tile
+    # counts (one part, or one per CTA of a cluster), the same for both
+    # products here (6 tiles each), so the two agree bit for bit; the balanced
+    # schedule cuts K at points that depend on the tile's position, so there
+    # they agree to FP32 rounding.
     An = synth.matrix(300, 200, 8, 0, "normal")
     Bn = synth.matrix(200, 170, 8, 1, "normal")
     A, B = torch.from_numpy(An).cuda(), torch.from_numpy(Bn).cuda()

@@ -16,7 +16,8 @@ from dense_fp32_tiled_gb300 import build as sg_build
 KINDS = {0: "A copy (16 B)", 1: "B copy (16 B)", 2: "A fragment read", 3: "B fragment read",
          4: "B copy (8 B)", 5: "B copy (4 B)", 6: "A copy (4 B)", 7: "A transpose read",
          8: "A transpose store", 11: "A fragment read (k-major copy of A, 8 x 16 tiles)",
-         12: "B fragment read (k-major copy of A, 8 x 16 tiles)"}
+         12: "B fragment read (k-major copy of A, 8 x 16 tiles)",
+         13: "partial tile store (cluster split of K)", 14: "partial tile row read (cluster split of K)"}
 
 
 @pytest.fixture(scope="module")
@@ -89,10 +90,35 @@ def test_fragment_reads_stay_inside_their_tile(lib):
                 assert all(o % 16 == 0 for o in offs)
 
 
+def test_cluster_partial_tile_written_and_read_once(lib):
+    # the stores of a CTA's 8 x 8 accumulators cover the 128 x 128 partial
+    # tile word for word, and the row reads of the sum (all 128 rows) read
+    # back exactly those words, 16 bytes at a time
+    def words(kind):
+        n_warps, n_steps, n_stages = sg.smem_shape(kind)
+        assert n_stages == 1
+        out = []
+        for warp in range(n_warps):
+            for step in range(n_steps):
+                offs, width = sg.smem_request(kind, warp, step, 0)
+                assert width == 16 and all(o % 16 == 0 for o in offs)
+                out += [o // 4 + w for o in offs for w in range(4)]
+        return out
+    stored, read = words(13), words(14)
+    assert len(stored) == 128 * 128 and sorted(stored) == list(range(128 * 128))
+    assert sorted(read) == sorted(stored)
+    # a row read covers exactly its row (words 128 r .. 128 r + 127)
+    for warp in range(8):
+        for step in range(16):
+            offs, _ = sg.smem_request(14, warp, step, 0)
+            row = 8 * step + warp
+            assert sorted(o // 4 for o in offs) == list(range(128 * row, 128 * row + 128, 4))
+
+
 def test_bad_query_rejected(lib):
     with pytest.raises(sg.SgemmError):
         sg.smem_request(9, 0, 0, 0)
     with pytest.raises(sg.SgemmError):
-        sg.smem_request(13, 0, 0, 0)
+        sg.smem_request(15, 0, 0, 0)
     with pytest.raises(sg.SgemmError):
         sg.smem_request(0, 8, 0, 0)

@@ -172,10 +172,12 @@ def _plan_words(M, N, K, pA, lda, pB, ldb, pC, ldc):
     return words
 
 
+# Products with at most G / 2 tiles take the cluster split of K instead when
+# its CTAs get at most 3 K tiles more than stream-K's (test_clusterk_gpu.py);
+# these shapes keep the multi-part split.
 @pytest.mark.parametrize("M,N,K,lds,kind", [
-    (1024, 1024, 1024, None, "normal"),          # 64 tiles
-    (1000, 1030, 777, (777, 1030, 1030), "uniform"),  # 72 tiles, misaligned rows: cp.async path
-    (256, 256, 256, None, "uniform"),            # 4 tiles
+    (2048, 1024, 1024, None, "normal"),          # 128 tiles
+    (1000, 2470, 333, (333, 2470, 2470), "uniform"),  # 160 tiles, misaligned rows: cp.async path
     (2048, 256, 4096, None, "normal"),           # 32 tiles, deep K
 ])
 def test_multipart_split_full_check(oracle_lib, M, N, K, lds, kind):
@@ -204,7 +206,7 @@ def test_multipart_split_full_check(oracle_lib, M, N, K, lds, kind):
 
 
 def test_multipart_integer_exact_and_deterministic(oracle_lib):
-    M, N, K = 1024, 768, 2048
+    M, N, K = 2048, 1024, 1024
     A = synth.matrix(M, K, 47, 0, "int5")
     B = synth.matrix(K, N, 47, 1, "int5")
     tA, tB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
