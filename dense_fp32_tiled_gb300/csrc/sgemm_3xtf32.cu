@@ -444,6 +444,20 @@ sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, 
         SegIter seg(pair, pl);
         int t, kb0, kb1;
         while (seg.next(pl, t, kb0, kb1)) {
+            // a stream-K tile cut between pairs: its parts (pairs p_first ..
+            // p_first + nparts - 1) and their slots, worked out before the
+            // sums occupy the registers.  Pair p > p_first starts its range
+            // inside tile ts, so its slot is 2 p; only p_first's depends on
+            // where its range began.
+            const bool cut = kb0 != 0 || kb1 != pl.NB;
+            int p_first = 0, nparts = 0, first_slot = 0, my_slot = 0;
+            if (cut) {
+                const int ts = t - pl.dp_tiles;
+                p_first = pair_of_unit(ts * pl.NB, pl);
+                nparts = pair_of_unit((ts + 1) * pl.NB - 1, pl) - p_first + 1;
+                first_slot = part_slot(p_first, ts, pl);
+                my_slot = part_slot(pair, ts, pl);
+            }
             float total[EPI_COLS];
 #pragma unroll
             for (int c = 0; c < EPI_COLS; ++c) total[c] = 0.0f;
@@ -466,12 +480,8 @@ sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, 
                 if (lane == 0) mbar_arrive_cluster(empty0 + 8u * set);
             }
             bool store = true;
-            if (kb0 != 0 || kb1 != pl.NB) {
-                // a stream-K tile cut between pairs: hand over or finish
-                const int ts = t - pl.dp_tiles;
-                const int p_first = pair_of_unit(ts * pl.NB, pl), p_last = pair_of_unit((ts + 1) * pl.NB - 1, pl);
-                const int nparts = p_last - p_first + 1;
-                float *mine = partials + (static_cast<size_t>(part_slot(pair, ts, pl)) * 2 + rank) * SLOT_FLOATS;
+            if (cut) {  // hand over or finish
+                float *mine = partials + (static_cast<size_t>(my_slot) * 2 + rank) * SLOT_FLOATS;
 #pragma unroll
                 for (int c = 0; c < EPI_COLS; c += 4) {
                     const int chunk = (h * (EPI_COLS) + c) / 4;
@@ -488,26 +498,42 @@ sgemm_3xtf32_kernel(const __grid_constant__ TcMaps maps, float *__restrict__ C, 
                     last_part = before == static_cast<unsigned>(nparts - 1) ? 1 : 0;
                 }
                 epi_bar();
-                store = last_part != 0;
-                if (store) {
-                    // C = sum of the parts in part order, all read back from the workspace
+                if (last_part != 0) {
+                    // C = the sum of the parts in part order, read back from
+                    // the workspace four columns at a time and stored at once
+                    // (the running sums of all columns would not fit the
+                    // registers beside everything else live here)
+                    int tm, tn;
+                    pair_tile_coords(t, pl, tm, tn);
+                    const int row = tm * PM + static_cast<int>(rank) * TBM + rloc;
+                    const int col0 = tn * PN + h * (EPI_COLS);
+                    if (row < M && col0 < N) {
+                        float *crow = C + static_cast<size_t>(row) * ldc + col0;
+                        const int left = N - col0;
+                        for (int c = 0; c < EPI_COLS && c < left; c += 4) {
+                            const size_t off = (static_cast<size_t>((h * (EPI_COLS) + c) / 4) * TBM + rloc) * 4;
+                            float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            for (int k = 0; k < nparts; ++k) {
+                                const int sl = k == 0 ? first_slot : 2 * (p_first + k);
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                                    partials + (static_cast<size_t>(sl) * 2 + rank) * SLOT_FLOATS + off));
+                                sum.x += v.x;
+                                sum.y += v.y;
+                                sum.z += v.z;
+                                sum.w += v.w;
+                            }
+                            if (vc == 4 && c + 4 <= left) {
+                                *reinterpret_cast<float4 *>(crow + c) = sum;
+                            } else {
+                                const float e4[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-                    for (int c = 0; c < EPI_COLS; ++c) total[c] = 0.0f;
-                    for (int k = 0; k < nparts; ++k) {
-                        const float *slot =
-                            partials + (static_cast<size_t>(part_slot(p_first + k, ts, pl)) * 2 + rank) * SLOT_FLOATS;
-#pragma unroll
-                        for (int c = 0; c < EPI_COLS; c += 4) {
-                            const int chunk = (h * (EPI_COLS) + c) / 4;
-                            const float4 v =
-                                __ldcg(reinterpret_cast<const float4 *>(slot + (static_cast<size_t>(chunk) * TBM + rloc) * 4));
-                            total[c] += v.x;
-                            total[c + 1] += v.y;
-                            total[c + 2] += v.z;
-                            total[c + 3] += v.w;
+                                for (int e = 0; e < 4; ++e)
+                                    if (c + e < left) crow[c + e] = e4[e];
+                            }
                         }
                     }
                 }
+                store = false;
             }
             if (store) {
                 int tm, tn;

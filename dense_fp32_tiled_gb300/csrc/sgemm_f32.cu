@@ -149,6 +149,14 @@ __device__ __forceinline__ void acc_zero(Acc &acc) {
         for (int j = 0; j < TN / 2; ++j) acc.c[i][j] = make_float2(0.0f, 0.0f);
 }
 
+// threadIdx.x, read afresh at each call: the compiler can neither keep it
+// live across a loop nor merge two reads.
+__device__ __forceinline__ int tid_fresh() {
+    int t;
+    asm volatile("mov.u32 %0, %%tid.x;\n" : "=r"(t));
+    return t;
+}
+
 // Accumulates the product of the CTA's C tile (m0, n0) over K tiles
 // [kt0, kt1) into acc.  VA = A copy width in floats (4 or 1), VB = B copy
 // width in floats (4, 2 or 1), chosen on the host from alignment; with TMA
@@ -167,10 +175,16 @@ __device__ __forceinline__ void acc_zero(Acc &acc) {
 //   4. 16 k steps of fragment reads and packed FMAs on tile kt.
 // On return every copy has landed; the caller must __syncthreads() before
 // starting another range (other threads may still read shared memory).
+//
+// The tile origin (m0, n0) is read from shared memory (`org`, written before
+// a barrier the whole CTA passed) and the copy coordinates from a fresh read
+// of the thread index at each copy issue, so neither is held in registers
+// through the K loop: with 64 accumulators in a 128-register budget the
+// narrow-copy variants have no room to keep them.
 template <int VA, int VB, bool TMA>
-__device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, const int m0, const int n0,
-                                            const int kt0, const int kt1, uint32_t &pipe, float *smem,
-                                            const uint32_t bars, Acc &acc) {
+__device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, const int2 *org, const int kt0,
+                                            const int kt1, uint32_t &pipe, float *smem, const uint32_t bars,
+                                            Acc &acc) {
     static_assert(!TMA || (VA == 4 && VB == 4), "tensor copies need 16-byte aligned rows");
     constexpr uint32_t RING = STAGES;
     const int tid = threadIdx.x;
@@ -178,55 +192,46 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t u0 = pipe - static_cast<uint32_t>(kt0);  // load index of tile kt is u0 + kt
 
-    // ---- A copies (global -> raw staging tile).  Rows past M and columns
-    // past K are zero-filled by a zero source size ("边界处理会破坏漂亮形状").
+    // Copies: A (global -> raw staging tile) and B (global -> row-major tile).
+    // Rows past M and columns past K or N are zero-filled by a zero or short
+    // source size ("边界处理会破坏漂亮形状").
     constexpr int NA = VA == 4 ? A_COPIES16 : A_COPIES4;
-    int a_m0, a_k;
-    if constexpr (VA == 4) a_copy16_coord(tid, 0, a_m0, a_k);
-    else a_copy4_coord(tid, 0, a_m0, a_k);
-    constexpr int A_ROW_STEP = VA == 4 ? 64 : 16;  // rows between a thread's copies
-    const float *a_base = p.A + static_cast<size_t>(m0 + a_m0 < M ? m0 + a_m0 : 0) * p.lda + a_k;
-    const size_t a_step = static_cast<size_t>(A_ROW_STEP) * p.lda;
-
-    // ---- B copies (global -> shared, row-major tile)
     constexpr int NB = b_copies<VB>();
-    int b_k0, b_n;
-    b_copy_coord<VB>(tid, 0, b_k0, b_n);
-    const int b_col = n0 + b_n;
-    const int b_valid = N - b_col;  // valid floats from b_col on
-    const uint32_t b_bytes = b_valid >= VB ? VB * 4u : (b_valid > 0 ? b_valid * 4u : 0u);
-    const float *b_colp = p.B + (b_valid > 0 ? b_col : 0);
 
     auto issue_tile = [&](int kt) {
         const uint32_t stage = (u0 + kt) % RING;
         const int kb = kt * BK;
+        const int2 o = *org;  // (m0, n0)
         if constexpr (TMA) {
             if (tid == 0) {
                 const uint32_t bar = bars + 8 * stage;
                 mbar_expect_tx(bar, STAGE_FLOATS * 4);
-                tma_load_2d(sbase + ar_word(stage, 0, 0) * 4, &maps.a, kb, m0, bar);
-                tma_load_2d(sbase + bs_word(stage, 0, 0) * 4, &maps.b, n0, kb, bar);
+                tma_load_2d(sbase + ar_word(stage, 0, 0) * 4, &maps.a, kb, o.x, bar);
+                tma_load_2d(sbase + bs_word(stage, 0, 0) * 4, &maps.b, o.y, kb, bar);
             }
         } else {
+            const int t = tid_fresh();
 #pragma unroll
             for (int q = 0; q < NA; ++q) {
                 int m, k;
-                if constexpr (VA == 4) a_copy16_coord(tid, q, m, k);
-                else a_copy4_coord(tid, q, m, k);
+                if constexpr (VA == 4) a_copy16_coord(t, q, m, k);
+                else a_copy4_coord(t, q, m, k);
                 const int kg = kb + k;
                 const int left = K - kg;  // valid floats from kg on
-                uint32_t bytes = (m0 + m < M && left > 0) ? (left >= VA ? VA * 4u : left * 4u) : 0u;
-                const float *src = bytes ? a_base + q * a_step + kb : p.A;
+                const uint32_t bytes = (o.x + m < M && left > 0) ? (left >= VA ? VA * 4u : left * 4u) : 0u;
+                const float *src = bytes ? p.A + (static_cast<size_t>(o.x + m) * p.lda + kg) : p.A;
                 cp_async<VA * 4>(sbase + ar_word(stage, m, k) * 4, src, bytes);
             }
 #pragma unroll
             for (int q = 0; q < NB; ++q) {
                 int k, n;
-                b_copy_coord<VB>(tid, q, k, n);
+                b_copy_coord<VB>(t, q, k, n);
                 const int kg = kb + k;
-                const bool ok = kg < K && b_bytes != 0;
-                const float *src = ok ? b_colp + static_cast<size_t>(kg) * p.ldb : p.B;
-                cp_async<VB * 4>(sbase + bs_word(stage, k, n) * 4, src, ok ? b_bytes : 0u);
+                const int valid = N - (o.y + n);  // valid floats from column o.y + n on
+                const uint32_t bytes =
+                    kg < K && valid > 0 ? (valid >= VB ? VB * 4u : static_cast<uint32_t>(valid) * 4u) : 0u;
+                const float *src = bytes ? p.B + (static_cast<size_t>(kg) * p.ldb + (o.y + n)) : p.B;
+                cp_async<VB * 4>(sbase + bs_word(stage, k, n) * 4, src, bytes);
             }
             cp_async_commit();
         }
@@ -261,9 +266,6 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
         }
     };
 
-    const int ra = frag_row0(tid);
-    const int cb = frag_col0(tid);
-
     // prologue: tiles kt0 .. kt0+STAGES-2 in flight, tile kt0 transposed
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
@@ -285,6 +287,10 @@ __device__ __forceinline__ void mma_k_range(const Problem &p, const Maps &maps, 
 
         const uint32_t stage = (u0 + kt) % STAGES;
         const int buf = (u0 + kt) & 1;
+        // fragment offsets: from a fresh thread index in the narrow-copy
+        // variants (no room to keep them), else from tid
+        const int tf = TMA ? tid : tid_fresh();
+        const int ra = frag_row0(tf), cb = frag_col0(tf);
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
             const float4 a0 = *reinterpret_cast<const float4 *>(smem + as_word(buf, k, ra));
@@ -323,6 +329,20 @@ __device__ __forceinline__ void init_bars(uint32_t bars) {
         }
         __syncthreads();
     }
+}
+
+// init_bars, and thread 0 publishes the CTA's tile origin (m0, n0) in `org`
+// for mma_k_range; the barrier makes both visible to the CTA.
+template <bool TMA>
+__device__ __forceinline__ void init_cta(uint32_t bars, int2 *org, int m0, int n0) {
+    if (threadIdx.x == 0) {
+        if (TMA) {
+            for (int s = 0; s < kMaxRing; ++s) mbar_init(bars + 8 * s, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        }
+        *org = make_int2(m0, n0);
+    }
+    __syncthreads();
 }
 
 // Writes the register tile to C tile (m0, n0) with guarded stores,
@@ -373,16 +393,17 @@ __global__ void __launch_bounds__(NT, 2) sgemm_f32_tiled_kernel(const Problem p,
     // a split-tail grid queued behind this one may start as SMs free up: it
     // writes other tiles and reads nothing this grid writes
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    __shared__ int2 org;
     float *smem = aligned_smem(smem_raw);
     const uint32_t bars = smem_u32(bar_mem);
-    init_bars<TMA>(bars);
     int tm, tn;
     tile_of(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
+    init_cta<TMA>(bars, &org, tm * BM, tn * BN);
     Acc acc;
     acc_zero(acc);
     uint32_t pipe = 0;
-    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
-    store_tile<false>(p, tm * BM, tn * BN, acc);
+    mma_k_range<VA, VB, TMA>(p, maps, &org, 0, (p.K + BK - 1) / BK, pipe, smem, bars, acc);
+    store_tile<false>(p, org.x, org.y, acc);
 }
 
 // ---- cluster split of K ----------------------------------------------------
@@ -445,21 +466,28 @@ template <int VA, int VB, bool TMA>
 __global__ void __launch_bounds__(NT, 2) sgemm_f32_clusterk_kernel(const Problem p, const __grid_constant__ Maps maps) {
     extern __shared__ float smem_raw[];
     __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
+    __shared__ int2 org;
     float *smem = aligned_smem(smem_raw);
     const uint32_t bars = smem_u32(bar_mem);
-    init_bars<TMA>(bars);
-    const int S = static_cast<int>(cluster_nctarank());
-    const int rank = static_cast<int>(cluster_ctarank());
-    int tm, tn;
-    tile_of(static_cast<int>(blockIdx.x) / S, p.tiles_m, p.tiles_n, tm, tn);
-    const int KT = (p.K + BK - 1) / BK;
-    const int k0 = static_cast<int>(static_cast<long long>(KT) * rank / S);
-    const int k1 = static_cast<int>(static_cast<long long>(KT) * (rank + 1) / S);
+    int k0, k1;
+    {
+        const int S = static_cast<int>(cluster_nctarank());
+        const int rank = static_cast<int>(cluster_ctarank());
+        int tm, tn;
+        tile_of(static_cast<int>(blockIdx.x) / S, p.tiles_m, p.tiles_n, tm, tn);
+        init_cta<TMA>(bars, &org, tm * BM, tn * BN);
+        const int KT = (p.K + BK - 1) / BK;
+        k0 = static_cast<int>(static_cast<long long>(KT) * rank / S);
+        k1 = static_cast<int>(static_cast<long long>(KT) * (rank + 1) / S);
+    }
     Acc acc;
     acc_zero(acc);
     uint32_t pipe = 0;
-    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
+    mma_k_range<VA, VB, TMA>(p, maps, &org, k0, k1, pipe, smem, bars, acc);
     __syncthreads();  // every thread is done with the ring: its space becomes the partial tile
+    // the cluster shape is read again here rather than kept through the K loop
+    const int S = static_cast<int>(cluster_nctarank());
+    const int rank = static_cast<int>(cluster_ctarank());
     const int tid = threadIdx.x;
 #pragma unroll
     for (int q = 0; q < 2 * TM; ++q) {
@@ -486,7 +514,7 @@ __global__ void __launch_bounds__(NT, 2) sgemm_f32_clusterk_kernel(const Problem
             sum.z += v.z;
             sum.w += v.w;
         }
-        store_c4(p, tm * BM + row, tn * BN + col, sum);
+        store_c4(p, org.x + row, org.y + col, sum);
     }
     cluster_barrier();  // no CTA leaves while a peer may still read its shared memory
 }
@@ -679,12 +707,15 @@ __device__ __forceinline__ void store_partial(float *slot, const Acc &acc) {
         *reinterpret_cast<float4 *>(slot + 4 * (q * NT + threadIdx.x)) = make_float4(lo.x, lo.y, hi.x, hi.y);
     }
 }
+// (at most 4 loads in flight: with the 64 accumulators live, loading all 16
+// first would not fit the 128-register budget)
 __device__ __forceinline__ void add_partial(const float *slot, Acc &acc) {
 #pragma unroll
     for (int q = 0; q < TM * TN / 4; ++q) {
         const float4 v = __ldcg(reinterpret_cast<const float4 *>(slot + 4 * (q * NT + threadIdx.x)));
         float2 &lo = acc.c[q >> 1][2 * (q & 1)], &hi = acc.c[q >> 1][2 * (q & 1) + 1];
         lo.x += v.x; lo.y += v.y; hi.x += v.z; hi.y += v.w;
+        if ((q & 3) == 3) asm volatile("" ::: "memory");
     }
 }
 // Thread 0 waits for a flag raised by another CTA; a wait longer than
@@ -715,47 +746,66 @@ __device__ __forceinline__ void raise_flag(unsigned *flag) {
 // K tile) iterations of the remaining tiles, cut at tile boundaries.  K tiles
 // are bk deep (BK, or BK_AT for the k-major kernels).
 struct SkWalk {
-    const Problem &p;  // the kernel parameter (read from parameter space, not held in registers)
-    int KT, G, dp_tiles;
-    long long total_iters, base, it, it_end;
-    int dp_lin;
-
-    __device__ __forceinline__ SkWalk(const Problem &prob, int dp, int bk) : p(prob) {
-        KT = (p.K + bk - 1) / bk;
-        G = gridDim.x;
-        dp_tiles = dp;
-        total_iters = static_cast<long long>(p.tiles_m * p.tiles_n - dp_tiles) * KT;
-        base = static_cast<long long>(dp_tiles) * KT;
-        it_end = base + total_iters * (blockIdx.x + 1) / G;
-        it = base + total_iters * blockIdx.x / G;
-        dp_lin = blockIdx.x;
-    }
-    // The next segment: tile lin (linear tile index), its C tile (tm, tn) and
-    // K tiles [k0, k1); false when the CTA is done.
-    __device__ __forceinline__ bool next(int &lin, int &tm, int &tn, int &k0, int &k1) {
-        if (dp_lin < dp_tiles) {
-            lin = dp_lin;
-            k0 = 0;
-            k1 = KT;
-            dp_lin += G;
-        } else if (it < it_end) {
-            lin = static_cast<int>(it / KT);
-            k0 = static_cast<int>(it % KT);
-            k1 = static_cast<int>(k0 + (it_end - it) < KT ? k0 + (it_end - it) : KT);
-            it += k1 - k0;
-        } else {
-            return false;
-        }
-        tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
-        return true;
-    }
-    // The last CTA holding a part of tile lin: the owner adds the parts of
-    // CTAs blockIdx.x + 1 .. last_part(lin).
-    __device__ __forceinline__ int last_part(int lin) const {
-        const long long last = static_cast<long long>(lin + 1) * KT - 1 - base;
-        return static_cast<int>(((last + 1) * G + total_iters - 1) / total_iters - 1);
-    }
+    long long it, it_end;  // this CTA's stream-K iterations not yet taken: [it, it_end)
+    int dp_lin;            // its next data-parallel tile
+    int lin, k0, k1;       // the current segment: tile lin, K tiles [k0, k1)
+    int last;              // the last CTA holding a part of tile lin (see sk_last_part)
+    int more;              // 0 once the CTA is done
+    int2 org;              // the segment's tile origin (m0, n0)
+    int KT;                // K tiles per tile
+    unsigned pipe;         // K tiles this CTA loaded before the segment (see mma_k_range)
 };
+// Stream-K iterations (tile, K tile) after the dp_tiles data-parallel tiles.
+__device__ __forceinline__ long long sk_total(const Problem &p, int dp_tiles, int KT) {
+    return static_cast<long long>(p.tiles_m * p.tiles_n - dp_tiles) * KT;
+}
+// Thread 0 only: this CTA's range, CTA c of G taking iterations
+// [total c / G, total (c+1) / G) after the data-parallel ones.
+__device__ __forceinline__ void sk_begin(SkWalk &w, const Problem &p, int dp_tiles, int KT) {
+    const long long total = sk_total(p, dp_tiles, KT), base = static_cast<long long>(dp_tiles) * KT;
+    w.it = base + total * blockIdx.x / gridDim.x;
+    w.it_end = base + total * (blockIdx.x + 1) / gridDim.x;
+    w.dp_lin = blockIdx.x;
+    w.KT = KT;
+    w.k0 = w.k1 = 0;
+    w.pipe = 0u;
+}
+// The last CTA holding a part of tile lin: the owner adds the parts of CTAs
+// blockIdx.x + 1 .. sk_last_part(lin).
+__device__ __forceinline__ int sk_last_part(const Problem &p, int dp_tiles, int KT, int lin) {
+    const long long total = sk_total(p, dp_tiles, KT);
+    const long long last = static_cast<long long>(lin + 1) * KT - 1 - static_cast<long long>(dp_tiles) * KT;
+    return static_cast<int>(((last + 1) * gridDim.x + total - 1) / total - 1);
+}
+// Thread 0 only: the next segment (whole data-parallel tiles first, then the
+// range cut at tile boundaries), or more = 0 when the CTA is done.
+__device__ __forceinline__ void sk_next(SkWalk &w, const Problem &p, int dp_tiles) {
+    const int KT = w.KT;
+    w.pipe += static_cast<unsigned>(w.k1 - w.k0);  // the segment just finished
+    int lin, k0, k1;
+    if (w.dp_lin < dp_tiles) {
+        lin = w.dp_lin;
+        k0 = 0;
+        k1 = KT;
+        w.dp_lin += gridDim.x;
+    } else if (w.it < w.it_end) {
+        lin = static_cast<int>(w.it / KT);
+        k0 = static_cast<int>(w.it % KT);
+        k1 = static_cast<int>(k0 + (w.it_end - w.it) < KT ? k0 + (w.it_end - w.it) : KT);
+        w.it += k1 - k0;
+    } else {
+        w.more = 0;
+        return;
+    }
+    int tm, tn;
+    tile_of(lin, p.tiles_m, p.tiles_n, tm, tn);
+    w.lin = lin;
+    w.k0 = k0;
+    w.k1 = k1;
+    w.last = lin >= dp_tiles ? sk_last_part(p, dp_tiles, KT, lin) : static_cast<int>(blockIdx.x);
+    w.org = make_int2(tm * BM, tn * BN);
+    w.more = 1;
+}
 
 // Stream-K schedule.  A persistent, co-resident grid of G CTAs first computes
 // tiles 0 .. dp_tiles-1 one whole tile at a time (tile c, c+G, ...: CTAs
@@ -782,44 +832,47 @@ sgemm_f32_streamk_kernel(const Problem p, const __grid_constant__ Maps maps, con
                          float *partials) {
     extern __shared__ float smem_raw[];
     __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
+    __shared__ SkWalk w;  // advanced by thread 0 between barriers
     float *smem = aligned_smem(smem_raw);
     const uint32_t bars = smem_u32(bar_mem);
     init_bars<TMA>(bars);
-    uint32_t pipe = 0;
-    SkWalk w(p, dp_tiles, BK);
-    unsigned *error = flags + (partials ? gridDim.x : p.tiles_m * p.tiles_n);
+    if (threadIdx.x == 0) sk_begin(w, p, dp_tiles, (p.K + BK - 1) / BK);
     // One loop over segments (whole data-parallel tiles first, then this CTA's
     // stream-K range cut at tile boundaries), so the main loop is inlined once.
-    int lin, tm, tn, k0, k1;
-    while (w.next(lin, tm, tn, k0, k1)) {
+    for (;;) {
+        if (threadIdx.x == 0) sk_next(w, p, dp_tiles);
+        __syncthreads();  // the segment is visible to the CTA
+        if (!w.more) break;
         Acc acc;
         acc_zero(acc);
-        mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
-        if (k0 == 0 && k1 == w.KT) {
-            store_tile<false>(p, tm * BM, tn * BN, acc);
+        uint32_t pipe = w.pipe;
+        mma_k_range<VA, VB, TMA>(p, maps, &w.org, w.k0, w.k1, pipe, smem, bars, acc);
+        const int lin = w.lin, k0 = w.k0;
+        if (k0 == 0 && w.k1 == w.KT) {
+            store_tile<false>(p, w.org.x, w.org.y, acc);
         } else if (k0 > 0) {  // hand the partial sums for k >= k0 over to the owner
             if (partials) {
                 store_partial(partials + static_cast<size_t>(blockIdx.x) * (BM * BN), acc);
                 raise_flag(flags + blockIdx.x);
             } else {
-                store_tile<false>(p, tm * BM, tn * BN, acc);
+                store_tile<false>(p, w.org.x, w.org.y, acc);
                 raise_flag(flags + lin);
             }
         } else if (partials) {  // owner: add the parts of CTAs blockIdx.x+1 .. c_last
-            const int c_last = w.last_part(lin);
+            const int c_last = w.last;
             for (int c = blockIdx.x + 1; c <= c_last; ++c) {
-                wait_flag(flags + c, error);
+                wait_flag(flags + c, flags + gridDim.x);
                 add_partial(partials + static_cast<size_t>(c) * (BM * BN), acc);
             }
-            store_tile<false>(p, tm * BM, tn * BN, acc);
+            store_tile<false>(p, w.org.x, w.org.y, acc);
             if (threadIdx.x == 0)
                 for (int c = blockIdx.x + 1; c <= c_last; ++c) flags[c] = 0u;
         } else {  // owner of a two-part tile
-            wait_flag(flags + lin, error);
-            store_tile<true>(p, tm * BM, tn * BN, acc);
+            wait_flag(flags + lin, flags + p.tiles_m * p.tiles_n);
+            store_tile<true>(p, w.org.x, w.org.y, acc);
             if (threadIdx.x == 0) flags[lin] = 0u;
         }
-        __syncthreads();  // shared memory free for the next segment
+        __syncthreads();  // shared memory (ring and segment) free for the next segment
     }
 }
 
@@ -831,42 +884,45 @@ sgemm_f32_kmajor_streamk_kernel(const Problem p, const __grid_constant__ Maps ma
                                 unsigned *flags, float *partials) {
     extern __shared__ float smem_raw[];
     __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
+    __shared__ SkWalk w;  // advanced by thread 0 between barriers
     float *smem = aligned_smem(smem_raw);
     const uint32_t bars = smem_u32(bar_mem);
     init_bars<true>(bars);
-    uint32_t pipe = 0;
-    SkWalk w(p, dp_tiles, BK_AT);
-    unsigned *error = flags + (partials ? gridDim.x : p.tiles_m * p.tiles_n);
-    int lin, tm, tn, k0, k1;
-    while (w.next(lin, tm, tn, k0, k1)) {
+    if (threadIdx.x == 0) sk_begin(w, p, dp_tiles, (p.K + BK_AT - 1) / BK_AT);
+    for (;;) {
+        if (threadIdx.x == 0) sk_next(w, p, dp_tiles);
+        __syncthreads();  // the segment is visible to the CTA
+        if (!w.more) break;
         Acc16 acc;
         acc16_zero(acc);
-        kmajor16_k_range(maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
-        if (k0 == 0 && k1 == w.KT) {
-            store_tile16<false>(p, tm * BM, tn * BN, acc);
+        uint32_t pipe = w.pipe;
+        kmajor16_k_range(maps, w.org.x, w.org.y, w.k0, w.k1, pipe, smem, bars, acc);
+        const int lin = w.lin, k0 = w.k0;
+        if (k0 == 0 && w.k1 == w.KT) {
+            store_tile16<false>(p, w.org.x, w.org.y, acc);
         } else if (k0 > 0) {  // hand the partial sums for k >= k0 over to the owner
             if (partials) {
                 store_partial16(partials + static_cast<size_t>(blockIdx.x) * (BM * BN), acc);
                 raise_flag(flags + blockIdx.x);
             } else {
-                store_tile16<false>(p, tm * BM, tn * BN, acc);
+                store_tile16<false>(p, w.org.x, w.org.y, acc);
                 raise_flag(flags + lin);
             }
         } else if (partials) {  // owner: add the parts of CTAs blockIdx.x+1 .. c_last
-            const int c_last = w.last_part(lin);
+            const int c_last = w.last;
             for (int c = blockIdx.x + 1; c <= c_last; ++c) {
-                wait_flag(flags + c, error);
+                wait_flag(flags + c, flags + gridDim.x);
                 add_partial16(partials + static_cast<size_t>(c) * (BM * BN), acc);
             }
-            store_tile16<false>(p, tm * BM, tn * BN, acc);
+            store_tile16<false>(p, w.org.x, w.org.y, acc);
             if (threadIdx.x == 0)
                 for (int c = blockIdx.x + 1; c <= c_last; ++c) flags[c] = 0u;
         } else {  // owner of a two-part tile
-            wait_flag(flags + lin, error);
-            store_tile16<true>(p, tm * BM, tn * BN, acc);
+            wait_flag(flags + lin, flags + p.tiles_m * p.tiles_n);
+            store_tile16<true>(p, w.org.x, w.org.y, acc);
             if (threadIdx.x == 0) flags[lin] = 0u;
         }
-        __syncthreads();  // shared memory free for the next segment
+        __syncthreads();  // shared memory (ring and segment) free for the next segment
     }
 }
 
@@ -885,19 +941,20 @@ sgemm_f32_tail_kernel(const Problem p, const __grid_constant__ Maps maps, const 
     extern __shared__ float smem_raw[];
     __shared__ __align__(8) uint64_t bar_mem[kMaxRing];
     __shared__ int last;
+    __shared__ int2 org;
     float *smem = aligned_smem(smem_raw);
     const uint32_t bars = smem_u32(bar_mem);
-    init_bars<TMA>(bars);
     const int c = blockIdx.x, tile = c / parts, part = c - tile * parts;
     const int KT = (p.K + BK - 1) / BK;
     const int k0 = static_cast<int>(static_cast<long long>(KT) * part / parts);
     const int k1 = static_cast<int>(static_cast<long long>(KT) * (part + 1) / parts);
     int tm, tn;
     tile_of(dp_tiles + tile, p.tiles_m, p.tiles_n, tm, tn);
+    init_cta<TMA>(bars, &org, tm * BM, tn * BN);
     Acc acc;
     acc_zero(acc);
     uint32_t pipe = 0;
-    mma_k_range<VA, VB, TMA>(p, maps, tm * BM, tn * BN, k0, k1, pipe, smem, bars, acc);
+    mma_k_range<VA, VB, TMA>(p, maps, &org, k0, k1, pipe, smem, bars, acc);
     store_partial(slots + static_cast<size_t>(c) * (BM * BN), acc);
     __threadfence();
     __syncthreads();
@@ -911,7 +968,7 @@ sgemm_f32_tail_kernel(const Problem p, const __grid_constant__ Maps maps, const 
         if (threadIdx.x == 0) counts[tile] = 0u;  // every part has counted itself: leave the word zero
         acc_zero(acc);
         for (int k = 0; k < parts; ++k) add_partial(slots + static_cast<size_t>(tile * parts + k) * (BM * BN), acc);
-        store_tile<false>(p, tm * BM, tn * BN, acc);
+        store_tile<false>(p, org.x, org.y, acc);
     }
 }
 
@@ -1502,22 +1559,32 @@ Plan effective_plan(long long T, long long KT, long long G, long long sms, bool 
 // most G / 2 tiles (the split then fills the GPU without a second wave), at
 // least 2 K tiles per CTA, on the 8 x 8 kernels (variant v).  S = the most
 // CTAs per tile that keep all of them resident, at most 8 (the portable
-// cluster size).  When the stream-K schedule over all tiles could run instead
-// (`streamk`: the workspace has room for it), the split is taken only if its
-// CTAs get at most 3 K tiles more than stream-K's: measured on GB300, the
-// split saves stream-K's fixed costs (flag memset, hand-over waits, the
-// owner's serial sum of the parts), worth about 3 K tiles of one CTA
-// (1024^3: 53.1 -> 49.5 us, S = 4, 16 K tiles per CTA against 13.5; 256^3
-// 20.2 -> 12.8 us; 512^3 22.6 -> 20.8 us), and loses when its grid leaves
-// more slots empty (2048 x 1024 x 1024: S = 2, 32 K tiles per CTA against 27,
-// 82.6 -> 88.4 us).  SGEMM_F32_TUNE schedule=0..3 turns it off.
-int cluster_split(long long T, long long KT, long long G, int v, bool streamk) {
+// cluster size).
+// When the multi-part stream-K schedule `sk` (kind 2, g CTAs) could run
+// instead, the split is taken only if it is expected to be faster.  Cost in
+// K tiles of one CTA (about 2.4 us each with two CTAs per SM), fitted to
+// GB300 timings of both schedules (1024^3, 1024 x 1024 x 2048 and x 4096,
+// 2048 x 1024 x 1024, 512 x 512 x 1024, 256 x 256 x 1024):
+//   cluster split: 4.7 + ceil(KT / S)  (launch, the two cluster barriers and
+//                  the sum over distributed shared memory);
+//   stream-K:      7.5 + T KT / g + 0.25 ceil(g / T)  (flag reset, hand-over
+//                  waits, and the owner's serial sum of ceil(g / T) parts).
+// E.g. 1024^3: 16 against 13.5 + 2.8 + 1.25 (split: 49.2 us, stream-K 53.1);
+// 512 x 512 x 1024: 8 against 4 + 2.8 + 4 (30.7 against 38.9 us);
+// 2048 x 1024 x 1024: 32 against 26.9 + 2.8 + 0.75 (88.3 against 83.9 us).
+// SGEMM_F32_TUNE schedule=0..3 turns the split off.
+int cluster_split(long long T, long long KT, long long G, int v, const Plan *sk) {
     if (v >= kAtVariant || kCk[v] == nullptr || tune().schedule >= 0 || T <= 0 || 2 * T > G) return 0;
     long long S = G / T;
     if (S > 8) S = 8;
     if (S > KT / 2) S = KT / 2;
     if (S < 2) return 0;
-    if (streamk && static_cast<double>((KT + S - 1) / S) > static_cast<double>(T * KT) / G + 3.0) return 0;
+    if (sk != nullptr && sk->grid > 0) {
+        const double g = static_cast<double>(sk->grid);
+        const double split = static_cast<double>((KT + S - 1) / S);
+        const double streamk = static_cast<double>(T * KT) / g + 2.8 + 0.25 * static_cast<double>((sk->grid + T - 1) / T);
+        if (split > streamk) return 0;
+    }
     return static_cast<int>(S);
 }
 
@@ -1603,7 +1670,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     cfg.dynamicSmemBytes = smem_of(v);
     cfg.stream = stream;
     const bool streamk = flags != nullptr && pl.kind == 2 && flag_bytes >= pl.bytes;
-    if (const int S = cluster_split(T, KT, G, v, streamk)) {
+    if (const int S = cluster_split(T, KT, G, v, streamk ? &pl : nullptr)) {
         sg_nvtx::Range r("sgemm_f32: cluster split of K");
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -1808,7 +1875,7 @@ extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int ld
     const long long G = static_cast<long long>(info.sk_per_sm[v]) * info.sms;
     const int copies = (rp.a ? 4 : 0) | (rp.b ? 8 : 0) | (rp.at ? 16 : 0);
     const Plan pl = effective_plan(T, KT, G, info.sms, is_tma(v), avail);
-    if (K > 0 && cluster_split(T, KT, G, v, pl.kind == 2)) {
+    if (K > 0 && cluster_split(T, KT, G, v, pl.kind == 2 ? &pl : nullptr)) {
         *kind = 32 | copies;  // cluster split of K: no schedule words
         return SGEMM_OK;
     }

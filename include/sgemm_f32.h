@@ -115,10 +115,11 @@ int sgemm_f32(int M, int N, int K,
  *      (one count per leftover tile, then S * R slots of 64 KiB).
  *   0  otherwise, or with a smaller workspace: exactly as sgemm_f32.
  * The cluster split of K (see sgemm_f32) takes precedence where it applies,
- * except over schedule 2 when that gives its CTAs more than 3 K tiles fewer
- * each (measured on GB300: the cluster split saves schedule 2's flag reset,
- * hand-over waits and serial sum of the parts, worth about 3 K tiles of one
- * CTA); it uses no workspace.
+ * except over schedule 2 where a cost model fitted to GB300 timings expects
+ * schedule 2 to be faster: the split costs its CTAs' K tiles plus about 4.7
+ * K tiles of fixed cost; schedule 2 its CTAs' (fewer) K tiles plus about 7.5
+ * and a quarter K tile per part of a tile (flag reset, hand-over waits, the
+ * serial sum of the parts).  The split uses no workspace.
  * sgemm_f32_workspace_size reports the bytes for the current device.  The
  * call zero-fills the words it uses at the start of the workspace on
  * `stream` before the kernels, so the workspace needs no preparation and its

@@ -172,13 +172,13 @@ def _plan_words(M, N, K, pA, lda, pB, ldb, pC, ldc):
     return words
 
 
-# Products with at most G / 2 tiles take the cluster split of K instead when
-# its CTAs get at most 3 K tiles more than stream-K's (test_clusterk_gpu.py);
-# these shapes keep the multi-part split.
+# Products with at most G / 2 tiles take the cluster split of K instead where
+# it is expected to be faster (test_clusterk_gpu.py); these shapes keep the
+# multi-part split.
 @pytest.mark.parametrize("M,N,K,lds,kind", [
     (2048, 1024, 1024, None, "normal"),          # 128 tiles
     (1000, 2470, 333, (333, 2470, 2470), "uniform"),  # 160 tiles, misaligned rows: cp.async path
-    (2048, 256, 4096, None, "normal"),           # 32 tiles, deep K
+    (1024, 256, 8192, None, "normal"),           # 16 tiles, deep K
 ])
 def test_multipart_split_full_check(oracle_lib, M, N, K, lds, kind):
     lda, ldb, ldc = lds or (K, N, N)
