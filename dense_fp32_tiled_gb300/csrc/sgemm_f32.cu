@@ -1450,8 +1450,15 @@ int choose_variant(int M, int N, int K, const float *A, int lda, const float *B,
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-// Products below this many FLOPs get no repack room from
-// sgemm_f32_workspace_size_for (see there).
+// Products below this many FLOPs copy no operand (and get no room for copies
+// from sgemm_f32_workspace_size_for).  Measured on GB300 with a workspace
+// large enough for every copy (us, narrow copies -> copies first):
+// 300 x 262 x 190 13.1 -> 34.6, 512^3 with lda = ldb = 513 23.1 -> 32.8,
+// 700 x 900 x 333 30.1 -> 32.5, 1000 x 1030 x 777 52.8 -> 59.8 (or 54.5 with
+// rows repacked instead of the k-major copy); from about 2 GFLOP on the
+// copies win: 1024 x 1024 x 1025 60.9 -> 57.5, 2000 x 1030 x 777 91.7 -> 84.4
+// (earlier, before the cluster split: 1536^3 153.7 -> 131.3,
+// 2048 x 2048 x 2049 362.1 -> 289.3).
 constexpr double kRepackMinFlops = 2e9;
 
 // Whether transposing a 16-byte aligned A into its k-major copy first pays.
@@ -1502,6 +1509,10 @@ Repack plan_repack(int M, int N, int K, const float *A, int lda, const float *B,
                    size_t avail, const Policy &pol) {
     Repack r = {false, false, false, 0, 0, 0, 0, 0, 0, 0, 0};
     if (K <= 0 || encode_fn() == nullptr) return r;
+    // Below kRepackMinFlops the narrow-copy kernels (and their cluster split
+    // of K) beat every copy, whatever room the workspace has (see there),
+    // unless SGEMM_F32_TUNE picks the kernel family.
+    if (pol.at == 1 && 2.0 * M * N * K < kRepackMinFlops) return r;
     const bool ra = vector_class(A, lda) != 4, rb = vector_class(B, ldb) != 4;
     const bool want_at = pol.at == 2 || (pol.at == 1 && (ra || kmajor_pays(M, N, K)));
     if (!ra && !rb && !want_at) return r;
@@ -1831,12 +1842,8 @@ extern "C" size_t sgemm_f32_workspace_size(int M, int N, int K) {
 extern "C" size_t sgemm_f32_workspace_size_for(int M, int N, int K, const float *A, int lda, const float *B,
                                                int ldb) {
     const size_t base = sgemm_f32_workspace_size(M, N, K);
-    // Smaller products with unaligned rows run faster on the narrow copies
-    // than with the copies first (measured on GB300, narrow -> k-major A and
-    // repacked B: 512^3 with lda = ldb = 513 28.6 -> 37.3 us, 1000x1030x777
-    // 58.6 -> 61.1, 700x900x333 32.7 -> 35.5; from about 2 GFLOP on the copies
-    // win: 1024x1024x1025 61.4 -> 58.6, 1536^3 153.7 -> 131.3, 2048x2048x2049
-    // 362.1 -> 289.3 us), so no room is asked for them.
+    // Smaller products copy nothing (kRepackMinFlops), so no room is asked
+    // for them.
     if (base == 0 || K == 0 || 2.0 * M * N * K < kRepackMinFlops) return base;
     int dev = 0;
     DeviceInfo info;

@@ -128,8 +128,10 @@ int sgemm_f32(int M, int N, int K,
  * schedules 1 and 2 the last of them is an error word, nonzero only if a CTA
  * gave up waiting for a partner (about a second; the result is then wrong,
  * nothing hangs); in schedule 3 no CTA waits for another.
- * Operand copies (K > 0; each one kernel, HBM-bound; placed after the
- * schedule's words in the workspace):
+ * Operand copies (K > 0 and 2*M*N*K >= 2e9: smaller products run faster on
+ * the narrower copies of the kernels themselves, measured on GB300; each copy
+ * is one kernel, HBM-bound, placed after the schedule's words in the
+ * workspace):
  *   k-major A: when the k-major copy pays (large N, see
  *      sgemm_f32_workspace_size_for) or A's rows are not 16-byte aligned
  *      (pointer or lda), and the workspace has room for the schedule plus
@@ -187,8 +189,7 @@ size_t sgemm_f32_workspace_size(int M, int N, int K);
  * more, enough for the operand copies of sgemm_f32_ws, in two cases:
  *   - A's or B's rows are not 16-byte aligned and the product has at least
  *     2 GFLOP (2*M*N*K): room for the k-major copy of an unaligned A and the
- *     repacked copy of an unaligned B (smaller products measured faster
- *     without the copies);
+ *     repacked copy of an unaligned B (smaller products copy nothing);
  *   - the k-major copy of A pays: its expected saving, 6 % of the
  *     product's time at 68 TFLOP/s, exceeds 1.2 times the transpose's time
  *     (8*M*K bytes at 5.5 TB/s plus 4 us).  This holds for large N (4096^3:

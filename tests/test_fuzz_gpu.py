@@ -44,6 +44,8 @@ def _cases(n=36):
         K = int(np.exp(rng.uniform(0, np.log(1500))))
         if i % 3 == 0:  # force a partial last wave, with K deep enough to split
             M, N, K = int(rng.integers(2200, 2700)), int(rng.integers(2200, 2700)), int(rng.integers(17, 600))
+        elif i % 6 == 1:  # 180 .. 210 tiles, between half and all of the resident CTAs: multi-part split
+            M, N, K = 1800 + 3 * i, 1600 + 5 * i, 200 + 7 * i
         pads = [0, 0, 0, 1, 2, 3, 4]
         lda, ldb, ldc = K + int(rng.choice(pads)), N + int(rng.choice(pads)), N + int(rng.choice(pads))
         offs = [int(rng.choice([0, 0, 0, 1, 2])) for _ in range(3)]

@@ -86,8 +86,9 @@ def test_balanced_schedules_in_a_graph(oracle_lib, M, N, K, kind):
 
 def test_kmajor_copy_in_a_graph(oracle_lib):
     """A whose rows are not 16-byte aligned (lda = K + 1) with room for its
-    k-major copy: the transpose kernel, then the k-major kernels."""
-    M, N, K = 1000, 1032, 777
+    k-major copy (a product of at least 2 GFLOP): the transpose kernel, then
+    the k-major kernels."""
+    M, N, K = 1300, 1032, 777
     lda = K + 1
     tA = torch.empty(M, lda, device="cuda")[:, :K]
     tB = torch.empty(K, N, device="cuda")

@@ -78,14 +78,15 @@ def _run(M, N, K, A, lda, B, ldb, ldc, a_off=0, b_off=0, nbytes=None, guard=64):
     return C, kind
 
 
+# Products of at least 2 GFLOP (smaller ones copy nothing; the copy kernels
+# on tiny shapes are covered by test_forced_copies_on_small_shapes).
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc,a_off,b_off,bits", [
-    (1000, 1030, 777, 777, 1030, 1030, 0, 0, 16 | 8),   # the ragged workload: A k-major, B repacked
+    (1300, 1030, 777, 777, 1030, 1030, 0, 0, 16 | 8),   # ragged: A k-major, B repacked
     (2500, 2100, 333, 333, 2100, 2100, 0, 0, 16),       # A only (K odd), 380 tiles: split tail after
     (2500, 2100, 336, 336, 2102, 2100, 0, 0, 8),        # B only (ldb not a multiple of 4)
-    (1100, 900, 512, 512, 900, 901, 1, 0, 16),          # A base off by 4 bytes, C misaligned too
-    (300, 5, 7, 7, 5, 5, 0, 0, 16 | 8),                 # tiny: N < 4, K < 16
-    (129, 1030, 2049, 2049, 1030, 1030, 0, 0, 16 | 8),  # deep odd K
-    (1001, 700, 515, 515, 700, 700, 0, 0, 16),          # M not a multiple of 4: padded k-major rows
+    (2300, 900, 512, 512, 900, 901, 1, 0, 16),          # A base off by 4 bytes, C misaligned too
+    (512, 1030, 2049, 2049, 1030, 1030, 0, 0, 16 | 8),  # deep odd K
+    (3001, 700, 515, 515, 700, 700, 0, 0, 16),          # M not a multiple of 4: padded k-major rows
 ])
 def test_copied_operands_match_the_oracle(oracle_lib, M, N, K, lda, ldb, ldc, a_off, b_off, bits):
     A = synth.matrix(M, K, 351, 0, ld=lda, pad_value=np.nan)
@@ -140,6 +141,55 @@ def test_repacked_integer_exact_and_same_as_aligned_copy(oracle_lib):
     Ca, kind_a = _run(M, N, K, A4, K4, B, N, N)
     assert kind_a == 3
     np.testing.assert_array_equal(C, Ca)
+
+
+_FORCED_CHILD = r"""
+import sys, json
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import dense_fp32_tiled_gb300 as sg
+from dense_fp32_tiled_gb300 import synth
+import oracle
+from tests import _tolerance as tol
+from tests._gpu import dev_buffer
+sg.load_library()
+oracle.build()
+out = []
+for (M, N, K, lda, ldb) in json.loads(sys.argv[2]):
+    A = synth.matrix(M, K, 358, 0, ld=lda, pad_value=np.nan)
+    B = synth.matrix(K, N, 358, 1, ld=ldb, pad_value=np.nan)
+    tA, pA = dev_buffer(A)
+    tB, pB = dev_buffer(B)
+    tC = torch.full((M * N + 4,), float("nan"), device="cuda")
+    nbytes = sg.workspace_size(M, N, K) + (M + 4) * (K + 4) * 4 + (K + 4) * (M + 4) * 4 + (K + 4) * (N + 4) * 4 + 4096
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    _, kind, _ = sg.ws_schedule(M, N, K, pA, lda, pB, ldb, tC.data_ptr(), N, nbytes)
+    st = sg.sgemm_f32_ws(M, N, K, pA, lda, pB, ldb, tC.data_ptr(), N, ws.data_ptr(), nbytes,
+                         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == 0, st
+    C = tC.cpu().numpy()[:M * N].reshape(M, N)
+    Cr, Sr = oracle.gemm(A, B, M=M, N=N, K=K, lda=lda, ldb=ldb)
+    tol.assert_close(C, Cr, Sr, K, f"forced copies {M}x{N}x{K}")
+    out.append(kind)
+print(json.dumps(out))
+"""
+
+
+@pytest.mark.parametrize("tune,bits", [("kernels=kmajor16", 16 | 8), ("kernels=rowmajor8", 4 | 8)])
+def test_forced_copies_on_small_shapes(tune, bits):
+    """Below 2 GFLOP nothing is copied by default; with the kernel family
+    forced by SGEMM_F32_TUNE (read once per process, so in a child process)
+    the copies run on tiny and ragged shapes: N < 4, K < 16, M not a
+    multiple of 4, a deep odd K."""
+    import json, os, subprocess, sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    shapes = [(300, 5, 7, 7, 5), (129, 1030, 2049, 2049, 1030), (1001, 700, 515, 515, 702), (1000, 1030, 777, 777, 1030)]
+    r = subprocess.run([sys.executable, "-c", _FORCED_CHILD, root, json.dumps(shapes)], cwd=root,
+                       env=dict(os.environ, SGEMM_F32_TUNE=tune), capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    kinds = json.loads(r.stdout.strip().splitlines()[-1])
+    assert all(k & 28 == bits for k in kinds), kinds
 
 
 def test_smaller_workspace_keeps_the_unrepacked_path(oracle_lib):
