@@ -260,9 +260,10 @@ def ws_schedule(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: i
                 workspace_bytes: int = None):
     """(status, kind, words): what sgemm_f32_ws runs for these arguments with a
     workspace of `workspace_bytes` (default: workspace_size_for these
-    operands): kind = schedule (bits 0-1) + 4 if A is repacked + 8 if B is
-    + 16 if A is transposed into its k-major copy; words = the leading
-    workspace words it zero-fills and leaves zero."""
+    operands; 0 gives what sgemm_f32 runs): kind = schedule (bits 0-1) + 4 if
+    A is repacked + 8 if B is + 16 if A is transposed into its k-major copy
+    + 32 for the cluster split of K, with its cluster size in bits 8-12;
+    words = the leading workspace words it zero-fills and leaves zero."""
     if workspace_bytes is None:
         workspace_bytes = workspace_size_for(M, N, K, A, lda, B, ldb)
     kind, words = ctypes.c_int(), ctypes.c_longlong()

@@ -1235,6 +1235,7 @@ struct DeviceInfo {
     int state;                    // 0 = not yet set up, 1 = ready, < 0 = status
     int sms;                      // multiprocessors
     int sk_per_sm[kVariants];     // co-resident stream-K CTAs per SM
+    int max_cluster;              // largest cluster of the cluster split of K (8 .. 16)
     unsigned long long ctx;       // id of the CUDA context the set-up was made in
 };
 std::mutex g_mutex;
@@ -1285,6 +1286,26 @@ int setup_device(int dev, DeviceInfo *out) {
                      cudaFuncSetAttribute(kCk[v], cudaFuncAttributePreferredSharedMemoryCarveout,
                                           cudaSharedmemCarveoutMaxShared) != cudaSuccess))
                     st = SGEMM_ERR_DEVICE;
+            // Clusters beyond the portable 8 CTAs, where the GPU can place them
+            // with this kernel's resources (at most 16): every variant opts in,
+            // and the largest size the runtime can schedule for one of them
+            // bounds all (they share block size and shared memory).
+            d.max_cluster = 8;
+            if (st == SGEMM_OK) {
+                bool nonportable = true;
+                for (int v = 0; v < kVariants; ++v)
+                    if (kCk[v] != nullptr &&
+                        cudaFuncSetAttribute(kCk[v], cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+                        nonportable = false;
+                int most = 0;
+                cudaLaunchConfig_t q = {};
+                q.gridDim = dim3(16 * 16);
+                q.blockDim = dim3(NT);
+                q.dynamicSmemBytes = SMEM_BYTES;
+                if (nonportable && cudaOccupancyMaxPotentialClusterSize(&most, kCk[kTmaVariant], &q) == cudaSuccess)
+                    d.max_cluster = most >= 16 ? 16 : (most > 8 ? most : 8);
+                (void)cudaGetLastError();
+            }
             // the one-CTA-per-tile kernels may be launched with the padded
             // request of the cta_per_sm=1 diagnostic
             for (int v = 0; v < kVariants && st == SGEMM_OK; ++v)
@@ -1570,30 +1591,43 @@ Plan effective_plan(long long T, long long KT, long long G, long long sms, bool 
 // most G / 2 tiles (the split then fills the GPU without a second wave), at
 // least 2 K tiles per CTA, on the 8 x 8 kernels (variant v).  S = the most
 // CTAs per tile that keep all of them resident, at most 8 (the portable
-// cluster size).
+// cluster size); at most max_cluster (16 where the GPU schedules clusters of
+// 16 of these CTAs) when T clusters of that size take at most a quarter of
+// the resident CTAs.  Measured on GB300 (us, clusters of at most 8 -> of at
+// most 16): 256 x 256 x 1024 (S = 16) 20.7 -> 16.9, 256 x 256 x 4096 52.0 ->
+// 33.2; but with more tiles larger clusters lost: 512^3 (16 tiles, S = 16)
+// 20.6 -> 25.0, 768 x 512 x 512 (S = 12) 22.6 -> 25.7, 1024 x 512 x 1024
+// (S = 9) 32.7 -> 41.4, 128 x 4096 x 4096 (S = 9) 90.2 -> 117.1.
 // When the multi-part stream-K schedule `sk` (kind 2, g CTAs) could run
 // instead, the split is taken only if it is expected to be faster.  Cost in
-// K tiles of one CTA (about 2.4 us each with two CTAs per SM), fitted to
-// GB300 timings of both schedules (1024^3, 1024 x 1024 x 2048 and x 4096,
-// 2048 x 1024 x 1024, 512 x 512 x 1024, 256 x 256 x 1024):
-//   cluster split: 4.7 + ceil(KT / S)  (launch, the two cluster barriers and
+// K tiles of one CTA with two CTAs per SM (about 2.4 us each); a grid that
+// fills at most half the SMs runs one CTA per SM, whose K tile costs 0.55 of
+// that.  Fitted to GB300 timings of both schedules:
+//   cluster split: 4.7 + ceil(KT / S) (launch, the two cluster barriers and
 //                  the sum over distributed shared memory);
-//   stream-K:      7.5 + T KT / g + 0.25 ceil(g / T)  (flag reset, hand-over
+//   stream-K:      7.5 + T KT / g + 0.3 ceil(g / T) (flag reset, hand-over
 //                  waits, and the owner's serial sum of ceil(g / T) parts).
-// E.g. 1024^3: 16 against 13.5 + 2.8 + 1.25 (split: 49.2 us, stream-K 53.1);
-// 512 x 512 x 1024: 8 against 4 + 2.8 + 4 (30.7 against 38.9 us);
-// 2048 x 1024 x 1024: 32 against 26.9 + 2.8 + 0.75 (88.3 against 83.9 us).
+// Measured, split against stream-K (us): 1024^3 49.7 / 53.1, 512 x 512 x
+// 1024 30.9 / 38.9, 384 x 384 x 2048 31.5 / 61.2, 256 x 256 x 4096 33.2 /
+// 101.7; stream-K faster at 2048 x 1024 x 1024 88.3 / 83.9, 1024 x 1024 x
+// 2048 88.1 / 86.0, 1024 x 1024 x 4096 165 / 149.5, 512 x 512 x 4096 88.4 /
+// 63.3.  The model picks the faster of the two at every one of these shapes.
 // SGEMM_F32_TUNE schedule=0..3 turns the split off.
-int cluster_split(long long T, long long KT, long long G, int v, const Plan *sk) {
+int cluster_split(long long T, long long KT, long long G, int v, const Plan *sk, int max_cluster) {
     if (v >= kAtVariant || kCk[v] == nullptr || tune().schedule >= 0 || T <= 0 || 2 * T > G) return 0;
     long long S = G / T;
-    if (S > 8) S = 8;
+    // clusters above the portable 8 only while all of them use at most a
+    // quarter of the resident CTAs (at most 4 tiles here)
+    const long long cap = 4 * T * max_cluster <= G ? max_cluster : 8;
+    if (S > cap) S = cap;
     if (S > KT / 2) S = KT / 2;
     if (S < 2) return 0;
     if (sk != nullptr && sk->grid > 0) {
         const double g = static_cast<double>(sk->grid);
-        const double split = static_cast<double>((KT + S - 1) / S);
-        const double streamk = static_cast<double>(T * KT) / g + 2.8 + 0.25 * static_cast<double>((sk->grid + T - 1) / T);
+        const double lone = 0.55;  // K tile of a CTA alone on its SM
+        const double split = 4.7 + static_cast<double>((KT + S - 1) / S) * (4 * T * S <= G ? lone : 1.0);
+        const double streamk = 7.5 + static_cast<double>(T * KT) / g * (4 * sk->grid <= G ? lone : 1.0) +
+                               0.3 * static_cast<double>((sk->grid + T - 1) / T);
         if (split > streamk) return 0;
     }
     return static_cast<int>(S);
@@ -1681,7 +1715,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     cfg.dynamicSmemBytes = smem_of(v);
     cfg.stream = stream;
     const bool streamk = flags != nullptr && pl.kind == 2 && flag_bytes >= pl.bytes;
-    if (const int S = cluster_split(T, KT, G, v, streamk ? &pl : nullptr)) {
+    if (const int S = cluster_split(T, KT, G, v, streamk ? &pl : nullptr, info.max_cluster)) {
         sg_nvtx::Range r("sgemm_f32: cluster split of K");
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -1882,8 +1916,8 @@ extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int ld
     const long long G = static_cast<long long>(info.sk_per_sm[v]) * info.sms;
     const int copies = (rp.a ? 4 : 0) | (rp.b ? 8 : 0) | (rp.at ? 16 : 0);
     const Plan pl = effective_plan(T, KT, G, info.sms, is_tma(v), avail);
-    if (K > 0 && cluster_split(T, KT, G, v, pl.kind == 2 ? &pl : nullptr)) {
-        *kind = 32 | copies;  // cluster split of K: no schedule words
+    if (const int S = K > 0 ? cluster_split(T, KT, G, v, pl.kind == 2 ? &pl : nullptr, info.max_cluster) : 0) {
+        *kind = 32 | copies | (S << 8);  // cluster split of K: no schedule words
         return SGEMM_OK;
     }
     *kind = pl.kind | copies;

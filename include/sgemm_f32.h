@@ -65,7 +65,9 @@ typedef enum {
  * Schedule: one CTA per 128 x 128 output tile; or, for products with at
  * most G / 2 tiles (G = 2 CTAs per SM) and at least 4 K tiles of 16, the
  * cluster split of K: each tile runs on a thread-block cluster of S CTAs
- * (S = min(G / tiles, 8, K tiles / 2)), CTA r summing K tiles
+ * (S = min(G / tiles, C, K tiles / 2), C = 8, the portable cluster size, or
+ * 16 for at most 4 tiles where the GPU can schedule clusters of 16 of these
+ * CTAs), CTA r summing K tiles
  * [KT r / S, KT (r+1) / S); the S partial tiles stay in shared memory and
  * are added in rank order over distributed shared memory, so the result does
  * not depend on timing.  Either way one kernel launch, no device memory.
@@ -118,8 +120,9 @@ int sgemm_f32(int M, int N, int K,
  * except over schedule 2 where a cost model fitted to GB300 timings expects
  * schedule 2 to be faster: the split costs its CTAs' K tiles plus about 4.7
  * K tiles of fixed cost; schedule 2 its CTAs' (fewer) K tiles plus about 7.5
- * and a quarter K tile per part of a tile (flag reset, hand-over waits, the
- * serial sum of the parts).  The split uses no workspace.
+ * and 0.3 K tile per part of a tile (flag reset, hand-over waits, the serial
+ * sum of the parts); a grid that fills at most half the SMs runs its K tiles
+ * about twice as fast per CTA.  The split uses no workspace.
  * sgemm_f32_workspace_size reports the bytes for the current device.  The
  * call zero-fills the words it uses at the start of the workspace on
  * `stream` before the kernels, so the workspace needs no preparation and its
@@ -166,7 +169,8 @@ int sgemm_f32_ws(int M, int N, int K,
  * with a workspace of workspace_bytes bytes (host-only; launches nothing):
  * *kind = the schedule (0 to 3, as listed above) in bits 0-1, plus 4 if A is
  * repacked, 8 if B is repacked, 16 if A is transposed into its k-major copy
- * and 32 for the cluster split of K (then bits 0-1 are 0 and *words is 0);
+ * and 32 for the cluster split of K (then bits 0-1 are 0, bits 8-12 hold
+ * the cluster size S and *words is 0);
  * with workspace_bytes = 0 it reports what sgemm_f32 runs.
  * *words = the 32-bit words at the start of
  * the workspace that the call zero-fills and leaves zero on success (flags

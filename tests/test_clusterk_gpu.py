@@ -1,12 +1,14 @@
 """The cluster split of K vs the FP64 oracle (needs a GB300).
 
 Products with at most G / 2 output tiles (G = 2 CTAs per SM) run each tile
-on a thread-block cluster of S CTAs (2 <= S <= 8), each CTA summing a slice
-of K, the slices added in rank order through distributed shared memory.
+on a thread-block cluster of S CTAs (2 <= S <= 16; above 8 where the GPU
+schedules such clusters), each CTA summing a slice of K, the slices added in
+rank order through distributed shared memory.
 sgemm_f32 (no workspace) takes it whenever it applies; sgemm_f32_ws takes it
 unless its cost model expects the multi-part split to be faster.
-sgemm_f32_ws_schedule reports it as bit 32 with no workspace words, and
-with a workspace of 0 bytes it reports what sgemm_f32 runs.
+sgemm_f32_ws_schedule reports it as bit 32 with S in bits 8 and up and no
+workspace words, and with a workspace of 0 bytes it reports what sgemm_f32
+runs.
 """
 import numpy as np
 import pytest
@@ -34,12 +36,26 @@ def _tiles(M, N):
     return ((M + 127) // 128) * ((N + 127) // 128)
 
 
+_PTRS = (1 << 36, 2 << 36, 3 << 36)  # host-only schedule queries: never dereferenced
+
+
+def _max_cluster():
+    """The largest cluster the library uses on this GPU (16 where the GPU
+    schedules clusters of 16 of its CTAs, else 8): the size it reports for a
+    single tile with a deep K."""
+    sst, kind, _ = sg.ws_schedule(128, 128, 4096, *_PTRS[:1], 4096, _PTRS[1], 128, _PTRS[2], 128, 0)
+    assert sst == 0 and kind & 32
+    return kind >> 8
+
+
 def _cluster_size(M, N, K):
     """S as the library picks it without a workspace: the most CTAs per tile
-    that keep all of them resident, at most 8 and at most half the 16-deep
-    K tiles."""
+    that keep all of them resident, at most half the 16-deep K tiles, and at
+    most 8, or the largest cluster when T such clusters take at most a
+    quarter of the resident CTAs."""
     G = 2 * torch.cuda.get_device_properties(0).multi_processor_count
-    return min(G // _tiles(M, N), 8, (K + 15) // 16 // 2)
+    T, big = _tiles(M, N), _max_cluster()
+    return min(G // T, big if 4 * T * big <= G else 8, (K + 15) // 16 // 2)
 
 
 def _run(M, N, K, A, lda, B, ldb, ldc, offs=(0, 0, 0), nbytes=0, ws_fill=7):
@@ -75,9 +91,11 @@ def _padding_untouched(raw, M, N, ldc, c_off):
     assert np.isnan(raw[mask]).all(), "C written outside its M x N elements"
 
 
-# Every cluster size S = 2 .. 8 (the row ranges of the final sum are uneven
-# for S = 3, 5, 6, 7), ragged M, N and K tiles, every copy-width class of A,
-# B and C (row strides and base offsets), and products smaller than a tile.
+# Cluster sizes S = 2 .. 16 (the row ranges of the final sum are uneven for
+# S not dividing 128; sizes above 8 for at most 4 tiles, where the GPU has
+# them, else these shapes run with 8), ragged M, N and K tiles, every
+# copy-width class of A, B and C (row strides and base offsets), and products
+# smaller than a tile.
 @pytest.mark.parametrize("M,N,K,lds,offs,S", [
     (1024, 2432, 64, None, (0, 0, 0), 2),            # 152 tiles, 2 K tiles per CTA
     (100, 12923, 96, None, (0, 0, 0), 3),            # 1 x 101 tiles
@@ -85,19 +103,25 @@ def _padding_untouched(raw, M, N, ldc, c_off):
     (700, 1250, 160, (161, 1250, 1251), (1, 0, 3), 5),  # A and C 4-byte aligned
     (600, 1280, 200, (202, 1282, 1280), (2, 2, 0), 6),  # A and B 8-byte aligned
     (128, 5504, 224, (224, 5505, 5506), (0, 1, 2), 7),  # B 4-byte, C 8-byte aligned
-    (256, 256, 256, None, (0, 0, 0), 8),             # 4 tiles
-    (77, 250, 999, (1001, 252, 260), (0, 0, 0), 8),  # ragged K tile, padded C rows
+    (256, 256, 256, None, (0, 0, 0), 8),             # 4 tiles, 16 K tiles
     (1000, 1030, 777, (777, 1030, 1030), (0, 0, 0), 4),  # misaligned rows, ragged K
+    (256, 200, 320, None, (0, 0, 0), 10),            # 4 tiles, 20 K tiles
+    (128, 500, 384, (385, 500, 500), (0, 0, 0), 12),  # 4 tiles, A 4-byte aligned
+    (200, 130, 448, None, (0, 0, 2), 14),            # 4 tiles, C 8-byte aligned
+    (256, 256, 1024, None, (0, 0, 0), 16),           # 4 tiles
+    (512, 512, 1024, None, (0, 0, 0), 8),            # 16 tiles: at most 8 above 4 tiles
+    (77, 250, 999, (1001, 252, 260), (0, 0, 0), 16),  # ragged K tile, padded C rows
     (3, 5, 100, (100, 5, 7), (0, 0, 1), 3),          # a few elements
-    (1, 100, 512, None, (0, 0, 0), 8),               # one row
+    (1, 100, 512, None, (0, 0, 0), 16),              # one row
 ])
 def test_cluster_split_full_check(oracle_lib, M, N, K, lds, offs, S):
     lda, ldb, ldc = lds or (K, N, N)
+    S = min(S, _max_cluster()) if S > 8 else S
     assert _cluster_size(M, N, K) == S
     A = synth.matrix(M, K, 71, 0, "normal", ld=lda, pad_value=np.nan)
     B = synth.matrix(K, N, 71, 1, "normal", ld=ldb, pad_value=np.nan)
     C, raw, _, kind, words = _run(M, N, K, A, lda, B, ldb, ldc, offs)
-    assert kind == 32 and words == 0, kind
+    assert kind == 32 | (S << 8) and words == 0, kind
     Cr, Sr = oracle_lib.gemm(A, B, M=M, N=N, K=K, lda=lda, ldb=ldb)
     tol.assert_close(C, Cr, Sr, K, f"cluster split S={S} {M}x{N}x{K}")
     _padding_untouched(raw, M, N, ldc, offs[2])
@@ -105,11 +129,11 @@ def test_cluster_split_full_check(oracle_lib, M, N, K, lds, offs, S):
     # kernel and slices, so the same result bit for bit, and the workspace
     # is not touched at all
     nbytes = sg.workspace_size(M, N, K)
-    fake = [(q + 1 << 36) + 4 * o for q, o in enumerate(offs)]  # apart, with the offsets' alignment
+    fake = [p + 4 * o for p, o in zip(_PTRS, offs)]  # apart, with the offsets' alignment
     _, wkind, _ = sg.ws_schedule(M, N, K, fake[0], lda, fake[1], ldb, fake[2], ldc, nbytes)
-    if wkind == 32:
+    if wkind & 32:
         C2, raw2, ws, kind2, _ = _run(M, N, K, A, lda, B, ldb, ldc, offs, nbytes=nbytes)
-        assert kind2 == 32
+        assert kind2 == kind
         assert np.all(ws == 7), "the cluster split uses no workspace"
         np.testing.assert_array_equal(C2.view(np.uint32), C.view(np.uint32))
 
@@ -122,7 +146,7 @@ def test_cluster_split_integer_exact_and_deterministic(oracle_lib):
     C = torch.empty(M, N, device="cuda")
     sst, kind, _ = sg.ws_schedule(M, N, K, tA.data_ptr(), K, tB.data_ptr(), N, C.data_ptr(), N,
                                   sg.workspace_size_for(M, N, K, tA.data_ptr(), K, tB.data_ptr(), N))
-    assert sst == 0 and kind == 32  # the torch wrapper's balanced call takes it too
+    assert sst == 0 and kind == 32 | (4 << 8)  # the torch wrapper's balanced call takes it too
     C1 = sg.sgemm(tA, tB)
     C2 = sg.sgemm(tA, tB, balanced=False)
     C3 = sg.sgemm(tA, tB)
@@ -138,7 +162,7 @@ def test_not_taken_where_it_does_not_apply():
     workspace for a multi-part split that keeps its CTAs busier: no cluster
     split."""
     G = 2 * torch.cuda.get_device_properties(0).multi_processor_count
-    pA, pB, pC = 1 << 36, 2 << 36, 3 << 36  # host-only query: never dereferenced
+    pA, pB, pC = _PTRS
     for M, N, K in [(128 * (G // 2 + 1), 128, 512),  # G / 2 + 1 tiles
                     (1024, 1024, 48),                # 3 K tiles: S would be 1
                     (1024, 1024, 0)]:                # K = 0: C is zeroed
@@ -151,4 +175,4 @@ def test_not_taken_where_it_does_not_apply():
     _, kind, _ = sg.ws_schedule(M, N, K, pA, K, pB, N, pC, N, sg.workspace_size(M, N, K))
     assert kind == 2
     _, kind, _ = sg.ws_schedule(M, N, K, pA, K, pB, N, pC, N, 0)
-    assert kind == 32
+    assert kind == 32 | (2 << 8)

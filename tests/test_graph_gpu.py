@@ -67,7 +67,7 @@ def _replay_matches_direct(oracle_lib, M, N, K, call, tA, tB, tC, seed, check_to
 @pytest.mark.parametrize("M,N,K,kind", [
     (2432, 2560, 300, 3),   # 380 tiles: whole waves plus the split-tail grid (programmatic launch)
     (2048, 1024, 1024, 2),  # 128 tiles: cooperative stream-K grid with partial-sum slots
-    (1024, 1024, 1024, 32),  # 64 tiles: cluster split of K, partial sums through distributed shared memory
+    (1024, 1024, 1024, 32 | (4 << 8)),  # 64 tiles: cluster split of K (S = 4) through distributed shared memory
 ])
 def test_balanced_schedules_in_a_graph(oracle_lib, M, N, K, kind):
     tA = torch.empty(M, K, device="cuda")
