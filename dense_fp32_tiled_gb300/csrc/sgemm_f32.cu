@@ -1217,7 +1217,8 @@ bool encode_maps(Maps &maps, int M, int N, int K, const float *A, int lda, const
     if (enc == nullptr) return false;
     const cuuint64_t a_dim[2] = {static_cast<cuuint64_t>(a_kmajor ? M : K), static_cast<cuuint64_t>(a_kmajor ? K : M)};
     const cuuint64_t a_stride[1] = {static_cast<cuuint64_t>(lda) * 4};
-    const cuuint32_t a_box[2] = {a_kmajor ? BM : BK, a_kmajor ? BK_AT : BM};
+    const cuuint32_t a_box[2] = {static_cast<cuuint32_t>(a_kmajor ? BM : BK),
+                                 static_cast<cuuint32_t>(a_kmajor ? BK_AT : BM)};
     const cuuint64_t b_dim[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
     const cuuint64_t b_stride[1] = {static_cast<cuuint64_t>(ldb) * 4};
     const cuuint32_t b_box[2] = {BN, a_kmajor ? static_cast<cuuint32_t>(BK_AT) : static_cast<cuuint32_t>(BK)};
@@ -1235,7 +1236,8 @@ struct DeviceInfo {
     int state;                    // 0 = not yet set up, 1 = ready, < 0 = status
     int sms;                      // multiprocessors
     int sk_per_sm[kVariants];     // co-resident stream-K CTAs per SM
-    int max_cluster;              // largest cluster of the cluster split of K (8 .. 16)
+    int max_cluster;              // largest cluster of the cluster split of K (0 = none, else 2 .. 16)
+    int active_clusters[17];      // clusters of S CTAs the GPU holds at once (index S, 2 .. 16)
     unsigned long long ctx;       // id of the CUDA context the set-up was made in
 };
 std::mutex g_mutex;
@@ -1286,25 +1288,39 @@ int setup_device(int dev, DeviceInfo *out) {
                      cudaFuncSetAttribute(kCk[v], cudaFuncAttributePreferredSharedMemoryCarveout,
                                           cudaSharedmemCarveoutMaxShared) != cudaSuccess))
                     st = SGEMM_ERR_DEVICE;
-            // Clusters beyond the portable 8 CTAs, where the GPU can place them
-            // with this kernel's resources (at most 16): every variant opts in,
-            // and the largest size the runtime can schedule for one of them
-            // bounds all (they share block size and shared memory).
-            d.max_cluster = 8;
+            // The cluster split of K: every variant opts in to clusters beyond
+            // the portable 8 CTAs, and the runtime reports, for each size S up
+            // to 16, how many clusters of S of these CTAs the GPU holds at once
+            // (a cluster must fit in one GPC, so this can be fewer than G / S).
+            // All variants share block size and shared memory, so one variant's
+            // figures stand for all.  Sizes it cannot place are not used.
+            d.max_cluster = 0;
+            for (int S = 0; S <= 16; ++S) d.active_clusters[S] = 0;
             if (st == SGEMM_OK) {
                 bool nonportable = true;
                 for (int v = 0; v < kVariants; ++v)
                     if (kCk[v] != nullptr &&
                         cudaFuncSetAttribute(kCk[v], cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
                         nonportable = false;
-                int most = 0;
-                cudaLaunchConfig_t q = {};
-                q.gridDim = dim3(16 * 16);
-                q.blockDim = dim3(NT);
-                q.dynamicSmemBytes = SMEM_BYTES;
-                if (nonportable && cudaOccupancyMaxPotentialClusterSize(&most, kCk[kTmaVariant], &q) == cudaSuccess)
-                    d.max_cluster = most >= 16 ? 16 : (most > 8 ? most : 8);
-                (void)cudaGetLastError();
+                for (int S = 2; S <= (nonportable ? 16 : 8); ++S) {
+                    cudaLaunchAttribute attr;
+                    attr.id = cudaLaunchAttributeClusterDimension;
+                    attr.val.clusterDim.x = static_cast<unsigned>(S);
+                    attr.val.clusterDim.y = 1;
+                    attr.val.clusterDim.z = 1;
+                    cudaLaunchConfig_t q = {};
+                    q.gridDim = dim3(static_cast<unsigned>(S) * 64u);
+                    q.blockDim = dim3(NT);
+                    q.dynamicSmemBytes = SMEM_BYTES;
+                    q.attrs = &attr;
+                    q.numAttrs = 1;
+                    int n = 0;
+                    if (cudaOccupancyMaxActiveClusters(&n, kCk[kTmaVariant], &q) == cudaSuccess && n > 0) {
+                        d.active_clusters[S] = n;
+                        d.max_cluster = S;
+                    }
+                    (void)cudaGetLastError();
+                }
             }
             // the one-CTA-per-tile kernels may be launched with the padded
             // request of the cta_per_sm=1 diagnostic
@@ -1590,10 +1606,11 @@ Plan effective_plan(long long T, long long KT, long long G, long long sms, bool 
 // with G CTAs resident at once, or 0 when it does not apply: products with at
 // most G / 2 tiles (the split then fills the GPU without a second wave), at
 // least 2 K tiles per CTA, on the 8 x 8 kernels (variant v).  S = the most
-// CTAs per tile that keep all of them resident, at most 8 (the portable
-// cluster size); at most max_cluster (16 where the GPU schedules clusters of
-// 16 of these CTAs) when T clusters of that size take at most a quarter of
-// the resident CTAs.  Measured on GB300 (us, clusters of at most 8 -> of at
+// CTAs per tile that keep all T clusters resident at once (at most G / T, and
+// T at most the clusters of S the GPU holds at once: a cluster must fit in
+// one GPC), at most 8 (the portable cluster size), or at most the largest
+// size the GPU places (16 on GB300) when T clusters of it take at most a
+// quarter of the resident CTAs.  Measured on GB300 (us, clusters of at most 8 -> of at
 // most 16): 256 x 256 x 1024 (S = 16) 20.7 -> 16.9, 256 x 256 x 4096 52.0 ->
 // 33.2; but with more tiles larger clusters lost: 512^3 (16 tiles, S = 16)
 // 20.6 -> 25.0, 768 x 512 x 512 (S = 12) 22.6 -> 25.7, 1024 x 512 x 1024
@@ -1613,14 +1630,13 @@ Plan effective_plan(long long T, long long KT, long long G, long long sms, bool 
 // 2048 88.1 / 86.0, 1024 x 1024 x 4096 165 / 149.5, 512 x 512 x 4096 88.4 /
 // 63.3.  The model picks the faster of the two at every one of these shapes.
 // SGEMM_F32_TUNE schedule=0..3 turns the split off.
-int cluster_split(long long T, long long KT, long long G, int v, const Plan *sk, int max_cluster) {
+int cluster_split(long long T, long long KT, long long G, int v, const Plan *sk, const DeviceInfo &info) {
     if (v >= kAtVariant || kCk[v] == nullptr || tune().schedule >= 0 || T <= 0 || 2 * T > G) return 0;
-    long long S = G / T;
     // clusters above the portable 8 only while all of them use at most a
     // quarter of the resident CTAs (at most 4 tiles here)
-    const long long cap = 4 * T * max_cluster <= G ? max_cluster : 8;
-    if (S > cap) S = cap;
-    if (S > KT / 2) S = KT / 2;
+    const long long cap = 4 * T * info.max_cluster <= G ? info.max_cluster : (info.max_cluster < 8 ? info.max_cluster : 8);
+    long long S = cap < KT / 2 ? cap : KT / 2;
+    while (S >= 2 && (T * S > G || T > info.active_clusters[S])) --S;  // one wave of clusters
     if (S < 2) return 0;
     if (sk != nullptr && sk->grid > 0) {
         const double g = static_cast<double>(sk->grid);
@@ -1715,7 +1731,7 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
     cfg.dynamicSmemBytes = smem_of(v);
     cfg.stream = stream;
     const bool streamk = flags != nullptr && pl.kind == 2 && flag_bytes >= pl.bytes;
-    if (const int S = cluster_split(T, KT, G, v, streamk ? &pl : nullptr, info.max_cluster)) {
+    if (const int S = cluster_split(T, KT, G, v, streamk ? &pl : nullptr, info)) {
         sg_nvtx::Range r("sgemm_f32: cluster split of K");
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -1916,7 +1932,7 @@ extern "C" int sgemm_f32_ws_schedule(int M, int N, int K, const float *A, int ld
     const long long G = static_cast<long long>(info.sk_per_sm[v]) * info.sms;
     const int copies = (rp.a ? 4 : 0) | (rp.b ? 8 : 0) | (rp.at ? 16 : 0);
     const Plan pl = effective_plan(T, KT, G, info.sms, is_tma(v), avail);
-    if (const int S = K > 0 ? cluster_split(T, KT, G, v, pl.kind == 2 ? &pl : nullptr, info.max_cluster) : 0) {
+    if (const int S = K > 0 ? cluster_split(T, KT, G, v, pl.kind == 2 ? &pl : nullptr, info) : 0) {
         *kind = 32 | copies | (S << 8);  // cluster split of K: no schedule words
         return SGEMM_OK;
     }
