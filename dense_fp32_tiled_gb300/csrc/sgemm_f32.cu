@@ -1114,6 +1114,10 @@ int bk_of(int v) { return v == kAtVariant ? BK_AT : BK; }
 //   schedule = 0 | 1 | 2 | 3 : the schedule of sgemm_f32_ws when the
 //              workspace has room for it (3 needs tensor copies);
 //   parts    = 2 .. 16 : K parts of each split-tail tile;
+//   cluster  = 2 .. 16 | off : the cluster size of the cluster split of K
+//              wherever that size fits (T clusters resident at once, at
+//              least 2 K tiles per CTA), whatever the cost model says, or
+//              no cluster split;
 //   drain    = on : a diagnostic: the one-CTA-per-tile grid of the k-major
 //              kernels keeps one tile in flight and issues
 //              it only after the k steps of the one before, so no copy
@@ -1130,6 +1134,7 @@ struct Tune {
     int kernels = -1;   // -1 auto, 0 rowmajor8, 1 kmajor16
     int schedule = -1;
     int parts = -1;
+    int cluster = -1;   // -1 auto, 0 off, 2 .. 16 forced
     bool drain = false; // the drained-ring diagnostic kernels
     bool one_cta = false; // one CTA per SM in the one-CTA-per-tile grid (diagnostic)
 };
@@ -1160,6 +1165,8 @@ const Tune &tune() {
                 t.schedule = (val[0] >= '0' && val[0] <= '3' && val[1] == 0) ? static_cast<int>(num) : -1;
             } else if (!strcmp(key, "parts")) {
                 t.parts = (num >= 2 && num <= 16) ? static_cast<int>(num) : -1;
+            } else if (!strcmp(key, "cluster")) {
+                t.cluster = !strcmp(val, "off") ? 0 : (num >= 2 && num <= 16) ? static_cast<int>(num) : -1;
             } else if (!strcmp(key, "drain")) {
                 t.drain = !strcmp(val, "on");
             } else if (!strcmp(key, "cta_per_sm")) {
@@ -1629,9 +1636,15 @@ Plan effective_plan(long long T, long long KT, long long G, long long sms, bool 
 // 101.7; stream-K faster at 2048 x 1024 x 1024 88.3 / 83.9, 1024 x 1024 x
 // 2048 88.1 / 86.0, 1024 x 1024 x 4096 165 / 149.5, 512 x 512 x 4096 88.4 /
 // 63.3.  The model picks the faster of the two at every one of these shapes.
-// SGEMM_F32_TUNE schedule=0..3 turns the split off.
+// SGEMM_F32_TUNE schedule=0..3 or cluster=off turns the split off; cluster=S
+// forces its size where it fits.
 int cluster_split(long long T, long long KT, long long G, int v, const Plan *sk, const DeviceInfo &info) {
-    if (v >= kAtVariant || kCk[v] == nullptr || tune().schedule >= 0 || T <= 0 || 2 * T > G) return 0;
+    if (v >= kAtVariant || kCk[v] == nullptr || tune().schedule >= 0 || tune().cluster == 0 || T <= 0 || 2 * T > G)
+        return 0;
+    if (const int forced = tune().cluster; forced >= 2)
+        return forced <= info.max_cluster && forced <= KT / 2 && T * forced <= G && T <= info.active_clusters[forced]
+                   ? forced
+                   : 0;
     // clusters above the portable 8 only while all of them use at most a
     // quarter of the resident CTAs (at most 4 tiles here)
     const long long cap = 4 * T * info.max_cluster <= G ? info.max_cluster : (info.max_cluster < 8 ? info.max_cluster : 8);

@@ -178,3 +178,55 @@ def test_not_taken_where_it_does_not_apply():
     assert kind == 2
     _, kind, _ = sg.ws_schedule(M, N, K, pA, K, pB, N, pC, N, 0)
     assert kind == 32 | (2 << 8)  # S = 2: 128 clusters of 2
+
+
+_FORCED_CHILD = r"""
+import sys, json
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import dense_fp32_tiled_gb300 as sg
+from dense_fp32_tiled_gb300 import synth
+import oracle
+from tests import _tolerance as tol
+from tests._gpu import dev_buffer
+sg.load_library()
+oracle.build()
+out = []
+for (M, N, K) in json.loads(sys.argv[2]):
+    A = synth.matrix(M, K, 74, 0, "normal")
+    B = synth.matrix(K, N, 74, 1, "normal")
+    tA, pA = dev_buffer(A)
+    tB, pB = dev_buffer(B)
+    tC = torch.full((M * N + 4,), float("nan"), device="cuda")
+    _, kind, _ = sg.ws_schedule(M, N, K, pA, K, pB, N, tC.data_ptr(), N, 0)
+    assert sg.sgemm_f32(M, N, K, pA, K, pB, N, tC.data_ptr(), N, torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    Cr, Sr = oracle.gemm(A, B)
+    tol.assert_close(tC.cpu().numpy()[:M * N].reshape(M, N), Cr, Sr, K, f"forced cluster {M}x{N}x{K}")
+    out.append(kind)
+print(json.dumps(out))
+"""
+
+
+@pytest.mark.parametrize("tune", ["cluster=off", "cluster=3", "cluster=9", "cluster=13"])
+def test_forced_cluster_size(tune):
+    """SGEMM_F32_TUNE (read once per process, so in a child process) forces
+    the cluster size, or turns the split off, on shapes where the default
+    picks another: 4 and 12 tiles (S 9 and 13 need clusters of more than 8,
+    which the GPU may not schedule; then no split runs)."""
+    import json, os, subprocess, sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    shapes = [(256, 256, 1024), (384, 512, 768)]
+    r = subprocess.run([sys.executable, "-c", _FORCED_CHILD, root, json.dumps(shapes)], cwd=root,
+                       env=dict(os.environ, SGEMM_F32_TUNE=tune), capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    kinds = json.loads(r.stdout.strip().splitlines()[-1])
+    want = tune.split("=")[1]
+    for k in kinds:
+        if want == "off":
+            assert k & 32 == 0, kinds
+        elif int(want) <= 8 or _max_cluster() >= int(want):
+            assert k & 255 == 32 and k >> 8 == int(want), kinds
+        else:
+            assert k & 32 == 0, kinds
+
