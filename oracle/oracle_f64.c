@@ -7,7 +7,7 @@
  * check and the benchmark's CPU-baseline leg do.  It shares no code, header
  * or constant with the CUDA library.
  *
- * Sources (the surveyed web pages):
+ * Sources (the web pages this follows):
  *  - "CUDA 深入浅出（五）: Vectorized Load 和 Shared Memory Layout"
  *    (csh0101.cc), section "这一篇放进 GEMM 路径里看": the product is the
  *    textbook C = A x B; the tiled kernel only reorders data movement.
