@@ -1,6 +1,7 @@
-"""The C-ABI entry points captured in a CUDA graph and replayed (needs a GB300).
+"""sgemm_f32, sgemm_f32_ws, sgemm_f32_host and sgemm_f32_3xtf32 captured in a
+CUDA graph and replayed (needs a GB300).
 
-Every entry point only enqueues work on the caller's stream (kernel launches,
+Each of them only enqueues work on the caller's stream (kernel launches,
 memsets, and for the host-buffer path copies on two internal streams joined by
 events), so a stream capture records the whole call.  After a first call
 outside the capture (the per-device set-up runs once), a replayed graph must
@@ -104,7 +105,7 @@ def test_kmajor_copy_in_a_graph(oracle_lib):
     _replay_matches_direct(oracle_lib, M, N, K, call, tA, tB, tC, 321)
 
 
-def test_allocation_free_entry_in_a_graph(oracle_lib):
+def test_no_workspace_entry_in_a_graph(oracle_lib):
     M, N, K = 300, 262, 190
     tA = torch.empty(M, K, device="cuda")
     tB = torch.empty(K, N, device="cuda")
