@@ -267,14 +267,17 @@ size_t sgemm_f32_host_workspace_size(int M, int N, int K);
  * tiles (ceil(M/128) * ceil(N/128); e.g. M = N = 16256 fits, 16384 does not)
  * are rejected with SGEMM_ERR_SCRATCH_LIMIT before anything is launched.
  *
+ * Small products that take the cluster split of K (see sgemm_f32) use none
+ * of it.
+ *
  * The first call on each device looks up the array's device address (with
- * that device current) and keeps it; make that first call before any stream
- * capture begins.  The address belongs to the CUDA context it was looked up
- * in: a call made in a new context of the device (after cudaDeviceReset, for
- * instance) looks it up again.  Every call shares the one array, which keeps whatever the
- * last call left there: each call zero-fills the words it uses on `stream`
- * before its kernel, and calls that overlap on the GPU (different streams,
- * or different host threads) race on the array and must not be issued.
+ * that device current) and keeps it, so it costs more than later calls.  The
+ * address belongs to the CUDA context it was looked up in: a call made in a
+ * new context of the device (after cudaDeviceReset, for instance) looks it up
+ * again.  Every call shares the one array, which keeps whatever the last call
+ * left there: each call zero-fills the words it uses on `stream` before its
+ * kernel, and calls that overlap on the GPU (different streams, or different
+ * host threads) race on the array and must not be issued.
  */
 int sgemm_f32_static_scratch(int M, int N, int K,
                              const float *A, int lda,
