@@ -41,17 +41,36 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 // 4 floats), so the products always run on the tensor-copy kernels.
 long long pad4(long long n) { return (n + 3) / 4 * 4; }
 
-// Row panels: up to kMaxPanels panels of `rows` rows (the last may be
-// shorter); with several panels, a last panel of at least 512 rows is cut in
-// two (on the 128-row tile), so that the copy back of the last panel of C,
-// which nothing hides, is half as long.  Panel p holds rows [start[p],
-// start[p + 1]).
+// Row panels, panel p holding rows [start[p], start[p + 1]).
+//   Wide products (N >= 2048, M >= 3 kPanelRows): a first panel of
+//   kPanelRows rows, one panel up to the last 512 rows, and a last panel of
+//   512 rows.  The product of a row of A takes several times longer than its
+//   copy here (the ratio grows with N), so the middle panel's rows have
+//   landed before the first panel's product ends, and one large product runs
+//   on the whole-wave schedules instead of several panel products of fewer
+//   tiles than the GPU holds at once.  Measured on GB300 against the plan
+//   below (TFLOP/s, pinned buffers): 4096^3 56.6 -> 58.8, 8192^3 68.0 ->
+//   69.2, 4096 x 2048 x 4096 49.2 -> 50.6; first / last panels of 768 / 512,
+//   1280 / 512, 1024 / 256 and 1024 / 1024 rows did no better overall.
+//   Otherwise: up to kMaxPanels panels of `rows` rows (the last may be
+//   shorter); with several panels, a last panel of at least 512 rows is cut
+//   in two (on the 128-row tile), so that the copy back of the last panel of
+//   C, which nothing hides, is half as long.
 struct Panels {
     int P;
     int start[kMaxPanels + 2];
     int rows(int p) const { return start[p + 1] - start[p]; }
 };
-Panels panels_of(int M) {
+Panels panels_of(int M, int N) {
+    if (N >= 2048 && M >= 3 * kPanelRows) {
+        Panels pn;
+        pn.start[0] = 0;
+        pn.start[1] = kPanelRows;
+        pn.start[2] = M - 512;
+        pn.start[3] = M;
+        pn.P = 3;
+        return pn;
+    }
     int P = M / kPanelRows;
     P = P < 1 ? 1 : (P > kMaxPanels ? kMaxPanels : P);
     int rows = (M + P - 1) / P;
@@ -84,7 +103,7 @@ struct HostLayout {
     size_t b, a, c, ws, ws_bytes, bytes;
 };
 HostLayout host_layout(int M, int N, int K) {
-    const Panels pn = panels_of(M);
+    const Panels pn = panels_of(M, N);
     HostLayout l;
     l.b = 0;
     l.a = round256(static_cast<size_t>(K) * pad4(N) * 4);
@@ -188,7 +207,7 @@ extern "C" int sgemm_f32_host(int M, int N, int K, const float *A, int lda, cons
     float *dA = reinterpret_cast<float *>(ws + l.a);
     float *dC = reinterpret_cast<float *>(ws + l.c);
     void *dW = ws + l.ws;
-    const Panels pn = panels_of(M);
+    const Panels pn = panels_of(M, N);
     const int P = pn.P;
     const int NB = col_blocks(P, N);
     const int K4 = static_cast<int>(pad4(K)), N4 = static_cast<int>(pad4(N));  // fit: checked above

@@ -207,11 +207,14 @@ size_t sgemm_f32_workspace_size_for(int M, int N, int K,
 /*
  * sgemm_f32_host -- the same product for operands in HOST memory: copies A
  * and B to the device, multiplies with sgemm_f32_ws, and copies C back.
- * A goes in row panels of about 1024 rows (at most 4, the last one cut in two
- * when it has at least 512 rows), B after the first panel, and each panel's product starts as soon as that panel and B have
- * landed; with several panels and N >= 512 the first panel's product runs in
- * column blocks of B (4 when N >= 1024, else 2), each while the next block of
- * B is still copying.
+ * A goes in row panels: for wide products (N >= 2048, M >= 3072) a first
+ * panel of 1024 rows, one panel up to the last 512 rows and a last panel of
+ * 512 rows; otherwise panels of about 1024 rows (at most 4, the last one cut
+ * in two when it has at least 512 rows).  B goes after the first panel, and
+ * each panel's product starts as soon as that panel and B have landed; with
+ * several panels and N >= 512 the first panel's product runs in column
+ * blocks of B (4 when N >= 1024, else 2), each while the next block of B is
+ * still copying.
  * Each finished panel of C is copied back while the next one computes.  The
  * copies run on two internal non-blocking streams (created once per device),
  * the products on `stream`.  The pages have no counterpart: this entry point

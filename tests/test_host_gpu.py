@@ -35,13 +35,14 @@ def test_pageable_strided_ragged(oracle_lib):
 
 
 @pytest.mark.parametrize("M,N,K", [(4100, 300, 200), (2048, 512, 1024), (129, 7, 3), (2500, 1030, 333),
-                                   (3000, 700, 64)])
+                                   (3000, 700, 64), (3200, 2100, 96)])
 def test_pinned_integer_exact(oracle_lib, M, N, K):
     """Pinned buffers across one to four row panels; integer inputs make every
     partial sum exact, so C must equal the oracle bit for bit.  With several
     panels and N >= 512 the first panel is computed in column blocks of B
     (2048x512: 256 + 256; 2500x1030: 256 + 256 + 256 + 262, rows not 16-byte
-    aligned; 3000x700: 256 + 444)."""
+    aligned; 3000x700: 256 + 444).  3200x2100 is wide: panels of 1024, 1664
+    and 512 rows, the first in column blocks of 512 + 512 + 512 + 564."""
     A = torch.from_numpy(synth.matrix(M, K, 93, 0, "int5")).pin_memory()
     B = torch.from_numpy(synth.matrix(K, N, 93, 1, "int5")).pin_memory()
     C = sg.sgemm_host(A, B)
