@@ -112,6 +112,8 @@ def _padding_untouched(raw, M, N, ldc, c_off):
     (256, 256, 1024, None, (0, 0, 0), 16),           # 4 tiles
     (512, 512, 1024, None, (0, 0, 0), 8),            # 16 tiles: at most 8 above 4 tiles
     (77, 250, 999, (1001, 252, 260), (0, 0, 0), 16),  # ragged K tile, padded C rows
+    (300, 600, 400, (400, 602, 600), (0, 0, 0), 8),  # A 16-byte, B 8-byte aligned
+    (200, 300, 500, (501, 301, 300), (0, 0, 0), 8),  # A and B 4-byte aligned
     (3, 5, 100, (100, 5, 7), (0, 0, 1), 3),          # a few elements
     (1, 100, 512, None, (0, 0, 0), 16),              # one row
 ])
