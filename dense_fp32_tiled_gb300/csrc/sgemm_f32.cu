@@ -744,7 +744,11 @@ __device__ __forceinline__ void raise_flag(unsigned *flag) {
 // The segments of one CTA of the stream-K schedules (below): first whole
 // data-parallel tiles (tile c, c + G, ...), then its share of the (tile,
 // K tile) iterations of the remaining tiles, cut at tile boundaries.  K tiles
-// are bk deep (BK, or BK_AT for the k-major kernels).
+// are bk deep (BK, or BK_AT for the k-major kernels).  The walk lives in
+// shared memory, one per CTA, and only thread 0 advances it, between the
+// barriers that already separate segments: in registers its 64-bit positions
+// would stay live through the K loop, where the 8 x 8 kernels have none to
+// spare.
 struct SkWalk {
     long long it, it_end;  // this CTA's stream-K iterations not yet taken: [it, it_end)
     int dp_lin;            // its next data-parallel tile
@@ -1754,11 +1758,13 @@ int run(int M, int N, int K, const float *A, int lda, const float *B, int ldb, f
         cfg.gridDim = dim3(static_cast<unsigned>(T * S));
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, kCk[v], p, maps) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return SGEMM_ERR_LAUNCH;
-        }
-        return SGEMM_OK;
+        if (cudaLaunchKernelEx(&cfg, kCk[v], p, maps) == cudaSuccess) return SGEMM_OK;
+        // The runtime refused the clusters (e.g. a process granted fewer SMs
+        // than the set-up's occupancy figures assume): run the schedule the
+        // call would run without the split.
+        (void)cudaGetLastError();
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
     }
     if (pl.kind == 3) {
         if (flags != nullptr && flag_bytes >= pl.bytes) {

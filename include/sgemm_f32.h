@@ -70,7 +70,9 @@ typedef enum {
  * CTAs), CTA r summing K tiles
  * [KT r / S, KT (r+1) / S); the S partial tiles stay in shared memory and
  * are added in rank order over distributed shared memory, so the result does
- * not depend on timing.  Either way one kernel launch, no device memory.
+ * not depend on timing.  Either way one kernel launch, no device memory.  If
+ * the runtime refuses the cluster launch, the call runs one CTA per tile
+ * instead (sgemm_f32_ws: the schedule it would run without the split).
  *
  * Edge cases: M == 0 or N == 0 returns SGEMM_OK without launching anything.
  * K == 0 sets C to zero (the empty sum); A and B may then be NULL.
