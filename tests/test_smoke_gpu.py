@@ -1,6 +1,6 @@
-"""The round-trip smoke check (__graft_entry__.smoke) as a GPU test, so that a
-change in the dispatch rules its shapes rely on fails here too (needs a
-GB300)."""
+"""The smoke check (__graft_entry__.smoke: a small product on each path,
+checked against the oracle) as a GPU test, so that a change in the dispatch
+rules its shapes rely on fails here too (needs a GB300)."""
 import os
 import sys
 
