@@ -1,8 +1,8 @@
 """Seeded random shapes, leading dimensions and base offsets through every
 schedule of sgemm_f32_ws (every other case with room to copy unaligned
 operands: an unaligned A into its k-major copy, an unaligned B into aligned
-rows) and through the 3xTF32 variant, against the FP64 oracle (needs a
-GB300).
+rows), through sgemm_f32 and sgemm_f32_static_scratch, and through the 3xTF32
+variant, against the FP64 oracle (needs a GB300).
 
 Shapes are drawn log-uniformly so that small products (one CTA per tile,
 multi-part split, cluster split of K), products with a partial last wave
@@ -93,6 +93,18 @@ def test_random_shapes_every_schedule(oracle_lib):
         raw = tC.cpu().numpy()[oc:oc + c_elems]
         C = np.stack([raw[r * ldc:r * ldc + N] for r in range(M)])
         _check(oracle_lib, A, B, C, M, N, K, lda, ldb, what, 500 + i)
+        # the entry points without a workspace on the same operands: sgemm_f32
+        # (one CTA per tile or the cluster split of K) and, every other case,
+        # sgemm_f32_static_scratch (its fixed scratch for the flags)
+        for name, fn in (("sgemm_f32", sg.sgemm_f32), ("static scratch", sg.sgemm_f32_static_scratch)):
+            if name == "static scratch" and i % 2:
+                continue
+            tC.fill_(float("nan"))
+            assert fn(M, N, K, pA, lda, pB, ldb, pC, ldc, s) == 0, what
+            torch.cuda.synchronize()
+            raw = tC.cpu().numpy()[oc:oc + c_elems]
+            C = np.stack([raw[r * ldc:r * ldc + N] for r in range(M)])
+            _check(oracle_lib, A, B, C, M, N, K, lda, ldb, f"{name} " + what, 500 + i)
         if i % 3 == 0:  # the tensor-core variant on the same operands
             tbytes = sg.tc_workspace_size(M, N, K)
             tws = torch.empty(max(tbytes, 256) + 256, dtype=torch.uint8, device="cuda")
